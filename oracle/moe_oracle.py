@@ -1,0 +1,339 @@
+"""Plain, slow, fp64 reference of the MoE expert layer.  TEST INFRASTRUCTURE ONLY.
+
+What the layer computes, as the pages describe it:
+
+* Each token is routed to k of E experts with a routing weight; tokens are grouped by expert
+  (per-expert counts, group offsets, a token reorder), every expert runs its own small matrix
+  product on its group, and the expert outputs are aggregated back per token by routing weight
+  (kongchang.com, "Prime Intellect推出Prime Mega MoE", section "为什么 MoE 训练特别需要融合内核",
+  the grouped-GEMM explainer).
+* The fused layer is expert-parallel dispatch, the two expert linear layers, SwiGLU, and combine
+  (MarkTechPost, "Prime Intellect Releases Prime Mega MoE", section "How does the fused kernel
+  work?").  The experts are gated and carry no bias (ic.work analysis, section
+  "算子下沉时代的硬件死锁暗礁").  With every expert on one device, dispatch is a gather of token
+  rows into expert order and combine is the weighted sum back to token order.
+* Training needs the backward of the same layer, activation and weight gradients (MarkTechPost,
+  "How does the fused kernel work?"; ic.work, section "从 3.11 倍到 1.32 倍的性能漏斗").
+
+Readings where the pages are silent (each is also listed with the design notes):
+  W13 is [E, 2I, H] with rows [0, I) the gate projection and rows [I, 2I) the up projection;
+  SwiGLU is silu(g) * u with silu(z) = z * sigmoid(z), no clamp; the routing weight multiplies
+  the expert output (after the down projection); the token reorder is stable by slot index
+  s = t*k + j; the backward is that of the loss <dy, y>.
+
+MXFP8 (OCP Microscaling v1.0, E4M3 elements, one E8M0 scale per 32 elements along the
+contraction axis): the oracle quantises and dequantises each GEMM operand at the point where the
+CUDA path feeds the block-scaled MMA, then computes in fp64.  The shared exponent of a block is
+floor(log2(amax)) - 8 (8 is the largest E4M3 exponent); elements are divided by 2^exp, rounded to
+the nearest E4M3 value (ties to even) and saturated to +-448.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "route", "permute_rows", "unpermute_sum", "sigmoid", "silu",
+    "e4m3_round", "mx_block_exponent", "mx_qdq", "mx_qdq_segments",
+    "forward", "backward", "forward_tokens", "backward_tokens", "wgrad_experts",
+]
+
+
+# ----------------------------------------------------------------------------------------------
+# routing bookkeeping: per-expert counts, group offsets, stable token reorder and its inverse
+# ----------------------------------------------------------------------------------------------
+def route(topk_idx: np.ndarray, E: int) -> dict:
+    """Group the T*k slots by expert (counting sort, stable in slot order s = t*k + j).
+
+    Returns cnt[E] (tokens per expert), off[E+1] (exclusive prefix of cnt: the group offsets),
+    perm[S] (perm[p] = slot at sorted position p) and inv[S] (inv[perm[p]] = p).
+    """
+    flat = np.asarray(topk_idx).reshape(-1).astype(np.int64)
+    S = flat.size
+    if S and (flat.min() < 0 or flat.max() >= E):
+        raise ValueError("expert id out of range")
+    cnt = np.zeros(E, dtype=np.int64)
+    for e in flat:
+        cnt[e] += 1
+    off = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        off[e + 1] = off[e] + cnt[e]
+    perm = np.empty(S, dtype=np.int64)
+    fill = off[:E].copy()
+    for s in range(S):                       # walking slots in order keeps ties in slot order
+        e = flat[s]
+        perm[fill[e]] = s
+        fill[e] += 1
+    inv = np.empty(S, dtype=np.int64)
+    inv[perm] = np.arange(S, dtype=np.int64)
+    return {"cnt": cnt, "off": off, "perm": perm, "inv": inv}
+
+
+def permute_rows(x: np.ndarray, perm: np.ndarray, k: int) -> np.ndarray:
+    """Dispatch: row p of the result is the token of slot perm[p]."""
+    return x[perm // k]
+
+
+def unpermute_sum(rows: np.ndarray, inv: np.ndarray, T: int, k: int, weights=None) -> np.ndarray:
+    """Combine: out[t] = sum_j weights[t, j] * rows[inv[t*k + j]] (unweighted if weights is None)."""
+    out = np.zeros((T,) + rows.shape[1:], dtype=np.float64)
+    for j in range(k):
+        r = rows[inv[np.arange(T) * k + j]]
+        out += r if weights is None else weights[:, j:j + 1] * r
+    return out
+
+
+def sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def silu(z):
+    return z * sigmoid(z)
+
+
+# ----------------------------------------------------------------------------------------------
+# MXFP8: E4M3 elements with one E8M0 power-of-two scale per block of 32
+# ----------------------------------------------------------------------------------------------
+E4M3_MAX = 448.0
+E4M3_EMAX = 8          # exponent of the largest normal E4M3 value (448 = 1.75 * 2^8)
+E4M3_EMIN = -6         # exponent of the smallest normal; subnormal spacing is 2^-9
+MX_BLOCK = 32
+
+
+def e4m3_round(v: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 value (3 mantissa bits, ties to even), saturated to +-448."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)                      # a = m * 2^ex with m in [0.5, 1)
+    e = np.maximum(ex - 1, E4M3_EMIN)        # binade exponent, floored at the subnormal range
+    step = np.ldexp(1.0, e - 3)
+    q = np.minimum(np.round(a / step) * step, E4M3_MAX)
+    return np.copysign(q, v)
+
+
+def mx_block_exponent(amax: np.ndarray) -> np.ndarray:
+    """Shared block exponent floor(log2(amax)) - 8, clamped to the E8M0 range; -127 for amax = 0."""
+    amax = np.asarray(amax, dtype=np.float64)
+    _, ex = np.frexp(amax)
+    se = (ex - 1) - E4M3_EMAX
+    se = np.clip(se, -127, 127)
+    return np.where(amax > 0, se, -127).astype(np.int64)
+
+
+def _qdq_last_axis(a: np.ndarray) -> np.ndarray:
+    n = a.shape[-1]
+    nb = -(-n // MX_BLOCK)
+    pad = nb * MX_BLOCK - n
+    if pad:
+        a = np.concatenate([a, np.zeros(a.shape[:-1] + (pad,))], axis=-1)
+    b = a.reshape(a.shape[:-1] + (nb, MX_BLOCK))
+    se = mx_block_exponent(np.abs(b).max(axis=-1))[..., None]
+    scale = np.ldexp(1.0, se)
+    q = e4m3_round(b / scale) * scale
+    q = q.reshape(a.shape)
+    return q[..., :n] if pad else q
+
+
+def mx_qdq(a: np.ndarray, axis: int) -> np.ndarray:
+    """Quantise to MXFP8 with 32-element blocks running along `axis`, then dequantise (fp64)."""
+    a = np.moveaxis(np.asarray(a, dtype=np.float64), axis, -1)
+    return np.moveaxis(_qdq_last_axis(a), -1, axis)
+
+
+def mx_qdq_segments(a: np.ndarray, starts: np.ndarray) -> np.ndarray:
+    """MXFP8 qdq along axis 0 with blocks restarting at each segment start (expert group).
+
+    Rows [starts[i], starts[i+1]) form one segment; blocks of 32 rows run from the segment's
+    first row and the last, shorter block is padded with zeros.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    out = np.empty_like(a)
+    for i in range(len(starts) - 1):
+        lo, hi = int(starts[i]), int(starts[i + 1])
+        if hi > lo:
+            out[lo:hi] = mx_qdq(a[lo:hi], axis=0)
+    return out
+
+
+# ----------------------------------------------------------------------------------------------
+# forward
+# ----------------------------------------------------------------------------------------------
+def _as64(a):
+    return np.asarray(a, dtype=np.float64)
+
+
+def forward(x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, keep: bool = False):
+    """y[t] = sum_j w[t,j] * W2[e] (silu(W13[e,:I] x[t]) * (W13[e,I:] x[t])), e = topk_idx[t,j].
+
+    Evaluated per expert group in sorted (routed) order.  With keep=True also returns the
+    intermediates in sorted order: X_perm, g, u, h, o (and the routing dict).
+    """
+    x, W13, W2 = _as64(x), _as64(W13), _as64(W2)
+    T, H = x.shape
+    E, I2, _ = W13.shape
+    I = I2 // 2
+    k = topk_idx.shape[1]
+    r = route(topk_idx, E)
+    wflat = _as64(topk_w).reshape(-1)
+    X = permute_rows(x, r["perm"], k)
+    if mxfp8:
+        X = mx_qdq(X, axis=1)                # activations quantised along H (the contraction)
+    S = T * k
+    g = np.zeros((S, I)); u = np.zeros((S, I)); h = np.zeros((S, I)); o = np.zeros((S, H))
+    for e in range(E):
+        lo, hi = r["off"][e], r["off"][e + 1]
+        if hi == lo:
+            continue
+        Wg, Wu, Wd = W13[e, :I], W13[e, I:], W2[e]
+        if mxfp8:
+            Wg, Wu = mx_qdq(Wg, axis=1), mx_qdq(Wu, axis=1)
+            Wd = mx_qdq(Wd, axis=1)          # W2[e] is [H, I]: blocks along I, the contraction
+        g[lo:hi] = X[lo:hi] @ Wg.T
+        u[lo:hi] = X[lo:hi] @ Wu.T
+        h[lo:hi] = silu(g[lo:hi]) * u[lo:hi]
+        hq = mx_qdq(h[lo:hi], axis=1) if mxfp8 else h[lo:hi]
+        o[lo:hi] = hq @ Wd.T
+    w_sorted = wflat[r["perm"]]
+    y = unpermute_sum(w_sorted[:, None] * o, r["inv"], T, k)
+    if keep:
+        return y, {"route": r, "X_perm": X, "g": g, "u": u, "h": h, "o": o, "w_sorted": w_sorted}
+    return y
+
+
+# ----------------------------------------------------------------------------------------------
+# backward of the loss L = <dy, y>
+# ----------------------------------------------------------------------------------------------
+def backward(dy, x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, keep: bool = False):
+    """Gradients of <dy, y> with respect to x, W13, W2 and topk_w.
+
+    Per slot (t, j) routed to expert e, with g, u, h from the forward:
+      dA = W2[e]^T dy[t]                    dtopk_w[t, j] = <dA, h>   (= <dy[t], o[t, j]>)
+      dh = w * dA                           dg = dh * u * s(g) * (1 + g * (1 - s(g)))
+      du = dh * silu(g)                     dx[t] += W13[e,:I]^T dg + W13[e,I:]^T du
+      dW2[e] += dy[t] (w h)^T               dW13[e,:I] += dg x[t]^T,  dW13[e,I:] += du x[t]^T
+    In MXFP8 mode each GEMM operand is quantised along that GEMM's contraction axis first
+    (for the weight gradients the contraction runs over the tokens of one expert group).
+    """
+    dy, x, W13, W2 = _as64(dy), _as64(x), _as64(W13), _as64(W2)
+    T, H = x.shape
+    E, I2, _ = W13.shape
+    I = I2 // 2
+    k = topk_idx.shape[1]
+    _, fw = forward(x, topk_idx, topk_w, W13, W2, mxfp8=mxfp8, keep=True)
+    r = fw["route"]
+    off = r["off"]
+    g, u, h, w_s = fw["g"], fw["u"], fw["h"], fw["w_sorted"]
+    X = fw["X_perm"]                         # already quantised along H in MXFP8 mode
+    X_raw = permute_rows(x, r["perm"], k)
+    dY = permute_rows(dy, r["perm"], k)
+    dYq = mx_qdq(dY, axis=1) if mxfp8 else dY
+    S = T * k
+    dA = np.zeros((S, I)); dG = np.zeros((S, 2 * I)); Hw = np.zeros((S, I)); dXp = np.zeros((S, H))
+    dW13 = np.zeros_like(W13); dW2 = np.zeros_like(W2)
+    for e in range(E):
+        lo, hi = off[e], off[e + 1]
+        if hi == lo:
+            continue
+        Wd = mx_qdq(W2[e], axis=0) if mxfp8 else W2[e]       # contraction over H: blocks along H
+        dA[lo:hi] = dYq[lo:hi] @ Wd
+        sg = sigmoid(g[lo:hi])
+        dh = w_s[lo:hi, None] * dA[lo:hi]
+        dG[lo:hi, :I] = dh * u[lo:hi] * sg * (1.0 + g[lo:hi] * (1.0 - sg))
+        dG[lo:hi, I:] = dh * g[lo:hi] * sg
+        Hw[lo:hi] = w_s[lo:hi, None] * h[lo:hi]
+        W = mx_qdq(W13[e], axis=0) if mxfp8 else W13[e]     # contraction over 2I: blocks along 2I
+        dGq = mx_qdq(dG[lo:hi], axis=1) if mxfp8 else dG[lo:hi]
+        dXp[lo:hi] = dGq @ W
+    dtw_sorted = np.einsum("si,si->s", dA, h)
+    if mxfp8:
+        a6, b6 = mx_qdq_segments(dY, off), mx_qdq_segments(Hw, off)
+        a7, b7 = mx_qdq_segments(dG, off), mx_qdq_segments(X_raw, off)
+    else:
+        a6, b6, a7, b7 = dY, Hw, dG, X_raw
+    for e in range(E):
+        lo, hi = off[e], off[e + 1]
+        if hi == lo:
+            continue                          # an expert without tokens has zero weight gradients
+        dW2[e] = a6[lo:hi].T @ b6[lo:hi]
+        dW13[e] = a7[lo:hi].T @ b7[lo:hi]
+    dx = unpermute_sum(dXp, r["inv"], T, k)
+    dtopk_w = np.empty(S)
+    dtopk_w[r["perm"]] = dtw_sorted
+    dtopk_w = dtopk_w.reshape(T, k)
+    out = {"dx": dx, "dW13": dW13, "dW2": dW2, "dtopk_w": dtopk_w}
+    if keep:
+        out.update({"fwd": fw, "dY_perm": dY, "dA": dA, "dG": dG, "Hw": Hw, "dXpart": dXp})
+    return out
+
+
+# ----------------------------------------------------------------------------------------------
+# sampled evaluation for full-size checks: a few tokens or a few experts at a time
+# ----------------------------------------------------------------------------------------------
+def forward_tokens(x, topk_idx, topk_w, W13, W2, tokens, *, mxfp8: bool = False):
+    """y[t] for the listed tokens only, one slot at a time (BF16 / MXFP8 as in `forward`)."""
+    I = W13.shape[1] // 2
+    out = np.zeros((len(tokens), x.shape[1]))
+    for n, t in enumerate(tokens):
+        xt = _as64(x[t])
+        if mxfp8:
+            xt = mx_qdq(xt[None], axis=1)[0]
+        for j in range(topk_idx.shape[1]):
+            e = int(topk_idx[t, j])
+            W = _as64(W13[e]); Wd = _as64(W2[e])
+            if mxfp8:
+                W = mx_qdq(W, axis=1); Wd = mx_qdq(Wd, axis=1)
+            g = W[:I] @ xt
+            u = W[I:] @ xt
+            hh = silu(g) * u
+            if mxfp8:
+                hh = mx_qdq(hh[None], axis=1)[0]
+            out[n] += float(topk_w[t, j]) * (Wd @ hh)
+    return out
+
+
+def backward_tokens(dy, x, topk_idx, topk_w, W13, W2, tokens):
+    """dx[t] and dtopk_w[t, :] for the listed tokens only (BF16 arithmetic, fp64)."""
+    I = W13.shape[1] // 2
+    k = topk_idx.shape[1]
+    dx = np.zeros((len(tokens), x.shape[1]))
+    dtw = np.zeros((len(tokens), k))
+    for n, t in enumerate(tokens):
+        xt, dyt = _as64(x[t]), _as64(dy[t])
+        for j in range(k):
+            e = int(topk_idx[t, j])
+            W = _as64(W13[e]); Wd = _as64(W2[e])
+            g = W[:I] @ xt
+            u = W[I:] @ xt
+            sg = sigmoid(g)
+            dA = Wd.T @ dyt
+            dtw[n, j] = dA @ (silu(g) * u)
+            dh = float(topk_w[t, j]) * dA
+            dg = dh * u * sg * (1.0 + g * (1.0 - sg))
+            du = dh * g * sg
+            dx[n] += W[:I].T @ dg + W[I:].T @ du
+    return dx, dtw
+
+
+def wgrad_experts(dy, x, topk_idx, topk_w, W13, W2, experts):
+    """(dW13[e], dW2[e]) for the listed experts only (BF16 arithmetic, fp64)."""
+    I = W13.shape[1] // 2
+    k = topk_idx.shape[1]
+    flat = np.asarray(topk_idx).reshape(-1)
+    wflat = _as64(topk_w).reshape(-1)
+    res = []
+    for e in experts:
+        slots = np.nonzero(flat == e)[0]
+        t = slots // k
+        X = _as64(x[t]); dY = _as64(dy[t]); w = wflat[slots][:, None]
+        W = _as64(W13[e]); Wd = _as64(W2[e])
+        g = X @ W[:I].T
+        u = X @ W[I:].T
+        sg = sigmoid(g)
+        h = g * sg * u
+        dA = dY @ Wd
+        dh = w * dA
+        dg = dh * u * sg * (1.0 + g * (1.0 - sg))
+        du = dh * g * sg
+        dW13_e = np.concatenate([dg.T @ X, du.T @ X], axis=0)
+        dW2_e = dY.T @ (w * h)
+        res.append((dW13_e, dW2_e))
+    return res
