@@ -1,0 +1,367 @@
+#!/usr/bin/env python
+"""Benchmark of the fused MoE expert layer on GB300: forward, backward and the activation-
+checkpointed layer (2 x forward + backward), in ms and TFLOP/s, with the fraction of the measured
+bf16 tensor peak.
+
+A step is one checkpointed layer over the Qwen3-30B-A3B-shaped workload (T=16384 tokens, H=2048,
+I=768, 128 experts, top-8, uniform routing): a forward, a forward that saves [g|u] (the
+recompute), and a backward that reuses it.  FLOPs are algorithmic: 2*T*k*H*3I per forward, twice
+that per backward; recompute FLOPs are not credited.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on a bounded token sample of the same workload (there is
+no runnable reference implementation).  Under torchrun each rank runs an independent replica of
+the layer (no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd/bwd/2xfwd+bwd ms & TFLOP/s (% of GB300 tensor peak), 1 GPU"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="qwen3_30b_a3b")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ------------------------------------------------------------------------------------------ dist
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.6)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as fh:
+            rows = [ln.strip().split(", ") for ln in fh if ln.strip()]
+        os.unlink(self.file.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1])); smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------------------ ours
+GEMM_FLOPS = {  # algorithmic FLOPs per launch of each grouped GEMM, in units of S*H*I
+    "gemm_fwd_gate_up_swiglu": 4, "gemm_fwd_gate_up_save": 4, "gemm_fwd_down_weighted": 2,
+    "gemm_bwd_down_swiglu_bwd": 2, "gemm_bwd_gate_up": 4, "gemm_wgrad_down": 2, "gemm_wgrad_gate_up": 4,
+}
+
+
+def cpu_baseline(cfg, budget_s: float, seed_tokens: int = 256):
+    """The oracle as it stands, on a token sample of the workload (all E experts, same k)."""
+    import numpy as np
+
+    import oracle
+    from moe_expert_layer_permute_gb300 import inputs as gen
+    cores = len(os.sched_getaffinity(0))
+    Ts = seed_tokens
+    sub = gen.custom_config(name=cfg.name + "_sample", T=Ts, H=cfg.H, I=cfg.I, E=cfg.E, k=cfg.k,
+                            routing=cfg.routing, seed=cfg.seed)
+    inp = gen.make_inputs(sub)
+    args = (inp.f64("x"), inp.topk_idx, inp.f64("topk_w"), inp.f64("W13"), inp.f64("W2"))
+    dy = inp.f64("dy")
+    runs = []
+    t_end = time.time() + budget_s
+    while True:
+        t0 = time.perf_counter()
+        oracle.forward(*args)
+        oracle.forward(*args)
+        oracle.backward(dy, *args)
+        runs.append(time.perf_counter() - t0)
+        if time.time() > t_end or len(runs) >= 3:
+            break
+    sec = statistics.median(runs)
+    flops = 4 * sub.fwd_flops()
+    del np
+    return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{Ts} tokens of {cfg.name} (all {cfg.E} experts, top-{cfg.k}), fp64 numpy, "
+                      f"checkpointed layer 2xfwd+bwd, median of {len(runs)} runs ({sec:.2f} s each)",
+            "seconds_per_layer_sample": sec}
+
+
+def run_ours(args, rank, ws, local):
+    import numpy as np
+    import torch
+
+    from moe_expert_layer_permute_gb300 import build as b
+    b.build()
+    from moe_expert_layer_permute_gb300 import binding as bd
+    from moe_expert_layer_permute_gb300 import inputs as gen
+
+    cfg = gen.CONFIGS[args.config]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = gen.make_inputs(cfg)
+
+    def host(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a))
+
+    h_in = {n: host(getattr(inp, n)).pin_memory() for n in ("x", "topk_idx", "topk_w", "W13", "W2", "dy")}
+    d = {n: t.to(dev) for n, t in h_in.items()}
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    wdt = torch.bfloat16
+    d["y"] = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    d["dx"] = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    d["dW13"] = torch.empty(E, 2 * I, H, dtype=wdt, device=dev)
+    d["dW2"] = torch.empty(E, H, I, dtype=wdt, device=dev)
+    d["dtw"] = torch.empty(T, k, dtype=torch.float32, device=dev)
+    sc = bd.Scratch(T, H, I, E, k, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd(flags=0):
+        bd.moe_fwd(d["x"], d["topk_idx"], d["topk_w"], d["W13"], d["W2"], d["y"], sc, flags=flags)
+
+    def bwd(flags=0):
+        bd.moe_bwd(d["dy"], d["x"], d["topk_idx"], d["topk_w"], d["W13"], d["W2"], d["dx"], d["dW13"], d["dW2"],
+                   d["dtw"], sc, flags=flags)
+
+    def step():
+        fwd()
+        fwd(bd.MOE_FLAG_SAVE_GU)
+        bwd(bd.MOE_FLAG_REUSE_FWD)
+
+    def timed(fn, n):
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        return allreduce_max(e0.elapsed_time(e1), ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if bd.moe_read_device_status(sc) != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    # forward alone and backward alone (the backward reuses a saved forward, as in the layer)
+    fwd_ms = timed(fwd, args.steps) / args.steps
+    fwd(bd.MOE_FLAG_SAVE_GU)
+    bwd_ms = timed(lambda: bwd(bd.MOE_FLAG_REUSE_FWD), args.steps) / args.steps
+    # the checkpointed layer, with per-kernel CUDA events recorded on the launch stream
+    bd.moe_trace_reset()
+    bd.moe_trace_enable(True)
+    full_total = timed(step, args.steps)
+    bd.moe_trace_enable(False)
+    kern = bd.moe_trace_read()
+    clk = clocks.stop()
+    full_ms = full_total / args.steps
+    status = bd.moe_read_device_status(sc)
+
+    # end to end through the public API: pinned host inputs in, outputs back to pinned host
+    h_out = {n: torch.empty(d[n].shape, dtype=d[n].dtype).pin_memory() for n in ("y", "dx", "dW13", "dW2", "dtw")}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        for n, t in h_in.items():
+            d[n].copy_(t, non_blocking=True)
+        step()
+        for n, t in h_out.items():
+            t.copy_(d[n], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_step()
+    e2e_ms = timed(e2e_step, e2e_steps) / e2e_steps
+
+    peaks, peak_src = load_peaks()
+    fwd_fl = cfg.fwd_flops()
+    full_fl = 4 * fwd_fl
+    shf = float(cfg.S) * H * I
+    rows = {}
+    total_ms = sum(v[1] for v in kern.values())
+    for name, (n, ms) in kern.items():
+        rows[name] = {"launches": n, "avg_ms": ms / n, "share": ms / total_ms if total_ms else None}
+    gemms = {n: v for n, v in rows.items() if n in GEMM_FLOPS}
+    top = max(gemms, key=lambda n: gemms[n]["avg_ms"] * gemms[n]["launches"]) if gemms else None
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    roof = None
+    if top:
+        ach = GEMM_FLOPS[top] * shf / (gemms[top]["avg_ms"] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                "traffic": None, "kernel": top,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)"}
+    full_tf = full_fl / (full_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": full_tf * ws, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": full_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) x/dy, N(0,1/sqrt(fan_in)) weights, uniform top-8 routing, softmax weights",
+        "config": {"workload": f"{cfg.name}: T={T} H={H} I={I} E={E} k={k} {cfg.precision} {cfg.routing} routing",
+                   "step": "fwd + fwd(save [g|u]) + bwd(reuse)", "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (weights alone 1.13 GiB per step)"},
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "full_ms": full_ms,
+        "fwd_tflops": fwd_fl / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": 2 * fwd_fl / (bwd_ms * 1e-3) / 1e12,
+        "full_tflops": full_tf, "frac_of_peak": full_tf / peak,
+        "peak_tflops": {"value": peak, "source": f"{peak_src} bf16_tflops_sustained"},
+        "identity_2fwd_plus_bwd_ms": 2 * fwd_ms + bwd_ms,
+        "roofline": roof,
+        "e2e": {"value": full_fl / (e2e_ms * 1e-3) / 1e12 * ws, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(sum(v[0] for v in kern.values())),
+        "kernels": rows, "clocks": clk, "device_status": status,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, budget_s=20.0)
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    return line
+
+
+def run_reference(args, rank, ws):
+    """The fp64 oracle timed on the host cores, each step a bounded token sample of the workload."""
+    import numpy as np
+
+    import oracle
+    from moe_expert_layer_permute_gb300 import inputs as gen
+    cfg = gen.CONFIGS[args.config]
+    cores = len(os.sched_getaffinity(0))
+    Ts = 64
+    sub = gen.custom_config(name=cfg.name + "_sample", T=Ts, H=cfg.H, I=cfg.I, E=cfg.E, k=cfg.k,
+                            routing=cfg.routing, seed=cfg.seed)
+    inp = gen.make_inputs(sub)
+    a = (inp.f64("x"), inp.topk_idx, inp.f64("topk_w"), inp.f64("W13"), inp.f64("W2"))
+    dy = inp.f64("dy")
+
+    def step():
+        oracle.forward(*a)
+        oracle.forward(*a)
+        oracle.backward(dy, *a)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    sec = (time.perf_counter() - t0) / args.steps
+    val = 4 * sub.fwd_flops() / sec / 1e12
+    del np
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same recipe as ours)",
+            "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} k={cfg.k} "
+                                   f"{cfg.precision} {cfg.routing} routing",
+                       "step": "fwd + fwd + bwd (oracle)", "parallelism": "single process"},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{Ts} tokens of {cfg.name} per step (all {cfg.E} experts, top-{cfg.k}), "
+                                       f"fp64 numpy checkpointed layer"},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    rank, ws, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, ws)), flush=True)
+        return
+    line = run_ours(args, rank, ws, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

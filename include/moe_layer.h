@@ -1,0 +1,169 @@
+/*
+ * moe_layer.h - C ABI of the GB300 fused MoE expert layer (forward and backward).
+ *
+ * The layer (MarkTechPost, "Prime Intellect Releases Prime Mega MoE", section "How does the fused
+ * kernel work?"): every token is dispatched to k of E experts, each expert applies two linear
+ * layers with SwiGLU between them, and the expert outputs are combined back per token by routing
+ * weight; the fused call keeps its intermediates in GPU-only scratch buffers instead of tensors.
+ * Grouping tokens by expert (counts, group offsets, token reorder) and the weighted aggregation
+ * follow kongchang.com, "Prime Intellect推出Prime Mega MoE", section "为什么 MoE 训练特别需要融合内核".
+ * The experts are gated and bias-free, H % 256 == 0 and I % 128 == 0, in BF16 or MXFP8 on
+ * Blackwell (ic.work analysis, section "算子下沉时代的硬件死锁暗礁").  One call per direction:
+ * moe_fwd and moe_bwd (the backward was added for training: MarkTechPost, same section).
+ *
+ * With every expert on one GPU, the expert-parallel dispatch is a gather of token rows into
+ * expert order and the combine is a weighted, fixed-order sum back to token order.
+ *
+ * Shapes (row-major, element strides; the innermost stride must be 1 and rows contiguous):
+ *   x, dy, y, dx : [T, H]  bf16          topk_idx : [T, k] int32 (expert ids, distinct per token)
+ *   topk_w       : [T, k]  fp32          dtopk_w  : [T, k] fp32
+ *   W13, dW13    : [E, 2I, H]            rows [0, I) = gate projection, rows [I, 2I) = up projection
+ *   W2,  dW2     : [E, H, I]             W13 / W2 are bf16; dW13 / dW2 are bf16 or fp32
+ *   y[t] = sum_j topk_w[t,j] * W2[e] (silu(W13[e,:I] x[t]) * (W13[e,I:] x[t])),  e = topk_idx[t,j]
+ *   moe_bwd returns the gradients of <dy, y> with respect to x, W13, W2 and topk_w.
+ *
+ * Conventions shared by every entry point:
+ *   - Ownership: the caller owns every buffer, the scratch buffer included.  The library never
+ *     allocates or frees device memory and keeps no pointer after a call returns.
+ *   - Asynchrony: moe_fwd / moe_bwd only enqueue work on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and never synchronise.  Outputs are overwritten, not accumulated.
+ *   - Errors: arguments are validated on the host before anything is launched; a negative
+ *     MOE_ERR_* code is returned and nothing is enqueued.  A launch failure returns MOE_ERR_CUDA.
+ *     Device-side problems (an expert id out of range under MOE_FLAG_DEBUG_CHECK, a pipeline wait
+ *     that timed out) never trap: the kernels record a code in the scratch status word, which
+ *     moe_read_device_status returns.
+ *   - Alignment: every device pointer must be 16-byte aligned (TMA); the scratch pointer 256-byte.
+ *   - T == 0 is a valid no-op (dW13 / dW2 are zeroed by moe_bwd).
+ *   - Calls that share one scratch buffer must be ordered on one stream.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- types ------------------------------------------------------------------------------- */
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
+typedef enum { MOE_DT_BF16 = 0, MOE_DT_F32 = 1, MOE_DT_I32 = 2 } moe_dtype;
+
+/* A view of a caller-owned buffer: `data` is a device pointer for the layer calls. */
+typedef struct {
+    void*   data;
+    int32_t dtype;      /* moe_dtype */
+    int32_t ndim;       /* 1..3 */
+    int64_t shape[3];
+    int64_t stride[3];  /* in elements */
+} moe_tensor;
+
+/* Problem description.  precision is a moe_precision; flags a set of MOE_FLAG_*. */
+typedef struct {
+    int64_t  T, H, I, E, k;
+    int32_t  precision;
+    uint32_t flags;
+} moe_desc;
+
+/* moe_fwd also stores the gate/up pre-activations [g|u] (bf16, 2I per routed row) in scratch, so
+ * that a following moe_bwd with MOE_FLAG_REUSE_FWD skips recomputing the first GEMM (the second
+ * forward of an activation-checkpointed layer is that recompute). */
+#define MOE_FLAG_SAVE_GU     0x1u
+/* moe_bwd reuses the routing, the dispatched rows and [g|u] left in scratch by the latest moe_fwd
+ * that had MOE_FLAG_SAVE_GU and the same x, topk_idx, topk_w, W13, W2 pointers and desc; returns
+ * MOE_ERR_STATE if the scratch handle does not record such a forward. */
+#define MOE_FLAG_REUSE_FWD   0x2u
+/* Kernels check 0 <= topk_idx < E and record MOE_DEV_BAD_EXPERT instead of reading out of range. */
+#define MOE_FLAG_DEBUG_CHECK 0x4u
+
+/* Host-side handle of a caller-owned device scratch buffer of at least moe_scratch_bytes(desc)
+ * bytes.  `state` is written by the library (which forward's results the buffer holds); zero it
+ * when the handle is created. */
+typedef struct {
+    void*    data;
+    uint64_t bytes;
+    moe_desc desc;
+    uint64_t state[4];
+} moe_scratch;
+
+/* ---- status codes ------------------------------------------------------------------------ */
+#define MOE_OK                0
+#define MOE_ERR_NULL         -1   /* a required pointer is NULL */
+#define MOE_ERR_SHAPE        -2   /* shape rules: H % 256, I % 128, 1 <= k <= E, tensor shapes */
+#define MOE_ERR_DTYPE        -3   /* a tensor has the wrong element type */
+#define MOE_ERR_LAYOUT       -4   /* rows not contiguous / innermost stride != 1 */
+#define MOE_ERR_ALIGN        -5   /* a pointer or row pitch is not 16-byte aligned */
+#define MOE_ERR_SCRATCH      -6   /* scratch missing, too small, misaligned or made for another desc */
+#define MOE_ERR_STATE        -7   /* MOE_FLAG_REUSE_FWD without a matching saved forward */
+#define MOE_ERR_UNSUPPORTED  -8   /* precision or size outside what this build supports */
+#define MOE_ERR_CUDA         -9   /* a CUDA runtime call or kernel launch failed */
+#define MOE_ERR_DEVICE       -10  /* the device status word holds a MOE_DEV_* code */
+
+/* device status word codes (moe_read_device_status) */
+#define MOE_DEV_OK            0
+#define MOE_DEV_BAD_EXPERT    1   /* an expert id outside [0, E) (MOE_FLAG_DEBUG_CHECK) */
+#define MOE_DEV_TIMEOUT       2   /* a pipeline wait gave up; the kernel exited early */
+
+/* ---- sizes -------------------------------------------------------------------------------- */
+/* Bytes of scratch moe_fwd / moe_bwd need for `desc` (0 if desc breaks the shape rules).
+ * It grows linearly in T*k (routed rows, each padded per expert to a multiple of 128). */
+size_t moe_scratch_bytes(const moe_desc* desc);
+
+/* ---- the layer ---------------------------------------------------------------------------- */
+/* Forward: y = the layer applied to x.  Scratch receives the routing bookkeeping, the dispatched
+ * rows, the hidden activations and (with MOE_FLAG_SAVE_GU) [g|u]. */
+int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* topk_w,
+            const moe_tensor* W13, const moe_tensor* W2, moe_tensor* y,
+            moe_scratch* scratch, void* stream);
+
+/* Backward of <dy, y>: dx, dW13, dW2 and dtopk_w (all overwritten).  Without
+ * MOE_FLAG_REUSE_FWD it recomputes the routing and the first GEMM itself. */
+int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_idx,
+            const moe_tensor* topk_w, const moe_tensor* W13, const moe_tensor* W2,
+            moe_tensor* dx, moe_tensor* dW13, moe_tensor* dW2, moe_tensor* dtopk_w,
+            moe_scratch* scratch, void* stream);
+
+/* Synchronises `stream`, returns the device status word in *status (a MOE_DEV_* code) and
+ * clears it.  Returns MOE_OK, or MOE_ERR_CUDA if the synchronisation itself failed. */
+int moe_read_device_status(moe_scratch* scratch, void* stream, int* status);
+
+/* Static message for a MOE_ERR_* code. */
+const char* moe_strerror(int code);
+
+/* ---- introspection (tests, tracing) ------------------------------------------------------- */
+/* Named regions of the scratch buffer, valid after a call on that scratch.  Layouts:
+ *   MOE_VIEW_COUNTS   int32[E]        tokens routed to each expert
+ *   MOE_VIEW_OFFSETS  int32[E+1]      exclusive prefix of the counts (group offsets)
+ *   MOE_VIEW_PERM     int32[T*k]      slot (t*k+j) at each sorted position, stable in slot order
+ *   MOE_VIEW_INV      int32[T*k]      sorted position of each slot
+ *   MOE_VIEW_PAD_OFFSETS int32[E+1]   start row of each expert in the padded row layout
+ *   MOE_VIEW_XPERM    bf16 [rows, H]  dispatched x rows (padded layout: expert e's rows start at
+ *                                     PAD_OFFSETS[e], padding rows are zero)
+ *   MOE_VIEW_HID      bf16 [rows, I]  silu(g) * u of every routed row (forward)
+ *   MOE_VIEW_GU       bf16 [rows, 2I] [g | u] pre-activations
+ *   MOE_VIEW_YPART    bf16 [rows, H]  w * expert output per routed row (forward, before combine)
+ *   MOE_VIEW_DG       bf16 [rows, 2I] [dg | du] (backward)
+ *   MOE_VIEW_HW       bf16 [rows, I]  w * h (backward)
+ *   MOE_VIEW_DYPERM   bf16 [rows, H]  dispatched dy rows (backward)
+ * `rows` is T*k + 128*E, the largest padded row count.  Returns MOE_ERR_SHAPE for an unknown id. */
+enum {
+    MOE_VIEW_COUNTS = 0, MOE_VIEW_OFFSETS, MOE_VIEW_PERM, MOE_VIEW_INV, MOE_VIEW_PAD_OFFSETS,
+    MOE_VIEW_XPERM, MOE_VIEW_HID, MOE_VIEW_GU, MOE_VIEW_YPART, MOE_VIEW_DG, MOE_VIEW_HW,
+    MOE_VIEW_DYPERM, MOE_VIEW_COUNT_
+};
+int moe_scratch_view(const moe_desc* desc, int view, uint64_t* offset, uint64_t* bytes);
+
+/* Per-kernel timing.  With tracing on, every launch made by moe_fwd / moe_bwd is bracketed by a
+ * pair of CUDA events recorded on the caller's stream (so the times are those of the launches as
+ * they run in the step).  moe_trace_read synchronises on the recorded events, and for each kernel
+ * kind i < *n fills names[i] (static strings), launches[i] and total_ms[i]; *n is set to the number
+ * of kinds seen.  moe_trace_reset clears the counters.  Not thread-safe. */
+int moe_trace_enable(int on);
+int moe_trace_reset(void);
+int moe_trace_read(const char** names, int64_t* launches, double* total_ms, int* n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_LAYER_H */

@@ -1,0 +1,65 @@
+// internal.h - scratch layout and kernel launchers of the MoE layer (host side, C++).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_layer.h"
+
+namespace moe {
+
+constexpr int kBM = 128;          // rows of a GEMM tile; each expert's rows are padded to a multiple
+constexpr int kBK = 64;           // bf16 elements of K per pipeline stage (one 128-byte row)
+constexpr int kRouteChunk = 2048; // slots per block of the routing kernels
+constexpr int kMaxExperts = 1024;
+
+// Byte offsets of every region of the scratch buffer for one desc.  The routed rows of expert e
+// occupy padded rows [pad_off[e], pad_off[e+1]) with pad_off[e] a multiple of 128, so a GEMM
+// tile never straddles two experts; padding rows hold zeros.  `rows` bounds the padded count.
+struct Layout {
+    int64_t T, H, I, E, k, S, rows, nb_route, n_dtw;
+    size_t ctrl, hist, cnt, off, pad_off, mtile, order, base, perm, inv, pos, row_slot;
+    size_t xperm, hid, gu, ypart, dyperm, dg, hw, dtw;
+    size_t total;
+};
+
+bool make_layout(const moe_desc* d, Layout* L);
+
+// ---- launchers (all asynchronous on `st`) ---------------------------------------------------
+struct Ctx {
+    cudaStream_t st;
+    char* base;        // scratch base
+    const Layout* L;
+    int* status;       // device status word
+    int num_sms;
+    const float* topk_w;  // routing weights [T*k] (caller's tensor)
+};
+
+// routing: counts, offsets, padded offsets, m-tile prefix, expert order, perm / inv / pos / row_slot
+cudaError_t launch_routing(const Ctx& c, const int32_t* topk_idx);
+// dst[r] = src[row_slot[r] / k] for every padded row r (zeros on padding rows); up to two pairs
+cudaError_t launch_gather(const Ctx& c, const void* src0, void* dst0, const void* src1, void* dst1);
+// out[t] = sum_j part[pos[t*k+j]] (fixed j order); optionally dtopk_w[s] = sum_n dtw[pos[s], n]
+cudaError_t launch_combine(const Ctx& c, const void* part, void* out, float* dtopk_w);
+
+// grouped GEMMs (persistent, TMA + tcgen05)
+enum class GemmKind : int {
+    FwdGateUp = 0,     // [g|u] = X_perm W13[e]^T, epilogue h = silu(g) u  (optionally saves [g|u])
+    FwdGateUpSaveOnly, // same GEMM, epilogue stores [g|u] only (backward recompute)
+    FwdDown,           // o = h W2[e]^T, epilogue Ypart = w o
+    BwdDown,           // dA = dY_perm W2[e], epilogue SwiGLU backward -> [dg|du], w h, <dA, h>
+    BwdGateUp,         // dXpart = [dg|du] W13[e]
+    WgradDown,         // dW2[e] = dY_perm^T (w h) over the expert's rows
+    WgradGateUp,       // dW13[e] = [dg|du]^T X_perm over the expert's rows
+};
+cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, bool out_f32, bool save_gu);
+// N tile of the backward down-projection product (and so the number of <dA, h> partials per row)
+int bwd_down_bn(int64_t I);
+
+// tracing hooks used by the launch sequence
+void trace_begin(cudaStream_t st, int kind_id);
+void trace_end(cudaStream_t st, int kind_id);
+
+}  // namespace moe

@@ -1,0 +1,357 @@
+// moe_api.cu - the C ABI of the MoE layer: argument checks, scratch layout, the forward and
+// backward launch sequences, device status, per-kernel tracing.
+//
+// Forward (one call, all on the caller's stream, no host synchronisation):
+//   routing -> gather x -> [g|u] = X W13^T, h = silu(g) u -> Ypart = w (h W2^T) -> y = combine
+// Backward of <dy, y>:
+//   [routing -> gather x -> [g|u] recompute]  (skipped under MOE_FLAG_REUSE_FWD)
+//   gather dy -> dA = dY W2 with the SwiGLU backward in the epilogue ([dg|du], w h, <dA, h>)
+//   -> dXpart = [dg|du] W13 -> dW2 = dY^T (w h) -> dW13 = [dg|du]^T X -> dx = combine(dXpart),
+//   dtopk_w = sum of the <dA, h> partials.
+// The single call per direction and the GPU-only scratch in place of intermediate tensors follow
+// MarkTechPost, "Prime Intellect Releases Prime Mega MoE", section "How does the fused kernel
+// work?"; the shape rules follow ic.work analysis, section "算子下沉时代的硬件死锁暗礁".
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool make_layout(const moe_desc* d, Layout* L) {
+    if (!d) return false;
+    if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0 || d->k <= 0) return false;
+    if (d->H % 256 != 0 || d->I % 128 != 0 || d->k > d->E || d->E > kMaxExperts) return false;
+    const int64_t S = d->T * d->k;
+    const int64_t rows = S + (int64_t)kBM * d->E;
+    if (rows >= (int64_t)INT32_MAX / 2) return false;
+    L->T = d->T; L->H = d->H; L->I = d->I; L->E = d->E; L->k = d->k; L->S = S; L->rows = rows;
+    L->nb_route = (S + kRouteChunk - 1) / kRouteChunk;
+    L->n_dtw = d->I / bwd_down_bn(d->I);
+    const size_t A = 4096;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, A); return at; };
+    L->ctrl = take(256);
+    L->hist = take((size_t)std::max<int64_t>(L->nb_route, 1) * d->E * 4);
+    L->cnt = take((size_t)d->E * 4);
+    L->off = take((size_t)(d->E + 1) * 4);
+    L->pad_off = take((size_t)(d->E + 1) * 4);
+    L->mtile = take((size_t)(d->E + 1) * 4);
+    L->order = take((size_t)d->E * 4);
+    L->base = take((size_t)std::max<int64_t>(L->nb_route, 1) * d->E * 4);
+    L->perm = take((size_t)S * 4);
+    L->inv = take((size_t)S * 4);
+    L->pos = take((size_t)S * 4);
+    L->row_slot = take((size_t)rows * 4);
+    L->xperm = take((size_t)rows * d->H * 2);
+    L->hid = take((size_t)rows * d->I * 2);
+    L->gu = take((size_t)rows * 2 * d->I * 2);
+    L->ypart = take((size_t)rows * d->H * 2);   // also dXpart in the backward
+    L->dyperm = take((size_t)rows * d->H * 2);
+    L->dg = take((size_t)rows * 2 * d->I * 2);
+    L->hw = take((size_t)rows * d->I * 2);
+    L->dtw = take((size_t)rows * L->n_dtw * 4);
+    L->total = o;
+    return true;
+}
+
+// ------------------------------------------------------------------------------------------
+// tracing
+// ------------------------------------------------------------------------------------------
+static const char* kTraceNames[] = {
+    "route_hist", "route_scan", "route_place", "gather_rows", "combine_rows",
+    "gemm_fwd_gate_up_swiglu", "gemm_fwd_gate_up_save", "gemm_fwd_down_weighted", "gemm_bwd_down_swiglu_bwd",
+    "gemm_bwd_gate_up", "gemm_wgrad_down", "gemm_wgrad_gate_up",
+};
+constexpr int kTraceKinds = sizeof(kTraceNames) / sizeof(kTraceNames[0]);
+
+struct TraceRec {
+    int kind;
+    cudaEvent_t a, b;
+};
+static bool g_trace_on = false;
+static std::vector<TraceRec> g_trace;
+static int64_t g_trace_launches[kTraceKinds];
+static double g_trace_ms[kTraceKinds];
+static cudaEvent_t g_pending_begin = nullptr;
+
+void trace_begin(cudaStream_t st, int kind) {
+    if (!g_trace_on) return;
+    cudaEventCreate(&g_pending_begin);
+    cudaEventRecord(g_pending_begin, st);
+}
+void trace_end(cudaStream_t st, int kind) {
+    if (!g_trace_on || !g_pending_begin) return;
+    cudaEvent_t e;
+    cudaEventCreate(&e);
+    cudaEventRecord(e, st);
+    g_trace.push_back({kind, g_pending_begin, e});
+    g_pending_begin = nullptr;
+}
+static void trace_flush() {
+    for (auto& r : g_trace) {
+        float ms = 0.f;
+        cudaEventSynchronize(r.b);
+        if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess && r.kind >= 0 && r.kind < kTraceKinds) {
+            g_trace_launches[r.kind] += 1;
+            g_trace_ms[r.kind] += ms;
+        }
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    g_trace.clear();
+}
+
+// ------------------------------------------------------------------------------------------
+// argument checks
+// ------------------------------------------------------------------------------------------
+static int num_sms_current() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+static int check_tensor(const moe_tensor* t, int dtype, int ndim, int64_t s0, int64_t s1, int64_t s2) {
+    if (!t) return MOE_ERR_NULL;
+    if (t->ndim != ndim) return MOE_ERR_SHAPE;
+    const int64_t want[3] = {s0, s1, s2};
+    for (int i = 0; i < ndim; ++i)
+        if (t->shape[i] != want[i]) return MOE_ERR_SHAPE;
+    if (t->dtype != dtype) return MOE_ERR_DTYPE;
+    int64_t expect = 1;
+    for (int i = ndim - 1; i >= 0; --i) {
+        if (t->shape[i] > 1 && t->stride[i] != expect) return MOE_ERR_LAYOUT;
+        expect *= t->shape[i];
+    }
+    if (expect > 0 && !t->data) return MOE_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0) return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
+static int check_weight_grad(const moe_tensor* t, int ndim, int64_t a, int64_t b, int64_t c, bool* f32) {
+    if (!t) return MOE_ERR_NULL;
+    *f32 = t->dtype == MOE_DT_F32;
+    return check_tensor(t, *f32 ? MOE_DT_F32 : MOE_DT_BF16, ndim, a, b, c);
+}
+
+static int check_desc_scratch(moe_scratch* s, Layout* L) {
+    if (!s) return MOE_ERR_NULL;
+    const moe_desc* d = &s->desc;
+    if (d->precision != MOE_BF16 && d->precision != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+    if (!make_layout(d, L)) return MOE_ERR_SHAPE;
+    if (d->precision == MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+    if (!s->data) return MOE_ERR_SCRATCH;
+    if (reinterpret_cast<uintptr_t>(s->data) % 256 != 0) return MOE_ERR_SCRATCH;
+    if (s->bytes < L->total) return MOE_ERR_SCRATCH;
+    return MOE_OK;
+}
+
+static uint64_t mix(uint64_t h, uint64_t v) {
+    h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+    return h;
+}
+static uint64_t fwd_tag(const moe_desc* d, const void* x, const void* idx, const void* w, const void* w13,
+                        const void* w2) {
+    uint64_t h = 0x6D6F655F66776400ull;
+    for (uint64_t v : {(uint64_t)d->T, (uint64_t)d->H, (uint64_t)d->I, (uint64_t)d->E, (uint64_t)d->k,
+                       (uint64_t)d->precision, (uint64_t)(uintptr_t)x, (uint64_t)(uintptr_t)idx,
+                       (uint64_t)(uintptr_t)w, (uint64_t)(uintptr_t)w13, (uint64_t)(uintptr_t)w2})
+        h = mix(h, v);
+    return h | 1ull;  // never 0 (0 = no saved forward)
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+#define MOE_TRY_CUDA(expr)                              \
+    do {                                                \
+        if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+    } while (0)
+
+extern "C" {
+
+size_t moe_scratch_bytes(const moe_desc* desc) {
+    Layout L;
+    return make_layout(desc, &L) ? L.total : 0;
+}
+
+int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* topk_w, const moe_tensor* W13,
+            const moe_tensor* W2, moe_tensor* y, moe_scratch* scratch, void* stream) {
+    Layout L;
+    int rc = check_desc_scratch(scratch, &L);
+    if (rc) return rc;
+    const moe_desc* d = &scratch->desc;
+    const int64_t T = d->T, H = d->H, I = d->I, E = d->E, k = d->k;
+    if ((rc = check_tensor(x, MOE_DT_BF16, 2, T, H, 0))) return rc;
+    if ((rc = check_tensor(topk_idx, MOE_DT_I32, 2, T, k, 0))) return rc;
+    if ((rc = check_tensor(topk_w, MOE_DT_F32, 2, T, k, 0))) return rc;
+    if ((rc = check_tensor(W13, MOE_DT_BF16, 3, E, 2 * I, H))) return rc;
+    if ((rc = check_tensor(W2, MOE_DT_BF16, 3, E, H, I))) return rc;
+    if ((rc = check_tensor(y, MOE_DT_BF16, 2, T, H, 0))) return rc;
+    const uint64_t tag = fwd_tag(d, x->data, topk_idx->data, topk_w->data, W13->data, W2->data);
+    const bool save = (d->flags & MOE_FLAG_SAVE_GU) != 0;
+    if (T == 0) {
+        scratch->state[0] = save ? tag : 0;
+        return MOE_OK;
+    }
+    const int nsm = num_sms_current();
+    if (nsm <= 0) return MOE_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char* base = reinterpret_cast<char*>(scratch->data);
+    Ctx c{st, base, &L, reinterpret_cast<int*>(base + L.ctrl), nsm, reinterpret_cast<const float*>(topk_w->data)};
+    MOE_TRY_CUDA(launch_routing(c, reinterpret_cast<const int32_t*>(topk_idx->data)));
+    MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, nullptr, nullptr));
+    MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUp, W13->data, nullptr, false, save));
+    MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdDown, W2->data, nullptr, false, false));
+    MOE_TRY_CUDA(launch_combine(c, base + L.ypart, y->data, nullptr));
+    // routing and dispatched rows are rewritten identically for the same inputs, so an earlier
+    // saved [g|u] of these inputs stays valid; anything else invalidates it
+    if (save)
+        scratch->state[0] = tag;
+    else if (scratch->state[0] != tag)
+        scratch->state[0] = 0;
+    return MOE_OK;
+}
+
+int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* topk_w,
+            const moe_tensor* W13, const moe_tensor* W2, moe_tensor* dx, moe_tensor* dW13, moe_tensor* dW2,
+            moe_tensor* dtopk_w, moe_scratch* scratch, void* stream) {
+    Layout L;
+    int rc = check_desc_scratch(scratch, &L);
+    if (rc) return rc;
+    const moe_desc* d = &scratch->desc;
+    const int64_t T = d->T, H = d->H, I = d->I, E = d->E, k = d->k;
+    bool f32_13 = false, f32_2 = false;
+    if ((rc = check_tensor(dy, MOE_DT_BF16, 2, T, H, 0))) return rc;
+    if ((rc = check_tensor(x, MOE_DT_BF16, 2, T, H, 0))) return rc;
+    if ((rc = check_tensor(topk_idx, MOE_DT_I32, 2, T, k, 0))) return rc;
+    if ((rc = check_tensor(topk_w, MOE_DT_F32, 2, T, k, 0))) return rc;
+    if ((rc = check_tensor(W13, MOE_DT_BF16, 3, E, 2 * I, H))) return rc;
+    if ((rc = check_tensor(W2, MOE_DT_BF16, 3, E, H, I))) return rc;
+    if ((rc = check_tensor(dx, MOE_DT_BF16, 2, T, H, 0))) return rc;
+    if ((rc = check_weight_grad(dW13, 3, E, 2 * I, H, &f32_13))) return rc;
+    if ((rc = check_weight_grad(dW2, 3, E, H, I, &f32_2))) return rc;
+    if ((rc = check_tensor(dtopk_w, MOE_DT_F32, 2, T, k, 0))) return rc;
+    const uint64_t tag = fwd_tag(d, x->data, topk_idx->data, topk_w->data, W13->data, W2->data);
+    const bool reuse = (d->flags & MOE_FLAG_REUSE_FWD) != 0;
+    if (reuse && scratch->state[0] != tag) return MOE_ERR_STATE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        MOE_TRY_CUDA(cudaMemsetAsync(dW13->data, 0, (size_t)E * 2 * I * H * (f32_13 ? 4 : 2), st));
+        MOE_TRY_CUDA(cudaMemsetAsync(dW2->data, 0, (size_t)E * H * I * (f32_2 ? 4 : 2), st));
+        return MOE_OK;
+    }
+    const int nsm = num_sms_current();
+    if (nsm <= 0) return MOE_ERR_CUDA;
+    char* base = reinterpret_cast<char*>(scratch->data);
+    Ctx c{st, base, &L, reinterpret_cast<int*>(base + L.ctrl), nsm, reinterpret_cast<const float*>(topk_w->data)};
+    if (!reuse) {
+        MOE_TRY_CUDA(launch_routing(c, reinterpret_cast<const int32_t*>(topk_idx->data)));
+        MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, dy->data, base + L.dyperm));
+        MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUpSaveOnly, W13->data, nullptr, false, true));
+    } else {
+        MOE_TRY_CUDA(launch_gather(c, dy->data, base + L.dyperm, nullptr, nullptr));
+    }
+    MOE_TRY_CUDA(launch_gemm(c, GemmKind::BwdDown, W2->data, nullptr, false, false));
+    MOE_TRY_CUDA(launch_gemm(c, GemmKind::BwdGateUp, W13->data, nullptr, false, false));
+    MOE_TRY_CUDA(launch_gemm(c, GemmKind::WgradDown, nullptr, dW2->data, f32_2, false));
+    MOE_TRY_CUDA(launch_gemm(c, GemmKind::WgradGateUp, nullptr, dW13->data, f32_13, false));
+    MOE_TRY_CUDA(launch_combine(c, base + L.ypart, dx->data, reinterpret_cast<float*>(dtopk_w->data)));
+    scratch->state[0] = tag;  // routing, dispatched x and [g|u] now describe these inputs
+    return MOE_OK;
+}
+
+int moe_read_device_status(moe_scratch* scratch, void* stream, int* status) {
+    if (!scratch || !scratch->data || !status) return MOE_ERR_NULL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    MOE_TRY_CUDA(cudaMemcpyAsync(&v, scratch->data, sizeof(int), cudaMemcpyDeviceToHost, st));
+    MOE_TRY_CUDA(cudaMemsetAsync(scratch->data, 0, sizeof(int), st));
+    MOE_TRY_CUDA(cudaStreamSynchronize(st));
+    *status = v;
+    return MOE_OK;
+}
+
+const char* moe_strerror(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_NULL: return "a required pointer is NULL";
+        case MOE_ERR_SHAPE: return "shape rules broken (H % 256, I % 128, 1 <= k <= E <= 1024, tensor shapes)";
+        case MOE_ERR_DTYPE: return "a tensor has the wrong element type";
+        case MOE_ERR_LAYOUT: return "a tensor is not contiguous row-major";
+        case MOE_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case MOE_ERR_SCRATCH: return "scratch missing, misaligned or smaller than moe_scratch_bytes";
+        case MOE_ERR_STATE: return "MOE_FLAG_REUSE_FWD without a matching forward saved in scratch";
+        case MOE_ERR_UNSUPPORTED: return "precision or size not supported";
+        case MOE_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case MOE_ERR_DEVICE: return "the device status word reports an error";
+        default: return "unknown status code";
+    }
+}
+
+int moe_scratch_view(const moe_desc* desc, int view, uint64_t* offset, uint64_t* bytes) {
+    Layout L;
+    if (!offset || !bytes) return MOE_ERR_NULL;
+    if (!make_layout(desc, &L)) return MOE_ERR_SHAPE;
+    const uint64_t R = L.rows, S = L.S, E = L.E, H = L.H, I = L.I;
+    switch (view) {
+        case MOE_VIEW_COUNTS: *offset = L.cnt; *bytes = E * 4; break;
+        case MOE_VIEW_OFFSETS: *offset = L.off; *bytes = (E + 1) * 4; break;
+        case MOE_VIEW_PERM: *offset = L.perm; *bytes = S * 4; break;
+        case MOE_VIEW_INV: *offset = L.inv; *bytes = S * 4; break;
+        case MOE_VIEW_PAD_OFFSETS: *offset = L.pad_off; *bytes = (E + 1) * 4; break;
+        case MOE_VIEW_XPERM: *offset = L.xperm; *bytes = R * H * 2; break;
+        case MOE_VIEW_HID: *offset = L.hid; *bytes = R * I * 2; break;
+        case MOE_VIEW_GU: *offset = L.gu; *bytes = R * 2 * I * 2; break;
+        case MOE_VIEW_YPART: *offset = L.ypart; *bytes = R * H * 2; break;
+        case MOE_VIEW_DG: *offset = L.dg; *bytes = R * 2 * I * 2; break;
+        case MOE_VIEW_HW: *offset = L.hw; *bytes = R * I * 2; break;
+        case MOE_VIEW_DYPERM: *offset = L.dyperm; *bytes = R * H * 2; break;
+        default: return MOE_ERR_SHAPE;
+    }
+    return MOE_OK;
+}
+
+int moe_trace_enable(int on) {
+    g_trace_on = on != 0;
+    return MOE_OK;
+}
+
+int moe_trace_reset(void) {
+    trace_flush();
+    for (int i = 0; i < kTraceKinds; ++i) {
+        g_trace_launches[i] = 0;
+        g_trace_ms[i] = 0.0;
+    }
+    return MOE_OK;
+}
+
+int moe_trace_read(const char** names, int64_t* launches, double* total_ms, int* n) {
+    if (!n) return MOE_ERR_NULL;
+    trace_flush();
+    int cap = *n, out = 0;
+    for (int i = 0; i < kTraceKinds; ++i) {
+        if (!g_trace_launches[i]) continue;
+        if (out < cap) {
+            if (names) names[out] = kTraceNames[i];
+            if (launches) launches[out] = g_trace_launches[i];
+            if (total_ms) total_ms[out] = g_trace_ms[i];
+        }
+        ++out;
+    }
+    *n = out;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+// rows.cu - the two HBM-bound row movers of the MoE layer.
+//
+// Dispatch and combine are the expert-parallel exchange steps of the fused layer (MarkTechPost,
+// "Prime Intellect Releases Prime Mega MoE", section "How does the fused kernel work?").  With
+// every expert on one GPU they reduce to
+//   gather  : dst[r] = src[row_slot[r] / k] for each padded routed row r (zero on padding rows),
+//   combine : out[t] = sum_j part[pos[t*k + j]], summed in fp32 in the fixed order j = 0..k-1,
+// where the routing weight has already been applied to `part` by the down-projection epilogue
+// (aggregation by routing weight: kongchang.com, "Prime Intellect推出Prime Mega MoE", section
+// "为什么 MoE 训练特别需要融合内核").  One warp moves one row with 16-byte accesses.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kRowThreads = 256;
+
+__global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint4* __restrict__ src0, uint4* __restrict__ dst0,
+                                                                   const uint4* __restrict__ src1, uint4* __restrict__ dst1,
+                                                                   const int* __restrict__ row_slot,
+                                                                   const int* __restrict__ mtile_total, int k,
+                                                                   int row_vecs) {
+    const int nrows = (*mtile_total) * kBM;
+    const int wpb = kRowThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const int stride = gridDim.x * wpb;
+    for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < nrows; r += stride) {
+        const int slot = row_slot[r];
+        uint4* d0 = dst0 + (size_t)r * row_vecs;
+        uint4* d1 = dst1 ? dst1 + (size_t)r * row_vecs : nullptr;
+        if (slot >= 0) {
+            const size_t t = (size_t)(slot / k);
+            const uint4* s0 = src0 + t * row_vecs;
+            const uint4* s1 = src1 ? src1 + t * row_vecs : nullptr;
+            int v = lane;
+            for (; v + 96 < row_vecs; v += 128) {
+                const uint4 a = __ldg(s0 + v), b = __ldg(s0 + v + 32), c = __ldg(s0 + v + 64), d = __ldg(s0 + v + 96);
+                d0[v] = a; d0[v + 32] = b; d0[v + 64] = c; d0[v + 96] = d;
+            }
+            for (; v < row_vecs; v += 32) d0[v] = __ldg(s0 + v);
+            if (s1) {
+                v = lane;
+                for (; v + 96 < row_vecs; v += 128) {
+                    const uint4 a = __ldg(s1 + v), b = __ldg(s1 + v + 32), c = __ldg(s1 + v + 64), d = __ldg(s1 + v + 96);
+                    d1[v] = a; d1[v + 32] = b; d1[v + 64] = c; d1[v + 96] = d;
+                }
+                for (; v < row_vecs; v += 32) d1[v] = __ldg(s1 + v);
+            }
+        } else {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int v = lane; v < row_vecs; v += 32) d0[v] = z;
+            if (d1)
+                for (int v = lane; v < row_vecs; v += 32) d1[v] = z;
+        }
+    }
+}
+
+// One warp per token.  Each lane owns 8 consecutive columns of every 256-column chunk.
+__global__ void __launch_bounds__(kRowThreads) combine_rows_kernel(const uint4* __restrict__ part, uint4* __restrict__ out,
+                                                                    const int* __restrict__ pos, int T, int k,
+                                                                    int row_vecs, const float* __restrict__ dtw,
+                                                                    int n_dtw, float* __restrict__ dtopk_w) {
+    const int wpb = kRowThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const int stride = gridDim.x * wpb;
+    for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += stride) {
+        const int* pt = pos + (size_t)t * k;
+        for (int v = lane; v < row_vecs; v += 32) {
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+            int j = 0;
+            for (; j + 4 <= k; j += 4) {
+                uint4 w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int p = pt[j + u];
+                    w[u] = p >= 0 ? __ldg(part + (size_t)p * row_vecs + v) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 a = unpack_bf16x2(w[u].x), b = unpack_bf16x2(w[u].y), c = unpack_bf16x2(w[u].z),
+                                 d = unpack_bf16x2(w[u].w);
+                    acc[0] += a.x; acc[1] += a.y; acc[2] += b.x; acc[3] += b.y;
+                    acc[4] += c.x; acc[5] += c.y; acc[6] += d.x; acc[7] += d.y;
+                }
+            }
+            for (; j < k; ++j) {
+                const int p = pt[j];
+                if (p < 0) continue;
+                const uint4 w = __ldg(part + (size_t)p * row_vecs + v);
+                const float2 a = unpack_bf16x2(w.x), b = unpack_bf16x2(w.y), c = unpack_bf16x2(w.z),
+                             d = unpack_bf16x2(w.w);
+                acc[0] += a.x; acc[1] += a.y; acc[2] += b.x; acc[3] += b.y;
+                acc[4] += c.x; acc[5] += c.y; acc[6] += d.x; acc[7] += d.y;
+            }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            out[(size_t)t * row_vecs + v] = o;
+        }
+        if (dtopk_w) {
+            for (int j = lane; j < k; j += 32) {
+                const int p = pt[j];
+                float s = 0.f;
+                if (p >= 0)
+                    for (int n = 0; n < n_dtw; ++n) s += dtw[(size_t)p * n_dtw + n];
+                dtopk_w[(size_t)t * k + j] = s;
+            }
+        }
+    }
+}
+
+static int row_grid(const Ctx& c) { return c.num_sms * 8; }
+
+cudaError_t launch_gather(const Ctx& c, const void* src0, void* dst0, const void* src1, void* dst1) {
+    const Layout& L = *c.L;
+    const int row_vecs = (int)(L.H * 2 / 16);
+    trace_begin(c.st, 3);
+    gather_rows_kernel<<<row_grid(c), kRowThreads, 0, c.st>>>(
+        reinterpret_cast<const uint4*>(src0), reinterpret_cast<uint4*>(dst0), reinterpret_cast<const uint4*>(src1),
+        reinterpret_cast<uint4*>(dst1), reinterpret_cast<const int*>(c.base + L.row_slot),
+        reinterpret_cast<const int*>(c.base + L.mtile) + L.E, (int)L.k, row_vecs);
+    trace_end(c.st, 3);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Ctx& c, const void* part, void* out, float* dtopk_w) {
+    const Layout& L = *c.L;
+    const int row_vecs = (int)(L.H * 2 / 16);
+    trace_begin(c.st, 4);
+    combine_rows_kernel<<<row_grid(c), kRowThreads, 0, c.st>>>(
+        reinterpret_cast<const uint4*>(part), reinterpret_cast<uint4*>(out),
+        reinterpret_cast<const int*>(c.base + L.pos), (int)L.T, (int)L.k, row_vecs,
+        reinterpret_cast<const float*>(c.base + L.dtw), (int)L.n_dtw, dtopk_w);
+    trace_end(c.st, 4);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

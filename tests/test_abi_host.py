@@ -1,0 +1,169 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads, exports every
+function `include/moe_layer.h` declares, sizes its scratch, and rejects bad arguments with the
+documented status codes before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from moe_expert_layer_permute_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bd():
+    build.build()
+    from moe_expert_layer_permute_gb300 import binding
+    return binding
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe_layer.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_function(bd):
+    declared = _declared_functions()
+    assert len(declared) >= 9
+    for name in declared:
+        assert hasattr(bd.LIB, name), name
+        ctypes.cast(getattr(bd.LIB, name), ctypes.c_void_p)
+    assert sorted(bd.EXPORTS) == declared
+
+
+def test_scratch_bytes_rules(bd):
+    ok = bd.make_desc(16384, 2048, 768, 128, 8)
+    n = bd.moe_scratch_bytes(ok)
+    assert n > 0
+    n2 = bd.moe_scratch_bytes(bd.make_desc(32768, 2048, 768, 128, 8))
+    assert n2 > n
+    for bad in [(16, 2000, 768, 8, 2), (16, 2048, 700, 8, 2), (16, 256, 128, 4, 5), (16, 256, 128, 2000, 2),
+                (-1, 256, 128, 8, 2), (16, 256, 128, 8, 0)]:
+        assert bd.moe_scratch_bytes(bd.make_desc(*bad)) == 0, bad
+    assert bd.moe_scratch_bytes(bd.make_desc(0, 256, 128, 8, 2)) > 0
+
+
+def test_scratch_views_are_disjoint_and_aligned(bd):
+    d = bd.make_desc(1000, 512, 256, 16, 4)
+    total = bd.moe_scratch_bytes(d)
+    spans = []
+    for v in range(12):
+        off, nb = ctypes.c_uint64(), ctypes.c_uint64()
+        assert bd.LIB.moe_scratch_view(ctypes.byref(d), v, ctypes.byref(off), ctypes.byref(nb)) == 0
+        assert off.value % 256 == 0 and off.value + nb.value <= total
+        spans.append((off.value, off.value + nb.value))
+    spans.sort()
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    off, nb = ctypes.c_uint64(), ctypes.c_uint64()
+    assert bd.LIB.moe_scratch_view(ctypes.byref(d), 99, ctypes.byref(off), ctypes.byref(nb)) == bd.ERR["MOE_ERR_SHAPE"]
+
+
+class _Fake:
+    """moe_tensor views with fake (never dereferenced) aligned device addresses."""
+
+    def __init__(self, bd):
+        self.bd = bd
+        self.addr = 1 << 20
+
+    def t(self, shape, dt, contiguous=True, misalign=0):
+        m = self.bd.MoeTensor()
+        m.data = self.addr + misalign
+        self.addr += 1 << 24
+        m.dtype = dt
+        m.ndim = len(shape)
+        st = 1
+        strides = []
+        for s in reversed(shape):
+            strides.append(st)
+            st *= s
+        strides = list(reversed(strides))
+        if not contiguous:
+            strides[0] *= 2
+        for i, (s, r) in enumerate(zip(shape, strides)):
+            m.shape[i] = s
+            m.stride[i] = r
+        return m
+
+
+def _fwd_args(bd, T=256, H=256, I=128, E=8, k=2, **over):
+    f = _Fake(bd)
+    a = {"x": f.t((T, H), bd.MOE_DT_BF16), "idx": f.t((T, k), bd.MOE_DT_I32), "w": f.t((T, k), bd.MOE_DT_F32),
+         "W13": f.t((E, 2 * I, H), bd.MOE_DT_BF16), "W2": f.t((E, H, I), bd.MOE_DT_BF16),
+         "y": f.t((T, H), bd.MOE_DT_BF16)}
+    a.update({k_: v(f) for k_, v in over.items()})
+    s = bd.MoeScratch()
+    s.desc = bd.make_desc(T, H, I, E, k)
+    s.bytes = bd.moe_scratch_bytes(s.desc)
+    s.data = 1 << 40
+    return a, s
+
+
+def _call_fwd(bd, a, s):
+    return bd.LIB.moe_fwd(*[ctypes.byref(a[n]) for n in ("x", "idx", "w", "W13", "W2", "y")], ctypes.byref(s), None)
+
+
+@pytest.mark.parametrize("over,code", [
+    ({"x": lambda f: f.t((256, 512), 0)}, "MOE_ERR_SHAPE"),
+    ({"idx": lambda f: f.t((256, 2), 1)}, "MOE_ERR_DTYPE"),
+    ({"w": lambda f: f.t((256, 2), 0)}, "MOE_ERR_DTYPE"),
+    ({"W13": lambda f: f.t((8, 256, 256), 0, contiguous=False)}, "MOE_ERR_LAYOUT"),
+    ({"y": lambda f: f.t((256, 256), 0, misalign=8)}, "MOE_ERR_ALIGN"),
+    ({"W2": lambda f: f.t((8, 128, 256), 0)}, "MOE_ERR_SHAPE"),
+])
+def test_fwd_rejects_bad_tensors(bd, over, code):
+    a, s = _fwd_args(bd, **over)
+    assert _call_fwd(bd, a, s) == bd.ERR[code]
+
+
+def test_fwd_rejects_bad_scratch_and_desc(bd):
+    a, s = _fwd_args(bd)
+    s.bytes -= 1
+    assert _call_fwd(bd, a, s) == bd.ERR["MOE_ERR_SCRATCH"]
+    a, s = _fwd_args(bd)
+    s.data = (1 << 40) + 64
+    assert _call_fwd(bd, a, s) == bd.ERR["MOE_ERR_SCRATCH"]
+    a, s = _fwd_args(bd)
+    s.desc.H = 384
+    assert _call_fwd(bd, a, s) == bd.ERR["MOE_ERR_SHAPE"]
+    a, s = _fwd_args(bd)
+    s.desc.precision = 7
+    assert _call_fwd(bd, a, s) == bd.ERR["MOE_ERR_UNSUPPORTED"]
+    assert bd.LIB.moe_fwd(None, None, None, None, None, None, None, None) == bd.ERR["MOE_ERR_NULL"]
+
+
+def test_bwd_reuse_needs_a_saved_forward(bd):
+    a, s = _fwd_args(bd)
+    f = _Fake(bd)
+    f.addr = 1 << 36
+    dy = f.t((256, 256), 0); dx = f.t((256, 256), 0)
+    dW13 = f.t((8, 256, 256), 1); dW2 = f.t((8, 256, 128), 1); dtw = f.t((256, 2), 1)
+    s.desc.flags = bd.MOE_FLAG_REUSE_FWD
+    rc = bd.LIB.moe_bwd(ctypes.byref(dy), *[ctypes.byref(a[n]) for n in ("x", "idx", "w", "W13", "W2")],
+                        ctypes.byref(dx), ctypes.byref(dW13), ctypes.byref(dW2), ctypes.byref(dtw),
+                        ctypes.byref(s), None)
+    assert rc == bd.ERR["MOE_ERR_STATE"]
+    dW2_bad = f.t((8, 256, 128), 2)
+    s.desc.flags = 0
+    rc = bd.LIB.moe_bwd(ctypes.byref(dy), *[ctypes.byref(a[n]) for n in ("x", "idx", "w", "W13", "W2")],
+                        ctypes.byref(dx), ctypes.byref(dW13), ctypes.byref(dW2_bad), ctypes.byref(dtw),
+                        ctypes.byref(s), None)
+    assert rc == bd.ERR["MOE_ERR_DTYPE"]
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a CUDA device")
+def test_valid_call_without_a_device_reports_cuda_error(bd):
+    a, s = _fwd_args(bd)
+    assert _call_fwd(bd, a, s) == bd.ERR["MOE_ERR_CUDA"]
+
+
+def test_strerror_and_trace_api(bd):
+    for code in bd.ERRORS:
+        assert bd.strerror(code)
+    assert "unknown" in bd.strerror(-1234)
+    bd.moe_trace_reset()
+    assert bd.moe_trace_read() == {}
