@@ -128,12 +128,15 @@ static int check_tensor(const moe_tensor* t, int dtype, int ndim, int64_t s0, in
     for (int i = 0; i < ndim; ++i)
         if (t->shape[i] != want[i]) return MOE_ERR_SHAPE;
     if (t->dtype != dtype) return MOE_ERR_DTYPE;
+    int64_t numel = 1;
+    for (int i = 0; i < ndim; ++i) numel *= t->shape[i];
+    if (numel == 0) return MOE_OK;  // an empty tensor is never dereferenced
     int64_t expect = 1;
     for (int i = ndim - 1; i >= 0; --i) {
         if (t->shape[i] > 1 && t->stride[i] != expect) return MOE_ERR_LAYOUT;
         expect *= t->shape[i];
     }
-    if (expect > 0 && !t->data) return MOE_ERR_NULL;
+    if (!t->data) return MOE_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0) return MOE_ERR_ALIGN;
     return MOE_OK;
 }
