@@ -67,6 +67,9 @@ CONFIGS = {
                                  routing="zipf", seed=1004),
     "skew_zipf_4k": LayerConfig("skew_zipf_4k", T=4096, H=2048, I=768, E=128, k=8,
                                 routing="zipf", seed=1004),
+    # the 30B layer shape at a quarter of the tokens: inputs still larger than L2, a few GB on the
+    # device, small enough for a many-pass profiler capture
+    "profile_30b_t4096": LayerConfig("profile_30b_t4096", T=4096, H=2048, I=768, E=128, k=8, seed=1001),
 }
 
 
