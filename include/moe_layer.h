@@ -131,6 +131,25 @@ int moe_read_device_status(moe_scratch* scratch, void* stream, int* status);
 /* Static message for a MOE_ERR_* code. */
 const char* moe_strerror(int code);
 
+/* ---- routing without caller-provided scratch ---------------------------------------------- */
+/* The pages have no counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory or hand over a scratch buffer (code running inside an allocator's hooks, runtimes
+ * that reserve all device memory up front and forbid later allocations, loops where an allocation
+ * would synchronise the device).  It computes the same routing bookkeeping as moe_fwd:
+ *   counts  int32[E]     tokens routed to each expert
+ *   offsets int32[E+1]   exclusive prefix of counts
+ *   perm    int32[T*k]   slot at each sorted position, stable in slot order s = t*k + j
+ *   inv     int32[T*k]   sorted position of each slot (-1 for a slot whose id is outside [0, E))
+ * from topk_idx int32[T, k] (all device pointers, 4-byte aligned, caller-owned), asynchronously on
+ * `stream`.  It allocates nothing: its working memory is a file-scope static device array of
+ * 65536 int32 (256 KiB) that every GPU loading the library holds until exit.  Sizes with
+ * 2 * ceil(T*k / 2048) * E > 65536 are rejected with MOE_ERR_UNSUPPORTED before any launch.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) and caches
+ * it; make that first call before any stream capture.  Calls share the array: calls whose kernels
+ * may overlap on the GPU (unordered streams) race on it and must not be issued. */
+int moe_route_static(const int32_t* topk_idx, int64_t T, int64_t k, int64_t E, int32_t* counts,
+                     int32_t* offsets, int32_t* perm, int32_t* inv, void* stream);
+
 /* ---- introspection (tests, tracing) ------------------------------------------------------- */
 /* Named regions of the scratch buffer, valid after a call on that scratch.  Layouts:
  *   MOE_VIEW_COUNTS   int32[E]        tokens routed to each expert

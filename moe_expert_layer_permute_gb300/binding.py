@@ -28,7 +28,7 @@ ERR = {v: k for k, v in ERRORS.items()}
 
 # every symbol the header declares
 EXPORTS = ("moe_scratch_bytes", "moe_fwd", "moe_bwd", "moe_read_device_status", "moe_strerror",
-           "moe_scratch_view", "moe_trace_enable", "moe_trace_reset", "moe_trace_read")
+           "moe_scratch_view", "moe_trace_enable", "moe_trace_reset", "moe_trace_read", "moe_route_static")
 
 
 class MoeTensor(ctypes.Structure):
@@ -72,6 +72,9 @@ def _load() -> ctypes.CDLL:
     lib.moe_trace_reset.restype = ctypes.c_int
     lib.moe_trace_read.argtypes = [_P(ctypes.c_char_p), _P(ctypes.c_int64), _P(ctypes.c_double), _P(ctypes.c_int)]
     lib.moe_trace_read.restype = ctypes.c_int
+    lib.moe_route_static.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + \
+        [ctypes.c_void_p] * 5
+    lib.moe_route_static.restype = ctypes.c_int
     return lib
 
 
@@ -185,3 +188,18 @@ def moe_trace_read() -> dict:
     n = ctypes.c_int(cap)
     LIB.moe_trace_read(names, launches, ms, ctypes.byref(n))
     return {names[i].decode(): (int(launches[i]), float(ms[i])) for i in range(min(n.value, cap))}
+
+
+def moe_route_static(topk_idx, E: int, counts, offsets, perm, inv, stream=None) -> None:
+    """Routing bookkeeping into caller-owned int32 tensors, with no scratch buffer (the library's
+    static device array instead): counts [E], offsets [E+1], perm [T*k], inv [T*k]."""
+    T, k = topk_idx.shape
+    for t in (topk_idx, counts, offsets, perm, inv):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise MoeError(ERR["MOE_ERR_DTYPE"], "moe_route_static")
+    if counts.numel() != E or offsets.numel() != E + 1 or perm.numel() != T * k or inv.numel() != T * k:
+        raise MoeError(ERR["MOE_ERR_SHAPE"], "moe_route_static")
+    rc = LIB.moe_route_static(topk_idx.data_ptr(), T, k, E, counts.data_ptr(), offsets.data_ptr(),
+                              perm.data_ptr(), inv.data_ptr(), _stream_ptr(stream))
+    if rc:
+        raise MoeError(rc, "moe_route_static")
