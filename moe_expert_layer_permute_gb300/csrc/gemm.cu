@@ -13,8 +13,10 @@
 //               (128-byte swizzle) and counts their bytes on a per-stage mbarrier;
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16) into one of two
 //               TMEM accumulators and releases each smem stage with tcgen05.commit;
-//   warps 2..5  epilogue: tcgen05.ld the finished accumulator (one TMEM lane = one row per
-//               thread), apply the fused epilogue and store to global memory, then release the
+//   warps 2..   epilogue (4 warps, or 8 for the SwiGLU backward): tcgen05.ld the finished
+//               accumulator (one TMEM lane = one row per thread; warp w reads lane quarter w % 4,
+//               and with 8 warps the two warps of a quarter take alternate 32-column chunks),
+//               apply the fused epilogue and store to global memory, then release the
 //               accumulator, so the epilogue of tile i overlaps the MMAs of tile i+1.
 // Routed rows are laid out per expert padded to multiples of 128, so a row tile belongs to one
 // expert and a weight-gradient K slice never crosses into the next expert's rows.
@@ -29,11 +31,16 @@
 namespace moe {
 
 constexpr int kStages = 4;
-constexpr int kEpiWarps = 4;
-constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_GU_ONLY, EPI_WEIGHTED, EPI_SWIGLU_BWD, EPI_PLAIN, EPI_WGRAD };
+
+// Epilogue warps: the SwiGLU backward reads [g|u] and writes three outputs per element and needs
+// two warps per TMEM lane quarter to keep up with the MMAs; the other epilogues use one.
+template <int EPI>
+constexpr int epi_warps() { return EPI == EPI_SWIGLU_BWD ? 8 : 4; }
+template <int EPI>
+constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI>(); }
 
 struct GemmArgs {
     const int* mtile;          // [E+1] prefix of 128-row tiles per expert
@@ -43,7 +50,7 @@ struct GemmArgs {
     const __nv_bfloat16* gu;   // [rows, 2I] saved pre-activations (SwiGLU backward)
     void* out0;
     void* out1;
-    float* dtw;                // [rows, n_tiles] partial <dA, h> per n-tile
+    float* dtw;                // [rows, 2 * n_tiles] partial <dA, h> per n-tile and column half
     int* status;
     int E, I;
     int n_tiles, m_tiles, k_blocks;
@@ -100,13 +107,15 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs a) {
     constexpr int kBTileBytes = BN * kBK * 2;
     constexpr int kStageBytes = kATileBytes + kBTileBytes;
     constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, A_MN, B_MN);
     constexpr uint32_t kTmemCols = 2 * BN;
+    constexpr int kEpiWarps = epi_warps<EPI>();
+    constexpr int kHalves = kEpiWarps / 4;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -235,6 +244,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;               // TMEM lanes [32*quarter, 32*quarter + 32)
+        const int half = (warp - 2) >> 2;           // which alternate 32-column chunks (8 warps)
         const int r = quarter * 32 + lane;          // row of the tile owned by this thread
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         int acc = 0;
@@ -251,7 +261,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 __nv_bfloat16* hid = reinterpret_cast<__nv_bfloat16*>(a.out0);
                 __nv_bfloat16* gu = reinterpret_cast<__nv_bfloat16*>(a.out1);
 #pragma unroll 1
-                for (int c = 0; c < BN / 64; ++c) {
+                for (int c = half; c < BN / 64; c += kHalves) {
                     float u[32];
                     tmem_ld32(tacc + 32 * c, v);
                     tmem_ld32(tacc + BN / 2 + 32 * c, u);
@@ -270,7 +280,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const float w = slot >= 0 ? a.topk_w[slot] : 0.f;
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out0);
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = half; c < BN / 32; c += kHalves) {
                     tmem_ld32(tacc + 32 * c, v);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] *= w;
@@ -284,7 +294,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const __nv_bfloat16* gurow = a.gu + grow * (2LL * a.I);
                 float dot = 0.f;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = half; c < BN / 32; c += kHalves) {
                     float g[32], u[32];
                     tmem_ld32(tacc + 32 * c, v);   // dA
                     const int col = t.n0 + 32 * c;
@@ -307,18 +317,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     store_bf16x32(dG + grow * (2LL * a.I) + a.I + col, u);
                     store_bf16x32(hw + grow * (long long)a.I + col, v);
                 }
-                a.dtw[grow * a.n_tiles + t.nt] = dot;
+                a.dtw[grow * (2 * a.n_tiles) + 2 * t.nt + half] = dot;
             } else if constexpr (EPI == EPI_PLAIN) {
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out0);
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = half; c < BN / 32; c += kHalves) {
                     tmem_ld32(tacc + 32 * c, v);
                     store_bf16x32(out + grow * (long long)a.ld0 + t.n0 + 32 * c, v);
                 }
             } else {  // EPI_WGRAD
                 const long long off = (long long)t.e * a.out_e_stride + grow * a.ld0 + t.n0;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = half; c < BN / 32; c += kHalves) {
                     if (t.kb > 0) {
                         tmem_ld32(tacc + 32 * c, v);
                     } else {
@@ -391,7 +401,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
                                         1024 + kStages * (kATileBytes + BN * kBK * 2) + 128 + (kMaxExperts + 1) * 4);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    kern<<<c.num_sms, kGemmThreads, smem, c.st>>>(ta, tb, a);
+    kern<<<c.num_sms, gemm_threads<EPI>(), smem, c.st>>>(ta, tb, a);
     return cudaGetLastError();
 }
 

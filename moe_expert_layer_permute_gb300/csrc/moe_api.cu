@@ -31,7 +31,7 @@ bool make_layout(const moe_desc* d, Layout* L) {
     if (rows >= (int64_t)INT32_MAX / 2) return false;
     L->T = d->T; L->H = d->H; L->I = d->I; L->E = d->E; L->k = d->k; L->S = S; L->rows = rows;
     L->nb_route = (S + kRouteChunk - 1) / kRouteChunk;
-    L->n_dtw = d->I / bwd_down_bn(d->I);
+    L->n_dtw = 2 * (d->I / bwd_down_bn(d->I));  // two column halves per n-tile
     const size_t A = 4096;
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, A); return at; };

@@ -70,6 +70,9 @@ CONFIGS = {
     # the 30B layer shape at a quarter of the tokens: inputs still larger than L2, a few GB on the
     # device, small enough for a many-pass profiler capture
     "profile_30b_t4096": LayerConfig("profile_30b_t4096", T=4096, H=2048, I=768, E=128, k=8, seed=1001),
+    # the 30B layer's per-expert work (about 1024 routed rows per expert) on 32 experts: the
+    # GEMMs' arithmetic intensity of the full workload at a quarter of its device footprint
+    "profile_30b_e32": LayerConfig("profile_30b_e32", T=4096, H=2048, I=768, E=32, k=8, seed=1001),
 }
 
 
