@@ -29,9 +29,10 @@
  *     legacy default stream) and never synchronise.  Outputs are overwritten, not accumulated.
  *   - Errors: arguments are validated on the host before anything is launched; a negative
  *     MOE_ERR_* code is returned and nothing is enqueued.  A launch failure returns MOE_ERR_CUDA.
- *     Device-side problems (an expert id out of range under MOE_FLAG_DEBUG_CHECK, a pipeline wait
- *     that timed out) never trap: the kernels record a code in the scratch status word, which
- *     moe_read_device_status returns.
+ *     Device-side problems (an expert id outside [0, E), a pipeline wait that timed out) never
+ *     trap: the kernels record a code in the scratch status word, which moe_read_device_status
+ *     returns.  Out-of-range expert ids are always checked on the device and such slots are
+ *     dropped (they contribute nothing; their dtopk_w is 0).
  *   - Alignment: every device pointer must be 16-byte aligned (TMA); the scratch pointer 256-byte.
  *   - T == 0 is a valid no-op (dW13 / dW2 are zeroed by moe_bwd).
  *   - Calls that share one scratch buffer must be ordered on one stream.
@@ -74,8 +75,6 @@ typedef struct {
  * that had MOE_FLAG_SAVE_GU and the same x, topk_idx, topk_w, W13, W2 pointers and desc; returns
  * MOE_ERR_STATE if the scratch handle does not record such a forward. */
 #define MOE_FLAG_REUSE_FWD   0x2u
-/* Kernels check 0 <= topk_idx < E and record MOE_DEV_BAD_EXPERT instead of reading out of range. */
-#define MOE_FLAG_DEBUG_CHECK 0x4u
 
 /* Host-side handle of a caller-owned device scratch buffer of at least moe_scratch_bytes(desc)
  * bytes.  `state` is written by the library (which forward's results the buffer holds); zero it
@@ -102,7 +101,7 @@ typedef struct {
 
 /* device status word codes (moe_read_device_status) */
 #define MOE_DEV_OK            0
-#define MOE_DEV_BAD_EXPERT    1   /* an expert id outside [0, E) (MOE_FLAG_DEBUG_CHECK) */
+#define MOE_DEV_BAD_EXPERT    1   /* an expert id outside [0, E) was dropped */
 #define MOE_DEV_TIMEOUT       2   /* a pipeline wait gave up; the kernel exited early */
 
 /* ---- sizes -------------------------------------------------------------------------------- */
