@@ -290,31 +290,45 @@ def forward_tokens(x, topk_idx, topk_w, W13, W2, tokens, *, mxfp8: bool = False)
     return out
 
 
-def backward_tokens(dy, x, topk_idx, topk_w, W13, W2, tokens):
-    """dx[t] and dtopk_w[t, :] for the listed tokens only (BF16 arithmetic, fp64)."""
+def _row_qdq(v):
+    return mx_qdq(v[None], axis=1)[0]
+
+
+def backward_tokens(dy, x, topk_idx, topk_w, W13, W2, tokens, *, mxfp8: bool = False):
+    """dx[t] and dtopk_w[t, :] for the listed tokens only (fp64), with the quantisation points of
+    `backward` in MXFP8 mode: x and dy along H, W13 along H (forward) and along 2I (dgrad), W2
+    along H (dgrad), [dg|du] along 2I."""
     I = W13.shape[1] // 2
     k = topk_idx.shape[1]
     dx = np.zeros((len(tokens), x.shape[1]))
     dtw = np.zeros((len(tokens), k))
     for n, t in enumerate(tokens):
         xt, dyt = _as64(x[t]), _as64(dy[t])
+        if mxfp8:
+            xt, dyt = _row_qdq(xt), _row_qdq(dyt)
         for j in range(k):
             e = int(topk_idx[t, j])
             W = _as64(W13[e]); Wd = _as64(W2[e])
-            g = W[:I] @ xt
-            u = W[I:] @ xt
+            Wf = mx_qdq(W, axis=1) if mxfp8 else W          # forward: contraction over H
+            Wb = mx_qdq(W, axis=0) if mxfp8 else W          # dgrad: contraction over 2I
+            Wdb = mx_qdq(Wd, axis=0) if mxfp8 else Wd       # dgrad: contraction over H
+            g = Wf[:I] @ xt
+            u = Wf[I:] @ xt
             sg = sigmoid(g)
-            dA = Wd.T @ dyt
+            dA = Wdb.T @ dyt
             dtw[n, j] = dA @ (silu(g) * u)
             dh = float(topk_w[t, j]) * dA
-            dg = dh * u * sg * (1.0 + g * (1.0 - sg))
-            du = dh * g * sg
-            dx[n] += W[:I].T @ dg + W[I:].T @ du
+            dG = np.concatenate([dh * u * sg * (1.0 + g * (1.0 - sg)), dh * g * sg])
+            if mxfp8:
+                dG = _row_qdq(dG)
+            dx[n] += Wb.T @ dG
     return dx, dtw
 
 
-def wgrad_experts(dy, x, topk_idx, topk_w, W13, W2, experts):
-    """(dW13[e], dW2[e]) for the listed experts only (BF16 arithmetic, fp64)."""
+def wgrad_experts(dy, x, topk_idx, topk_w, W13, W2, experts, *, mxfp8: bool = False):
+    """(dW13[e], dW2[e]) for the listed experts only (fp64).  In MXFP8 mode the forward and dgrad
+    operands are quantised as in `backward`, and the weight-gradient operands along the expert's
+    tokens in slot order (blocks of 32 from the group's first token, zero-padded tail)."""
     I = W13.shape[1] // 2
     k = topk_idx.shape[1]
     flat = np.asarray(topk_idx).reshape(-1)
@@ -325,15 +339,21 @@ def wgrad_experts(dy, x, topk_idx, topk_w, W13, W2, experts):
         t = slots // k
         X = _as64(x[t]); dY = _as64(dy[t]); w = wflat[slots][:, None]
         W = _as64(W13[e]); Wd = _as64(W2[e])
-        g = X @ W[:I].T
-        u = X @ W[I:].T
+        Xf, dYb, Wf, Wdb = X, dY, W, Wd
+        if mxfp8:
+            Xf, dYb = mx_qdq(X, axis=1), mx_qdq(dY, axis=1)
+            Wf, Wdb = mx_qdq(W, axis=1), mx_qdq(Wd, axis=0)
+        g = Xf @ Wf[:I].T
+        u = Xf @ Wf[I:].T
         sg = sigmoid(g)
         h = g * sg * u
-        dA = dY @ Wd
+        dA = dYb @ Wdb
         dh = w * dA
-        dg = dh * u * sg * (1.0 + g * (1.0 - sg))
-        du = dh * g * sg
-        dW13_e = np.concatenate([dg.T @ X, du.T @ X], axis=0)
-        dW2_e = dY.T @ (w * h)
-        res.append((dW13_e, dW2_e))
+        dG = np.concatenate([dh * u * sg * (1.0 + g * (1.0 - sg)), dh * g * sg], axis=1)
+        Hw = w * h
+        if mxfp8 and len(slots):
+            seg = np.array([0, len(slots)])
+            dY, Hw = mx_qdq_segments(dY, seg), mx_qdq_segments(Hw, seg)
+            dG, X = mx_qdq_segments(dG, seg), mx_qdq_segments(X, seg)
+        res.append((dG.T @ X, dY.T @ Hw))
     return res

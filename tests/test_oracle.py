@@ -183,6 +183,13 @@ def test_sampled_forms_agree_with_full():
     yq = oracle.forward(x, idx, w, W13, W2, mxfp8=True)
     np.testing.assert_allclose(oracle.forward_tokens(x, idx, w, W13, W2, toks, mxfp8=True), yq[toks],
                                rtol=1e-11, atol=1e-12)
+    gq = oracle.backward(dy, x, idx, w, W13, W2, mxfp8=True)
+    dxq, dtwq = oracle.backward_tokens(dy, x, idx, w, W13, W2, toks, mxfp8=True)
+    np.testing.assert_allclose(dxq, gq["dx"][toks], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dtwq, gq["dtopk_w"][toks], rtol=1e-11, atol=1e-12)
+    for e, (a, b) in zip([1, 4], oracle.wgrad_experts(dy, x, idx, w, W13, W2, [1, 4], mxfp8=True)):
+        np.testing.assert_allclose(a, gq["dW13"][e], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(b, gq["dW2"][e], rtol=1e-11, atol=1e-12)
 
 
 # ---------------------------------------------------------------- planted mistakes must be caught
