@@ -75,6 +75,11 @@ typedef struct {
  * that had MOE_FLAG_SAVE_GU and the same x, topk_idx, topk_w, W13, W2 pointers and desc; returns
  * MOE_ERR_STATE if the scratch handle does not record such a forward. */
 #define MOE_FLAG_REUSE_FWD   0x2u
+/* MXFP8 only: W13 and W2 hold the same values as when an earlier call on this scratch (same
+ * pointers) quantised them, so their E4M3 copies in scratch are reused instead of being made
+ * again (a training step quantises its weights once: forward, recompute and backward share them).
+ * Returns MOE_ERR_STATE if the scratch handle records no quantisation of these pointers. */
+#define MOE_FLAG_REUSE_WEIGHTS 0x4u
 
 /* Host-side handle of a caller-owned device scratch buffer of at least moe_scratch_bytes(desc)
  * bytes.  `state` is written by the library (which forward's results the buffer holds); zero it
@@ -169,6 +174,22 @@ enum {
     MOE_VIEW_COUNTS = 0, MOE_VIEW_OFFSETS, MOE_VIEW_PERM, MOE_VIEW_INV, MOE_VIEW_PAD_OFFSETS,
     MOE_VIEW_XPERM, MOE_VIEW_HID, MOE_VIEW_GU, MOE_VIEW_YPART, MOE_VIEW_DG, MOE_VIEW_HW,
     MOE_VIEW_DYPERM, MOE_VIEW_COUNT_
+};
+/* MXFP8 operand copies (precision MOE_MXFP8 only): for each operand a uint8 E4M3 value array in
+ * the source's layout, then its E8M0 scales (one byte per 32 values) in tensor-core atoms of 128
+ * MN-rows x 4 K-blocks (512 bytes: MN-row m, K-block b at byte 16*(m%32) + 4*((m/32)%4) + b%4;
+ * atom (m/128, b/4) at ((m/128) * (K/128) + b/4) * 512).  "_R" copies are blocked along the row
+ * (MN = rows, K = columns), "_C" copies along the column (MN = columns, K = rows).
+ * W13_R stores each expert's rows in 128-row blocks of [64 gate rows | 64 up rows]. */
+enum {
+    MOE_VIEW_MX_X_R = 32, MOE_VIEW_MX_X_R_SF, MOE_VIEW_MX_X_C, MOE_VIEW_MX_X_C_SF,
+    MOE_VIEW_MX_H_R, MOE_VIEW_MX_H_R_SF,
+    MOE_VIEW_MX_DY_R, MOE_VIEW_MX_DY_R_SF, MOE_VIEW_MX_DY_C, MOE_VIEW_MX_DY_C_SF,
+    MOE_VIEW_MX_DG_R, MOE_VIEW_MX_DG_R_SF, MOE_VIEW_MX_DG_C, MOE_VIEW_MX_DG_C_SF,
+    MOE_VIEW_MX_HW_C, MOE_VIEW_MX_HW_C_SF,
+    MOE_VIEW_MX_W13_R, MOE_VIEW_MX_W13_R_SF, MOE_VIEW_MX_W13_C, MOE_VIEW_MX_W13_C_SF,
+    MOE_VIEW_MX_W2_R, MOE_VIEW_MX_W2_R_SF, MOE_VIEW_MX_W2_C, MOE_VIEW_MX_W2_C_SF,
+    MOE_VIEW_MX_END_
 };
 int moe_scratch_view(const moe_desc* desc, int view, uint64_t* offset, uint64_t* bytes);
 

@@ -17,10 +17,14 @@ from . import build as _build
 # ---- C structures ---------------------------------------------------------------------------
 MOE_BF16, MOE_MXFP8 = 0, 1
 MOE_DT_BF16, MOE_DT_F32, MOE_DT_I32 = 0, 1, 2
-MOE_FLAG_SAVE_GU, MOE_FLAG_REUSE_FWD = 0x1, 0x2
+MOE_FLAG_SAVE_GU, MOE_FLAG_REUSE_FWD, MOE_FLAG_REUSE_WEIGHTS = 0x1, 0x2, 0x4
 (MOE_VIEW_COUNTS, MOE_VIEW_OFFSETS, MOE_VIEW_PERM, MOE_VIEW_INV, MOE_VIEW_PAD_OFFSETS, MOE_VIEW_XPERM,
  MOE_VIEW_HID, MOE_VIEW_GU, MOE_VIEW_YPART, MOE_VIEW_DG, MOE_VIEW_HW, MOE_VIEW_DYPERM) = range(12)
 MOE_DEV_OK, MOE_DEV_BAD_EXPERT, MOE_DEV_TIMEOUT = 0, 1, 2
+MX_VIEWS = {name: 32 + i for i, name in enumerate(
+    ["x_r", "x_r_sf", "x_c", "x_c_sf", "h_r", "h_r_sf", "dy_r", "dy_r_sf", "dy_c", "dy_c_sf", "dg_r", "dg_r_sf",
+     "dg_c", "dg_c_sf", "hw_c", "hw_c_sf", "w13_r", "w13_r_sf", "w13_c", "w13_c_sf", "w2_r", "w2_r_sf", "w2_c",
+     "w2_c_sf"])}
 ERRORS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_DTYPE", -4: "MOE_ERR_LAYOUT",
           -5: "MOE_ERR_ALIGN", -6: "MOE_ERR_SCRATCH", -7: "MOE_ERR_STATE", -8: "MOE_ERR_UNSUPPORTED",
           -9: "MOE_ERR_CUDA", -10: "MOE_ERR_DEVICE"}

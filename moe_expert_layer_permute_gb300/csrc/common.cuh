@@ -86,6 +86,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
         : "memory");
 }
 
+// Plain bulk copy global -> shared (both addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ------------------------------------------------------------------------------------------
 // tcgen05: tensor memory, MMA, commit, loads
 // ------------------------------------------------------------------------------------------
@@ -110,6 +119,25 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// D[tmem] (+)= (A * 2^sfA) * (B * 2^sfB)^T with E4M3 A/B and one E8M0 scale per 32 K-elements
+// (kind::mxf8f6f4, block_scale, scale_vec::1X); scales are read from tensor memory.
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copy 32 rows x 128 bits from shared memory to tensor memory, replicated into all four 32-lane
+// quarters (4 columns): one 512-byte scale-factor atom.
+__device__ __forceinline__ void tmem_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Arrive (once) on an mbarrier when every tcgen05 operation issued so far by this thread is done.
@@ -148,6 +176,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Descriptor of an unswizzled shared-memory block whose 8-row x 16-byte core matrices are
+// `sbo` bytes apart (used for the 512-byte scale-factor atoms: rows of 16 bytes, SBO = 128).
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A/B, fp32 D and E8M0 block scales;
+// sfa_id / sfb_id select the byte (K-block) of the 32-bit scale column each MMA reads.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, bool a_mn_major, bool b_mn_major, uint32_t sfa_id,
+                                                  uint32_t sfb_id) {
+    return ((sfb_id & 3u) << 4)                        // B scale-factor id
+           | (0u << 7) | (0u << 10)                    // A, B: E4M3
+           | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | (1u << 23)     // scales are UE8M0
+           | ((uint32_t)(M >> 4) << 24) | ((sfa_id & 3u) << 29);
 }
 
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.

@@ -5,14 +5,17 @@
 // the fused kernel work?"); a grouped GEMM packs many differently sized per-expert products into
 // one launch indexed by group offsets (kongchang.com, "Prime Intellect推出Prime Mega MoE", section
 // "为什么 MoE 训练特别需要融合内核").  The backward adds the activation- and weight-gradient
-// products (ic.work analysis, section "从 3.11 倍到 1.32 倍的性能漏斗").
+// products (ic.work analysis, section "从 3.11 倍到 1.32 倍的性能漏斗").  Operands are BF16, or
+// MXFP8 (E4M3 with one E8M0 scale per 32 elements along K) on the block-scaled MMA.
 //
-// One kernel template serves all seven products.  Each CTA is persistent (one per SM) and walks a
-// static list of 128 x BN output tiles; its warps are specialised:
-//   warp 0      TMA producer: loads 64-deep K slices of A and B into a 4-stage smem ring
-//               (128-byte swizzle) and counts their bytes on a per-stage mbarrier;
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16) into one of two
-//               TMEM accumulators and releases each smem stage with tcgen05.commit;
+// One kernel template serves all seven products in both precisions.  Each CTA is persistent (one
+// per SM) and walks a static list of 128 x BN output tiles; its warps are specialised:
+//   warp 0      TMA producer: loads 128-byte-deep K slices of A and B (64 bf16 or 128 E4M3
+//               elements) into a 4-stage smem ring (128-byte swizzle), plus for MXFP8 the
+//               512-byte scale-factor atoms of the slice, and counts the bytes on an mbarrier;
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN; K=16 bf16 or K=32 E4M3,
+//               for MXFP8 after tcgen05.cp of the scale atoms into TMEM) into one of two TMEM
+//               accumulators and releases each smem stage with tcgen05.commit;
 //   warps 2..   epilogue (4 warps, or 8 for the SwiGLU backward): tcgen05.ld the finished
 //               accumulator (one TMEM lane = one row per thread; warp w reads lane quarter w % 4,
 //               and with 8 warps the two warps of a quarter take alternate 32-column chunks),
@@ -31,7 +34,9 @@
 namespace moe {
 
 constexpr int kStages = 4;
-constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
+constexpr int kRowBytes = 128;                       // bytes of K per smem row (128-byte swizzle)
+constexpr int kATileBytes = kBM * kRowBytes;         // 16 KB
+constexpr int kSfAtom = 512;                         // 128 MN x 4 K-blocks of E8M0 scales
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_GU_ONLY, EPI_WEIGHTED, EPI_SWIGLU_BWD, EPI_PLAIN, EPI_WGRAD };
 
@@ -58,6 +63,11 @@ struct GemmArgs {
     int ld0;                   // row pitch of out0 in elements
     long long out_e_stride;    // weight gradients: elements per expert
     int out_f32, save_gu;
+    // MXFP8 scale factors (atoms of 512 bytes, see quant.cu): atom (mn_tile, k_tile) of an
+    // operand is at sf + (mn_tile * kt + k_tile) * 512
+    const uint8_t* sfA;
+    const uint8_t* sfB;
+    int sfA_kt, sfB_kt;
 };
 
 struct Tile {
@@ -73,7 +83,9 @@ __device__ __forceinline__ int find_expert(const int* s_mtile, int E, int gm) {
     return lo;
 }
 
-template <int BN, bool WGRAD, bool SPLIT>
+// kElems: K elements per pipeline stage (64 bf16, 128 E4M3); a 128-row group holds
+// 128 / kElems stages of a weight-gradient contraction.
+template <int BN, bool WGRAD, bool SPLIT, int kElems>
 __device__ __forceinline__ Tile decode_tile(int L, const GemmArgs& a, const int* s_mtile) {
     Tile t;
     if (!WGRAD) {
@@ -94,7 +106,7 @@ __device__ __forceinline__ Tile decode_tile(int L, const GemmArgs& a, const int*
         t.m0 = mt * kBM;
         t.n0 = t.nt * BN;
         t.row0 = s_mtile[t.e] * kBM;
-        t.kb = (s_mtile[t.e + 1] - s_mtile[t.e]) * (kBM / kBK);
+        t.kb = (s_mtile[t.e + 1] - s_mtile[t.e]) * (kBM / kElems);
     }
     return t;
 }
@@ -106,22 +118,34 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
         if (clock64() - t0 > kWaitTimeoutCycles / 8) break;
 }
 
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI>
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs a) {
-    constexpr int kBTileBytes = BN * kBK * 2;
-    constexpr int kStageBytes = kATileBytes + kBTileBytes;
+    constexpr int kElems = MX ? 128 : 64;                // K elements per stage
+    constexpr int kMmaK = MX ? 32 : 16;                  // K elements per MMA
+    constexpr int kMnChunk = MX ? 128 : 64;              // MN elements per 128-byte row (MN-major)
+    constexpr int kBTileBytes = BN * kRowBytes;
+    constexpr int kSfBAtoms = BN / 128;
+    constexpr int kSfBytes = MX ? kSfAtom * (1 + kSfBAtoms) : 0;
+    constexpr int kStageBytes = kATileBytes + kBTileBytes + kSfBytes;
     constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, A_MN, B_MN);
-    constexpr uint32_t kTmemCols = 2 * BN;
+    constexpr uint32_t kSfCols = 4 * (1 + kSfBAtoms);    // TMEM columns of one stage's scales
+    constexpr uint32_t kTmemCols = MX ? 512 : 2 * BN;
     constexpr int kEpiWarps = epi_warps<EPI>();
     constexpr int kHalves = kEpiWarps / 4;
+    // MN-major operands: the next kMnChunk MN values start one chunk (kElems rows of 128 B) on
+    constexpr uint32_t kMnLbo = kElems * kRowBytes;
+    constexpr uint32_t kMnStep = kMmaK * kRowBytes;      // MN-major: bytes per MMA K step
+    constexpr uint32_t kKStep = kMmaK * (MX ? 1 : 2);    // K-major: bytes per MMA K step
+    static_assert(!MX || BN == 128, "MXFP8 tiles are 128 x 128 (accumulators and scales share TMEM)");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + kStages * kATileBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBTileBytes);
+    uint8_t* sSF = sB + kStages * kBTileBytes;           // MXFP8: per stage A atom then B atoms
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sSF + kStages * kSfBytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
     uint64_t* tfull = bars + 2 * kStages;
@@ -165,30 +189,59 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             long long issued = 0;
             bool ok = true;
             for (int L = blockIdx.x; L < num_tiles && ok; L += gridDim.x) {
-                const Tile t = decode_tile<BN, WGRAD, SPLIT>(L, a, s_mtile);
+                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems>(L, a, s_mtile);
+                // first B row of the tile (K-major B); MXFP8 gate/up weights are stored with
+                // 128-row blocks of [64 gate | 64 up] rows, so the split tile is one block
+                const int b_row0 = t.e * a.b_rows_e + ((SPLIT && MX) ? t.nt * BN : t.n0);
                 for (int kb = 0; kb < t.kb; ++kb) {
                     if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
                     uint8_t* dA = sA + stage * kATileBytes;
                     uint8_t* dB = sB + stage * kBTileBytes;
                     mbar_arrive_expect_tx(full + stage, kStageBytes);
-                    const int k0 = kb * kBK;
+                    const int k0 = kb * kElems;
                     if (!A_MN) {
                         tma_load_2d(dA, &tmA, full + stage, k0, t.m0);
                     } else {
-                        tma_load_2d(dA, &tmA, full + stage, t.m0, t.row0 + k0);
-                        tma_load_2d(dA + 8192, &tmA, full + stage, t.m0 + 64, t.row0 + k0);
+#pragma unroll
+                        for (int c = 0; c < kBM / kMnChunk; ++c)
+                            tma_load_2d(dA + c * kMnLbo, &tmA, full + stage, t.m0 + kMnChunk * c, t.row0 + k0);
                     }
                     if (!B_MN) {
-                        if (SPLIT) {
+                        if (SPLIT && !MX) {
                             tma_load_2d(dB, &tmB, full + stage, k0, t.e * a.b_rows_e + t.n0);
-                            tma_load_2d(dB + (BN / 2) * 128, &tmB, full + stage, k0, t.e * a.b_rows_e + a.b_up + t.n0);
+                            tma_load_2d(dB + (BN / 2) * kRowBytes, &tmB, full + stage, k0,
+                                        t.e * a.b_rows_e + a.b_up + t.n0);
                         } else {
-                            tma_load_2d(dB, &tmB, full + stage, k0, t.e * a.b_rows_e + t.n0);
+                            tma_load_2d(dB, &tmB, full + stage, k0, b_row0);
                         }
                     } else {
                         const int krow = WGRAD ? t.row0 + k0 : t.e * a.b_rows_e + k0;
 #pragma unroll
-                        for (int c = 0; c < BN / 64; ++c) tma_load_2d(dB + c * 8192, &tmB, full + stage, t.n0 + 64 * c, krow);
+                        for (int c = 0; c < BN / kMnChunk; ++c)
+                            tma_load_2d(dB + c * kMnLbo, &tmB, full + stage, t.n0 + kMnChunk * c, krow);
+                    }
+                    if constexpr (MX) {
+                        // scale atoms of this K slice: A (m-tile) then B (n-tiles)
+                        uint8_t* dS = sSF + stage * kSfBytes;
+                        const int ka = (WGRAD ? t.row0 / 128 : 0) + kb;
+                        bulk_load(dS, a.sfA + ((long long)(t.m0 / 128) * a.sfA_kt + ka) * kSfAtom, kSfAtom,
+                                  full + stage);
+#pragma unroll
+                        for (int c = 0; c < kSfBAtoms; ++c) {
+                            long long mn_tile, kt;
+                            if (!B_MN) {
+                                mn_tile = b_row0 / 128 + c;
+                                kt = kb;
+                            } else if (!WGRAD) {
+                                mn_tile = t.n0 / 128 + c;
+                                kt = (long long)t.e * a.b_rows_e / 128 + kb;
+                            } else {
+                                mn_tile = t.n0 / 128 + c;
+                                kt = t.row0 / 128 + kb;
+                            }
+                            bulk_load(dS + kSfAtom * (1 + c), a.sfB + (mn_tile * a.sfB_kt + kt) * kSfAtom, kSfAtom,
+                                      full + stage);
+                        }
                     }
                     ++issued;
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -212,9 +265,9 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB), sf_base = smem_u32(sSF);
             for (int L = blockIdx.x; L < num_tiles && ok; L += gridDim.x) {
-                const Tile t = decode_tile<BN, WGRAD, SPLIT>(L, a, s_mtile);
+                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems>(L, a, s_mtile);
                 if (!mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -222,11 +275,30 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                     if (!mbar_wait(full + stage, phase, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = a_base + stage * kATileBytes, sb = b_base + stage * kBTileBytes;
+                    if constexpr (MX) {
+                        const uint32_t sf_cols = tmem_base + 2 * BN + stage * kSfCols;
+                        const uint32_t ss = sf_base + stage * kSfBytes;
 #pragma unroll
-                    for (int ks = 0; ks < kBK / 16; ++ks) {
-                        const uint64_t ad = A_MN ? sdesc_sw128(sa + ks * 2048, 8192, 1024) : sdesc_sw128(sa + ks * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? sdesc_sw128(sb + ks * 2048, 8192, 1024) : sdesc_sw128(sb + ks * 32, 16, 1024);
-                        mma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0);
+                        for (int c = 0; c <= kSfBAtoms; ++c)
+                            tmem_cp_sf_atom(sf_cols + 4 * c, sdesc_plain(ss + kSfAtom * c, 128));
+#pragma unroll
+                        for (int ks = 0; ks < kElems / kMmaK; ++ks) {
+                            const uint64_t ad = A_MN ? sdesc_sw128(sa + ks * kMnStep, kMnLbo, 1024)
+                                                     : sdesc_sw128(sa + ks * kKStep, 16, 1024);
+                            const uint64_t bd = B_MN ? sdesc_sw128(sb + ks * kMnStep, kMnLbo, 1024)
+                                                     : sdesc_sw128(sb + ks * kKStep, 16, 1024);
+                            mma_mxf8(d_tmem, ad, bd, idesc_mxf8(kBM, BN, A_MN, B_MN, ks, ks), sf_cols, sf_cols + 4,
+                                     (kb | ks) != 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < kElems / kMmaK; ++ks) {
+                            const uint64_t ad = A_MN ? sdesc_sw128(sa + ks * kMnStep, kMnLbo, 1024)
+                                                     : sdesc_sw128(sa + ks * kKStep, 16, 1024);
+                            const uint64_t bd = B_MN ? sdesc_sw128(sb + ks * kMnStep, kMnLbo, 1024)
+                                                     : sdesc_sw128(sb + ks * kKStep, 16, 1024);
+                            mma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0);
+                        }
                     }
                     mma_commit(empty + stage);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -250,7 +322,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int L = blockIdx.x; L < num_tiles; L += gridDim.x) {
-            const Tile t = decode_tile<BN, WGRAD, SPLIT>(L, a, s_mtile);
+            const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems>(L, a, s_mtile);
             if (!mbar_wait(tfull + acc, acc_phase, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + lane_addr + (uint32_t)(acc * BN);
@@ -377,28 +449,32 @@ static EncodeTiledFn get_encode() {
     return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [outer, inner] array, box {64, box_rows}, 128B swizzle.
-static bool tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+// 2-D tensor map over a row-major [outer, inner] array of `esize`-byte elements with box
+// {128 bytes, box_rows} and 128-byte swizzle.
+static bool tmap_2d(CUtensorMap* m, const void* ptr, int esize, uint64_t inner, uint64_t outer, uint32_t box_rows) {
     EncodeTiledFn enc = get_encode();
     if (!enc) return false;
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2};
-    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint64_t strides[1] = {inner * esize};
+    const cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / esize), box_rows};
     const cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI>
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a) {
-    auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI>;
-    const size_t smem = 1024 + (size_t)kStages * (kATileBytes + BN * kBK * 2) + 128 + (size_t)(a.E + 1) * 4;
+    auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX>;
+    const size_t stage = (size_t)kATileBytes + BN * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
+    const size_t fixed = 1024 + kStages * stage + 128;
+    const size_t smem = fixed + (size_t)(a.E + 1) * 4;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        1024 + kStages * (kATileBytes + BN * kBK * 2) + 128 + (kMaxExperts + 1) * 4);
+                                        (int)(fixed + (kMaxExperts + 1) * 4));
     });
     if (attr_err != cudaSuccess) return attr_err;
     kern<<<c.num_sms, gemm_threads<EPI>(), smem, c.st>>>(ta, tb, a);
@@ -407,10 +483,126 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
 
 int bwd_down_bn(int64_t I) { return (I % 256 == 0) ? 256 : 128; }
 
-cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, bool out_f32, bool save_gu) {
+static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, void* out, GemmArgs& a) {
     const Layout& L = *c.L;
     char* b = c.base;
     const int64_t H = L.H, I = L.I, E = L.E, R = L.rows;
+    CUtensorMap ta, tb;
+    switch (kind) {
+        case GemmKind::FwdGateUp:
+        case GemmKind::FwdGateUpSaveOnly:
+            if (!tmap_2d(&ta, b + L.xperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 128))
+                return cudaErrorInvalidValue;
+            a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 64); a.b_rows_e = (int)(2 * I); a.b_up = (int)I;
+            a.out0 = b + L.hid; a.out1 = b + L.gu;
+            return kind == GemmKind::FwdGateUp
+                       ? run<256, false, false, true, false, EPI_SWIGLU, false>(c, ta, tb, a)
+                       : run<256, false, false, true, false, EPI_GU_ONLY, false>(c, ta, tb, a);
+        case GemmKind::FwdDown:
+            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 256)) return cudaErrorInvalidValue;
+            a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 64); a.b_rows_e = (int)H;
+            a.out0 = b + L.ypart; a.ld0 = (int)H;
+            return run<256, false, false, false, false, EPI_WEIGHTED, false>(c, ta, tb, a);
+        case GemmKind::BwdDown: {
+            const int bn = bwd_down_bn(I);
+            if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 64))
+                return cudaErrorInvalidValue;
+            a.n_tiles = (int)(I / bn); a.k_blocks = (int)(H / 64); a.b_rows_e = (int)H;
+            a.out0 = b + L.dg; a.out1 = b + L.hw; a.dtw = reinterpret_cast<float*>(b + L.dtw);
+            return bn == 256 ? run<256, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a)
+                             : run<128, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a);
+        }
+        case GemmKind::BwdGateUp:
+            if (!tmap_2d(&ta, b + L.dg, 2, 2 * I, R, 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 64))
+                return cudaErrorInvalidValue;
+            a.n_tiles = (int)(H / 256); a.k_blocks = (int)(2 * I / 64); a.b_rows_e = (int)(2 * I);
+            a.out0 = b + L.ypart; a.ld0 = (int)H;
+            return run<256, false, true, false, false, EPI_PLAIN, false>(c, ta, tb, a);
+        case GemmKind::WgradDown: {
+            const int bn = bwd_down_bn(I);
+            if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 64) || !tmap_2d(&tb, b + L.hw, 2, I, R, 64))
+                return cudaErrorInvalidValue;
+            a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / bn);
+            a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
+            return bn == 256 ? run<256, true, true, false, true, EPI_WGRAD, false>(c, ta, tb, a)
+                             : run<128, true, true, false, true, EPI_WGRAD, false>(c, ta, tb, a);
+        }
+        case GemmKind::WgradGateUp:
+            if (!tmap_2d(&ta, b + L.dg, 2, 2 * I, R, 64) || !tmap_2d(&tb, b + L.xperm, 2, H, R, 64))
+                return cudaErrorInvalidValue;
+            a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 256);
+            a.out0 = out; a.ld0 = (int)H; a.out_e_stride = 2 * I * H;
+            return run<256, true, true, false, true, EPI_WGRAD, false>(c, ta, tb, a);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// MXFP8: 128 x 128 tiles; operands are the E4M3 copies made by the quantiser (quant.cu).
+static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmArgs& a) {
+    const Layout& L = *c.L;
+    const MxLayout& M = L.mx;
+    char* b = c.base;
+    const int64_t H = L.H, I = L.I, E = L.E, R = L.rows;
+    auto u8 = [&](size_t off) { return reinterpret_cast<const uint8_t*>(b + off); };
+    CUtensorMap ta, tb;
+    switch (kind) {
+        case GemmKind::FwdGateUp:
+        case GemmKind::FwdGateUpSaveOnly:
+            if (!tmap_2d(&ta, b + M.x_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w13_r, 1, H, E * 2 * I, 128))
+                return cudaErrorInvalidValue;
+            a.n_tiles = (int)(I / 64); a.k_blocks = (int)(H / 128); a.b_rows_e = (int)(2 * I);
+            a.sfA = u8(M.x_r_sf); a.sfA_kt = (int)(H / 128);
+            a.sfB = u8(M.w13_r_sf); a.sfB_kt = (int)(H / 128);
+            a.out0 = b + L.hid; a.out1 = b + L.gu;
+            return kind == GemmKind::FwdGateUp ? run<128, false, false, true, false, EPI_SWIGLU, true>(c, ta, tb, a)
+                                               : run<128, false, false, true, false, EPI_GU_ONLY, true>(c, ta, tb, a);
+        case GemmKind::FwdDown:
+            if (!tmap_2d(&ta, b + M.h_r, 1, I, R, 128) || !tmap_2d(&tb, b + M.w2_r, 1, I, E * H, 128))
+                return cudaErrorInvalidValue;
+            a.n_tiles = (int)(H / 128); a.k_blocks = (int)(I / 128); a.b_rows_e = (int)H;
+            a.sfA = u8(M.h_r_sf); a.sfA_kt = (int)(I / 128);
+            a.sfB = u8(M.w2_r_sf); a.sfB_kt = (int)(I / 128);
+            a.out0 = b + L.ypart; a.ld0 = (int)H;
+            return run<128, false, false, false, false, EPI_WEIGHTED, true>(c, ta, tb, a);
+        case GemmKind::BwdDown:
+            if (!tmap_2d(&ta, b + M.dy_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w2_c, 1, I, E * H, 128))
+                return cudaErrorInvalidValue;
+            a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 128); a.b_rows_e = (int)H;
+            a.sfA = u8(M.dy_r_sf); a.sfA_kt = (int)(H / 128);
+            a.sfB = u8(M.w2_c_sf); a.sfB_kt = (int)(E * H / 128);
+            a.out0 = b + L.dg; a.out1 = b + L.hw; a.dtw = reinterpret_cast<float*>(b + L.dtw);
+            return run<128, false, true, false, false, EPI_SWIGLU_BWD, true>(c, ta, tb, a);
+        case GemmKind::BwdGateUp:
+            if (!tmap_2d(&ta, b + M.dg_r, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.w13_c, 1, H, E * 2 * I, 128))
+                return cudaErrorInvalidValue;
+            a.n_tiles = (int)(H / 128); a.k_blocks = (int)(2 * I / 128); a.b_rows_e = (int)(2 * I);
+            a.sfA = u8(M.dg_r_sf); a.sfA_kt = (int)(2 * I / 128);
+            a.sfB = u8(M.w13_c_sf); a.sfB_kt = (int)(E * 2 * I / 128);
+            a.out0 = b + L.ypart; a.ld0 = (int)H;
+            return run<128, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a);
+        case GemmKind::WgradDown:
+            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 128))
+                return cudaErrorInvalidValue;
+            a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / 128);
+            a.sfA = u8(M.dy_c_sf); a.sfA_kt = (int)(R / 128);
+            a.sfB = u8(M.hw_c_sf); a.sfB_kt = (int)(R / 128);
+            a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
+            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a);
+        case GemmKind::WgradGateUp:
+            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 128))
+                return cudaErrorInvalidValue;
+            a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 128);
+            a.sfA = u8(M.dg_c_sf); a.sfA_kt = (int)(R / 128);
+            a.sfB = u8(M.x_c_sf); a.sfB_kt = (int)(R / 128);
+            a.out0 = out; a.ld0 = (int)H; a.out_e_stride = 2 * I * H;
+            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, bool out_f32, bool save_gu) {
+    const Layout& L = *c.L;
+    char* b = c.base;
     GemmArgs a{};
     a.mtile = reinterpret_cast<const int*>(b + L.mtile);
     a.order = reinterpret_cast<const int*>(b + L.order);
@@ -418,69 +610,14 @@ cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, b
     a.topk_w = c.topk_w;
     a.gu = reinterpret_cast<const __nv_bfloat16*>(b + L.gu);
     a.status = c.status;
-    a.E = (int)E;
-    a.I = (int)I;
+    a.E = (int)L.E;
+    a.I = (int)L.I;
     a.out_f32 = out_f32 ? 1 : 0;
     a.save_gu = save_gu ? 1 : 0;
-    CUtensorMap ta, tb;
-    bool ok = true;
-    cudaError_t err = cudaSuccess;
-    const int trace_id = 5 + (int)kind;
+    const int trace_id = (L.mx_on ? kTraceGemmMx : kTraceGemm) + (int)kind;
     trace_begin(c.st, trace_id);
-    switch (kind) {
-        case GemmKind::FwdGateUp:
-        case GemmKind::FwdGateUpSaveOnly:
-            ok = tmap_bf16(&ta, b + L.xperm, H, R, 128) && tmap_bf16(&tb, W, H, E * 2 * I, 128);
-            a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / kBK); a.b_rows_e = (int)(2 * I); a.b_up = (int)I;
-            a.out0 = b + L.hid; a.out1 = b + L.gu;
-            if (!ok) break;
-            err = kind == GemmKind::FwdGateUp ? run<256, false, false, true, false, EPI_SWIGLU>(c, ta, tb, a)
-                                              : run<256, false, false, true, false, EPI_GU_ONLY>(c, ta, tb, a);
-            break;
-        case GemmKind::FwdDown:
-            ok = tmap_bf16(&ta, b + L.hid, I, R, 128) && tmap_bf16(&tb, W, I, E * H, 256);
-            a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / kBK); a.b_rows_e = (int)H;
-            a.out0 = b + L.ypart; a.ld0 = (int)H;
-            if (!ok) break;
-            err = run<256, false, false, false, false, EPI_WEIGHTED>(c, ta, tb, a);
-            break;
-        case GemmKind::BwdDown: {
-            const int bn = bwd_down_bn(I);
-            ok = tmap_bf16(&ta, b + L.dyperm, H, R, 128) && tmap_bf16(&tb, W, I, E * H, 64);
-            a.n_tiles = (int)(I / bn); a.k_blocks = (int)(H / kBK); a.b_rows_e = (int)H;
-            a.out0 = b + L.dg; a.out1 = b + L.hw; a.dtw = reinterpret_cast<float*>(b + L.dtw);
-            if (!ok) break;
-            err = bn == 256 ? run<256, false, true, false, false, EPI_SWIGLU_BWD>(c, ta, tb, a)
-                            : run<128, false, true, false, false, EPI_SWIGLU_BWD>(c, ta, tb, a);
-            break;
-        }
-        case GemmKind::BwdGateUp:
-            ok = tmap_bf16(&ta, b + L.dg, 2 * I, R, 128) && tmap_bf16(&tb, W, H, E * 2 * I, 64);
-            a.n_tiles = (int)(H / 256); a.k_blocks = (int)(2 * I / kBK); a.b_rows_e = (int)(2 * I);
-            a.out0 = b + L.ypart; a.ld0 = (int)H;
-            if (!ok) break;
-            err = run<256, false, true, false, false, EPI_PLAIN>(c, ta, tb, a);
-            break;
-        case GemmKind::WgradDown: {
-            const int bn = bwd_down_bn(I);
-            ok = tmap_bf16(&ta, b + L.dyperm, H, R, 64) && tmap_bf16(&tb, b + L.hw, I, R, 64);
-            a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / bn);
-            a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
-            if (!ok) break;
-            err = bn == 256 ? run<256, true, true, false, true, EPI_WGRAD>(c, ta, tb, a)
-                            : run<128, true, true, false, true, EPI_WGRAD>(c, ta, tb, a);
-            break;
-        }
-        case GemmKind::WgradGateUp:
-            ok = tmap_bf16(&ta, b + L.dg, 2 * I, R, 64) && tmap_bf16(&tb, b + L.xperm, H, R, 64);
-            a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 256);
-            a.out0 = out; a.ld0 = (int)H; a.out_e_stride = 2 * I * H;
-            if (!ok) break;
-            err = run<256, true, true, false, true, EPI_WGRAD>(c, ta, tb, a);
-            break;
-    }
+    const cudaError_t err = L.mx_on ? launch_gemm_mx(c, kind, out, a) : launch_gemm_bf16(c, kind, W, out, a);
     trace_end(c.st, trace_id);
-    if (!ok) return cudaErrorInvalidValue;
     return err;
 }
 

@@ -15,6 +15,18 @@ constexpr int kBK = 64;           // bf16 elements of K per pipeline stage (one 
 constexpr int kRouteChunk = 2048; // slots per block of the routing kernels
 constexpr int kMaxExperts = 1024;
 
+// MXFP8 operand copies (E4M3 values + E8M0 scale atoms, see quant.cu): "_r" blocked along the
+// row (K-major use), "_c" blocked along the column (MN-major use).
+struct MxLayout {
+    size_t x_r, x_r_sf, x_c, x_c_sf;      // dispatched x rows [rows, H]
+    size_t h_r, h_r_sf;                   // h [rows, I]
+    size_t dy_r, dy_r_sf, dy_c, dy_c_sf;  // dispatched dy rows [rows, H]
+    size_t dg_r, dg_r_sf, dg_c, dg_c_sf;  // [dg|du] [rows, 2I]
+    size_t hw_c, hw_c_sf;                 // w h [rows, I]
+    size_t w13_r, w13_r_sf, w13_c, w13_c_sf;  // W13 [E*2I, H] (the _r copy in [64 gate|64 up] blocks)
+    size_t w2_r, w2_r_sf, w2_c, w2_c_sf;      // W2 [E*H, I]
+};
+
 // Byte offsets of every region of the scratch buffer for one desc.  The routed rows of expert e
 // occupy padded rows [pad_off[e], pad_off[e+1]) with pad_off[e] a multiple of 128, so a GEMM
 // tile never straddles two experts; padding rows hold zeros.  `rows` bounds the padded count.
@@ -22,6 +34,8 @@ struct Layout {
     int64_t T, H, I, E, k, S, rows, nb_route, n_dtw;
     size_t ctrl, hist, cnt, off, pad_off, mtile, order, base, perm, inv, pos, row_slot;
     size_t xperm, hid, gu, ypart, dyperm, dg, hw, dtw;
+    bool mx_on;
+    MxLayout mx;
     size_t total;
 };
 
@@ -57,6 +71,18 @@ enum class GemmKind : int {
 cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, bool out_f32, bool save_gu);
 // N tile of the backward down-projection product (and so the number of <dA, h> partials per row)
 int bwd_down_bn(int64_t I);
+
+// MXFP8 quantiser over a bf16 [R_max, C] array (R_max % 32 == 0, C % 128 == 0); with tiles_dev only
+// the first tiles_dev[0] * 128 rows.  Any of the outputs may be null.  gate_up_I > 0 stores the
+// row-blocked copy of a [E*2I, H] gate/up weight in [64 gate | 64 up] row blocks.
+cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int C, const int* tiles_dev, void* q_row,
+                            void* sf_row, void* q_col, void* sf_col, int gate_up_I);
+
+// tracing ids: one per kernel kind; the GEMM kinds follow kTraceGemm (BF16) and kTraceGemmMx
+enum TraceId : int {
+    kTraceRouteHist = 0, kTraceRouteScan, kTraceRoutePlace, kTraceGather, kTraceCombine, kTraceQuant,
+    kTraceGemm, kTraceGemmMx = kTraceGemm + 7, kTraceKinds = kTraceGemmMx + 7
+};
 
 // tracing hooks used by the launch sequence
 void trace_begin(cudaStream_t st, int kind_id);

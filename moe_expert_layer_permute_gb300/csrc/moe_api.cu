@@ -27,11 +27,12 @@ bool make_layout(const moe_desc* d, Layout* L) {
     if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0 || d->k <= 0) return false;
     if (d->H % 256 != 0 || d->I % 128 != 0 || d->k > d->E || d->E > kMaxExperts) return false;
     const int64_t S = d->T * d->k;
-    const int64_t rows = S + (int64_t)kBM * d->E;
+    const int64_t rows = (S + kBM - 1) / kBM * kBM + (int64_t)kBM * d->E;  // a multiple of 128
     if (rows >= (int64_t)INT32_MAX / 2) return false;
     L->T = d->T; L->H = d->H; L->I = d->I; L->E = d->E; L->k = d->k; L->S = S; L->rows = rows;
     L->nb_route = (S + kRouteChunk - 1) / kRouteChunk;
-    L->n_dtw = 2 * (d->I / bwd_down_bn(d->I));  // two column halves per n-tile
+    L->mx_on = d->precision == MOE_MXFP8;
+    L->n_dtw = 2 * (d->I / (L->mx_on ? 128 : bwd_down_bn(d->I)));  // two column halves per n-tile
     const size_t A = 4096;
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, A); return at; };
@@ -55,6 +56,24 @@ bool make_layout(const moe_desc* d, Layout* L) {
     L->dg = take((size_t)rows * 2 * d->I * 2);
     L->hw = take((size_t)rows * d->I * 2);
     L->dtw = take((size_t)rows * L->n_dtw * 4);
+    L->mx = MxLayout{};
+    if (L->mx_on) {
+        MxLayout& M = L->mx;
+        const size_t H = d->H, I = d->I, E = d->E, R = rows;
+        auto q = [&](size_t elems, size_t* data, size_t* sf) { *data = take(elems); *sf = take(elems / 32); };
+        q(R * H, &M.x_r, &M.x_r_sf);
+        q(R * H, &M.x_c, &M.x_c_sf);
+        q(R * I, &M.h_r, &M.h_r_sf);
+        q(R * H, &M.dy_r, &M.dy_r_sf);
+        q(R * H, &M.dy_c, &M.dy_c_sf);
+        q(R * 2 * I, &M.dg_r, &M.dg_r_sf);
+        q(R * 2 * I, &M.dg_c, &M.dg_c_sf);
+        q(R * I, &M.hw_c, &M.hw_c_sf);
+        q(E * 2 * I * H, &M.w13_r, &M.w13_r_sf);
+        q(E * 2 * I * H, &M.w13_c, &M.w13_c_sf);
+        q(E * H * I, &M.w2_r, &M.w2_r_sf);
+        q(E * H * I, &M.w2_c, &M.w2_c_sf);
+    }
     L->total = o;
     return true;
 }
@@ -62,12 +81,13 @@ bool make_layout(const moe_desc* d, Layout* L) {
 // ------------------------------------------------------------------------------------------
 // tracing
 // ------------------------------------------------------------------------------------------
-static const char* kTraceNames[] = {
-    "route_hist", "route_scan", "route_place", "gather_rows", "combine_rows",
+static const char* kTraceNames[kTraceKinds] = {
+    "route_hist", "route_scan", "route_place", "gather_rows", "combine_rows", "mx_quant",
     "gemm_fwd_gate_up_swiglu", "gemm_fwd_gate_up_save", "gemm_fwd_down_weighted", "gemm_bwd_down_swiglu_bwd",
     "gemm_bwd_gate_up", "gemm_wgrad_down", "gemm_wgrad_gate_up",
+    "gemm_mx_fwd_gate_up_swiglu", "gemm_mx_fwd_gate_up_save", "gemm_mx_fwd_down_weighted",
+    "gemm_mx_bwd_down_swiglu_bwd", "gemm_mx_bwd_gate_up", "gemm_mx_wgrad_down", "gemm_mx_wgrad_gate_up",
 };
-constexpr int kTraceKinds = sizeof(kTraceNames) / sizeof(kTraceNames[0]);
 
 struct TraceRec {
     int kind;
@@ -152,7 +172,6 @@ static int check_desc_scratch(moe_scratch* s, Layout* L) {
     const moe_desc* d = &s->desc;
     if (d->precision != MOE_BF16 && d->precision != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
     if (!make_layout(d, L)) return MOE_ERR_SHAPE;
-    if (d->precision == MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
     if (!s->data) return MOE_ERR_SCRATCH;
     if (reinterpret_cast<uintptr_t>(s->data) % 256 != 0) return MOE_ERR_SCRATCH;
     if (s->bytes < L->total) return MOE_ERR_SCRATCH;
@@ -171,6 +190,43 @@ static uint64_t fwd_tag(const moe_desc* d, const void* x, const void* idx, const
                        (uint64_t)(uintptr_t)w, (uint64_t)(uintptr_t)w13, (uint64_t)(uintptr_t)w2})
         h = mix(h, v);
     return h | 1ull;  // never 0 (0 = no saved forward)
+}
+
+static uint64_t weights_tag(const moe_desc* d, const void* w13, const void* w2) {
+    uint64_t h = 0x6D6F655F77717500ull;
+    for (uint64_t v : {(uint64_t)d->H, (uint64_t)d->I, (uint64_t)d->E, (uint64_t)(uintptr_t)w13,
+                       (uint64_t)(uintptr_t)w2})
+        h = mix(h, v);
+    return h | 1ull;
+}
+
+// MXFP8 copies of the weights: W13 blocked along H (gate/up row blocks) and along 2I, W2 blocked
+// along I and along H.  Skipped when the caller states the weights are unchanged since the call
+// that made these copies on this scratch (MOE_FLAG_REUSE_WEIGHTS).
+static int mx_weights(const Ctx& c, moe_scratch* s, const void* W13, const void* W2) {
+    const Layout& L = *c.L;
+    const MxLayout& M = L.mx;
+    const moe_desc* d = &s->desc;
+    const uint64_t tag = weights_tag(d, W13, W2);
+    if (d->flags & MOE_FLAG_REUSE_WEIGHTS) return s->state[1] == tag ? MOE_OK : MOE_ERR_STATE;
+    char* b = c.base;
+    if (launch_mx_quant(c, W13, L.E * 2 * L.I, (int)L.H, nullptr, b + M.w13_r, b + M.w13_r_sf, b + M.w13_c,
+                        b + M.w13_c_sf, (int)L.I) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_mx_quant(c, W2, L.E * L.H, (int)L.I, nullptr, b + M.w2_r, b + M.w2_r_sf, b + M.w2_c, b + M.w2_c_sf,
+                        0) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    s->state[1] = tag;
+    return MOE_OK;
+}
+
+// activation quantisation over the padded routed rows (count read on the device)
+static cudaError_t mx_rows(const Ctx& c, size_t src, int C, size_t qr, size_t qr_sf, size_t qc, size_t qc_sf) {
+    const Layout& L = *c.L;
+    char* b = c.base;
+    return launch_mx_quant(c, b + src, L.rows, C, reinterpret_cast<const int*>(b + L.mtile) + L.E,
+                           qr ? b + qr : nullptr, qr ? b + qr_sf : nullptr, qc ? b + qc : nullptr,
+                           qc ? b + qc_sf : nullptr, 0);
 }
 
 }  // namespace moe
@@ -215,7 +271,13 @@ int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* t
     Ctx c{st, base, &L, reinterpret_cast<int*>(base + L.ctrl), nsm, reinterpret_cast<const float*>(topk_w->data)};
     MOE_TRY_CUDA(launch_routing(c, reinterpret_cast<const int32_t*>(topk_idx->data)));
     MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, nullptr, nullptr));
+    if (L.mx_on) {
+        const MxLayout& M = L.mx;
+        if ((rc = mx_weights(c, scratch, W13->data, W2->data))) return rc;
+        MOE_TRY_CUDA(mx_rows(c, L.xperm, (int)H, M.x_r, M.x_r_sf, 0, 0));
+    }
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUp, W13->data, nullptr, false, save));
+    if (L.mx_on) MOE_TRY_CUDA(mx_rows(c, L.hid, (int)I, L.mx.h_r, L.mx.h_r_sf, 0, 0));
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdDown, W2->data, nullptr, false, false));
     MOE_TRY_CUDA(launch_combine(c, base + L.ypart, y->data, nullptr));
     // routing and dispatched rows are rewritten identically for the same inputs, so an earlier
@@ -259,14 +321,23 @@ int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_id
     if (nsm <= 0) return MOE_ERR_CUDA;
     char* base = reinterpret_cast<char*>(scratch->data);
     Ctx c{st, base, &L, reinterpret_cast<int*>(base + L.ctrl), nsm, reinterpret_cast<const float*>(topk_w->data)};
+    const MxLayout& M = L.mx;
+    if (L.mx_on && (rc = mx_weights(c, scratch, W13->data, W2->data))) return rc;
     if (!reuse) {
         MOE_TRY_CUDA(launch_routing(c, reinterpret_cast<const int32_t*>(topk_idx->data)));
         MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, dy->data, base + L.dyperm));
+        if (L.mx_on) MOE_TRY_CUDA(mx_rows(c, L.xperm, (int)H, M.x_r, M.x_r_sf, 0, 0));
         MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUpSaveOnly, W13->data, nullptr, false, true));
     } else {
         MOE_TRY_CUDA(launch_gather(c, dy->data, base + L.dyperm, nullptr, nullptr));
     }
+    if (L.mx_on) MOE_TRY_CUDA(mx_rows(c, L.dyperm, (int)H, M.dy_r, M.dy_r_sf, M.dy_c, M.dy_c_sf));
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::BwdDown, W2->data, nullptr, false, false));
+    if (L.mx_on) {
+        MOE_TRY_CUDA(mx_rows(c, L.dg, (int)(2 * I), M.dg_r, M.dg_r_sf, M.dg_c, M.dg_c_sf));
+        MOE_TRY_CUDA(mx_rows(c, L.hw, (int)I, 0, 0, M.hw_c, M.hw_c_sf));
+        MOE_TRY_CUDA(mx_rows(c, L.xperm, (int)H, 0, 0, M.x_c, M.x_c_sf));
+    }
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::BwdGateUp, W13->data, nullptr, false, false));
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::WgradDown, nullptr, dW2->data, f32_2, false));
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::WgradGateUp, nullptr, dW13->data, f32_13, false));
@@ -321,7 +392,15 @@ int moe_scratch_view(const moe_desc* desc, int view, uint64_t* offset, uint64_t*
         case MOE_VIEW_DG: *offset = L.dg; *bytes = R * 2 * I * 2; break;
         case MOE_VIEW_HW: *offset = L.hw; *bytes = R * I * 2; break;
         case MOE_VIEW_DYPERM: *offset = L.dyperm; *bytes = R * H * 2; break;
-        default: return MOE_ERR_SHAPE;
+        default: {
+            if (!L.mx_on || view < MOE_VIEW_MX_X_R || view >= MOE_VIEW_MX_END_) return MOE_ERR_SHAPE;
+            // MxLayout lists the regions in view order: value array then scales, per operand
+            const int i = view - MOE_VIEW_MX_X_R;
+            const uint64_t elems[12] = {R * H, R * H, R * I, R * H, R * H, R * 2 * I,
+                                        R * 2 * I, R * I, E * 2 * I * H, E * 2 * I * H, E * H * I, E * H * I};
+            *offset = reinterpret_cast<const size_t*>(&L.mx)[i];
+            *bytes = (i % 2 == 0) ? elems[i / 2] : elems[i / 2] / 32;
+        }
     }
     return MOE_OK;
 }

@@ -170,21 +170,21 @@ cudaError_t launch_routing(const Ctx& c, const int32_t* topk_idx) {
     int* base = reinterpret_cast<int*>(c.base + L.base);
     const int S = (int)L.S, E = (int)L.E, nb = (int)L.nb_route;
     if (nb > 0) {
-        trace_begin(c.st, 0);
+        trace_begin(c.st, kTraceRouteHist);
         route_hist_kernel<<<nb, kRouteThreads, E * sizeof(int), c.st>>>(topk_idx, S, E, hist, c.status);
-        trace_end(c.st, 0);
+        trace_end(c.st, kTraceRouteHist);
     }
-    trace_begin(c.st, 1);
+    trace_begin(c.st, kTraceRouteScan);
     route_scan_kernel<<<1, 1024, 0, c.st>>>(hist, nb, E, cnt, off, pad_off, mtile, order, base);
-    trace_end(c.st, 1);
+    trace_end(c.st, kTraceRouteScan);
     if (nb > 0) {
-        trace_begin(c.st, 2);
+        trace_begin(c.st, kTraceRoutePlace);
         const size_t sm = (size_t)(E + 8 * E) * sizeof(int);
         route_place_kernel<<<nb, kRouteThreads, sm, c.st>>>(
             topk_idx, S, E, base, off, pad_off, cnt, reinterpret_cast<int*>(c.base + L.perm),
             reinterpret_cast<int*>(c.base + L.inv), reinterpret_cast<int*>(c.base + L.pos),
             reinterpret_cast<int*>(c.base + L.row_slot));
-        trace_end(c.st, 2);
+        trace_end(c.st, kTraceRoutePlace);
     }
     return cudaGetLastError();
 }

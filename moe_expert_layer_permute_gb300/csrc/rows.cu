@@ -118,24 +118,24 @@ static int row_grid(const Ctx& c) { return c.num_sms * 8; }
 cudaError_t launch_gather(const Ctx& c, const void* src0, void* dst0, const void* src1, void* dst1) {
     const Layout& L = *c.L;
     const int row_vecs = (int)(L.H * 2 / 16);
-    trace_begin(c.st, 3);
+    trace_begin(c.st, kTraceGather);
     gather_rows_kernel<<<row_grid(c), kRowThreads, 0, c.st>>>(
         reinterpret_cast<const uint4*>(src0), reinterpret_cast<uint4*>(dst0), reinterpret_cast<const uint4*>(src1),
         reinterpret_cast<uint4*>(dst1), reinterpret_cast<const int*>(c.base + L.row_slot),
         reinterpret_cast<const int*>(c.base + L.mtile) + L.E, (int)L.k, row_vecs);
-    trace_end(c.st, 3);
+    trace_end(c.st, kTraceGather);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const Ctx& c, const void* part, void* out, float* dtopk_w) {
     const Layout& L = *c.L;
     const int row_vecs = (int)(L.H * 2 / 16);
-    trace_begin(c.st, 4);
+    trace_begin(c.st, kTraceCombine);
     combine_rows_kernel<<<row_grid(c), kRowThreads, 0, c.st>>>(
         reinterpret_cast<const uint4*>(part), reinterpret_cast<uint4*>(out),
         reinterpret_cast<const int*>(c.base + L.pos), (int)L.T, (int)L.k, row_vecs,
         reinterpret_cast<const float*>(c.base + L.dtw), (int)L.n_dtw, dtopk_w);
-    trace_end(c.st, 4);
+    trace_end(c.st, kTraceCombine);
     return cudaGetLastError();
 }
 

@@ -41,7 +41,8 @@ class DeviceLayer:
         self.dW13 = torch.full((E, 2 * I, H), float("nan"), dtype=wgrad_dtype, device=dev)
         self.dW2 = torch.full((E, H, I), float("nan"), dtype=wgrad_dtype, device=dev)
         self.dtw = torch.full((T, k), float("nan"), dtype=torch.float32, device=dev)
-        self.scratch = bd.Scratch(T, H, I, E, k, device=dev)
+        prec = bd.MOE_MXFP8 if cfg.precision == "mxfp8" else bd.MOE_BF16
+        self.scratch = bd.Scratch(T, H, I, E, k, precision=prec, device=dev)
 
     def fwd(self, flags=0):
         self.bd.moe_fwd(self.x, self.idx, self.w, self.W13, self.W2, self.y, self.scratch, flags=flags)
@@ -57,4 +58,35 @@ class DeviceLayer:
         return self.scratch.view(which, dtype, shape)
 
     def rows(self):
-        return self.cfg.S + 128 * self.cfg.E
+        return (self.cfg.S + 127) // 128 * 128 + 128 * self.cfg.E
+
+
+# ---- MXFP8 decoding (E4M3 code table from its bit fields; scale atoms as the header documents)
+def e4m3_table() -> np.ndarray:
+    tab = np.zeros(256)
+    for code in range(256):
+        sg, ex, m = code >> 7, (code >> 3) & 0xF, code & 7
+        if ex == 0xF and m == 7:
+            tab[code] = np.nan
+            continue
+        v = (m / 8.0) * 2.0 ** -6 if ex == 0 else (1 + m / 8.0) * 2.0 ** (ex - 7)
+        tab[code] = -v if sg else v
+    return tab
+
+
+def sf_index(mn, kb, k_atoms):
+    return ((mn // 128) * k_atoms + kb // 4) * 512 + 16 * (mn % 32) + 4 * ((mn // 32) % 4) + kb % 4
+
+
+def decode_mx(q: np.ndarray, sf: np.ndarray, along: str) -> np.ndarray:
+    """Dequantise an E4M3 [R, C] array with its scale atoms; along='row' (blocks of 32 columns)
+    or 'col' (blocks of 32 rows)."""
+    R, C = q.shape
+    vals = e4m3_table()[q]
+    r = np.arange(R)[:, None]
+    c = np.arange(C)[None, :]
+    if along == "row":
+        idx = sf_index(r, c // 32, C // 128)
+    else:
+        idx = sf_index(c, r // 32, R // 128)
+    return vals * np.ldexp(1.0, sf[idx].astype(np.int64) - 127)

@@ -1,0 +1,167 @@
+"""MXFP8 path (E4M3 values, one E8M0 scale per 32 elements along each GEMM's contraction axis)
+against the fp64 oracle that applies the same quantise-dequantise rounding.
+
+Bar: the quantiser's outputs decode exactly to the oracle's quantise-dequantise of the same
+bf16 inputs; y, dx, dW13, dW2 and dtopk_w within a relative Frobenius error of 3e-2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_expert_layer_permute_gb300 import inputs as gen
+
+from _layer import DeviceLayer, decode_mx, f64, rel_fro
+
+pytestmark = pytest.mark.gpu
+TOL = 3e-2
+
+
+def mx(cfg):
+    import dataclasses
+    return dataclasses.replace(cfg, precision="mxfp8", name=cfg.name + "_mx")
+
+
+SMALL = {
+    "tiny": mx(gen.CONFIGS["tiny"]),
+    "medium": mx(gen.custom_config("medium", T=2048, H=512, I=256, E=16, k=4, seed=21)),
+    "medium_I384": mx(gen.custom_config("medium_I384", T=1500, H=768, I=384, E=12, k=3, seed=22)),
+    "skew_small": mx(gen.custom_config("skew_small", T=1024, H=256, I=128, E=32, k=8, routing="zipf", seed=23)),
+}
+
+
+def _args(inp):
+    return inp.f64("x"), inp.topk_idx, inp.f64("topk_w"), inp.f64("W13"), inp.f64("W2")
+
+
+def _padded_rows(L, inp):
+    bd = L.bd
+    cfg = inp.cfg
+    r = oracle.route(inp.topk_idx, cfg.E)
+    pad = L.view(bd.MOE_VIEW_PAD_OFFSETS, torch.int32, (cfg.E + 1,)).cpu().numpy()
+    prow = np.empty(cfg.S, dtype=np.int64)
+    for e in range(cfg.E):
+        lo, hi = r["off"][e], r["off"][e + 1]
+        prow[lo:hi] = pad[e] + np.arange(hi - lo)
+    return r, prow
+
+
+def _mxview(L, name, shape):
+    bd = L.bd
+    q = L.view(bd.MX_VIEWS[name], torch.uint8, shape).cpu().numpy()
+    sf = L.view(bd.MX_VIEWS[name + "_sf"], torch.uint8, (-1,)).cpu().numpy()
+    return q, sf
+
+
+def test_quantiser_matches_oracle_bit_exact(cuda_lib):
+    inp = gen.make_inputs(SMALL["medium"])
+    cfg = inp.cfg
+    L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
+    L.bwd()
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    H, I, E, R = cfg.H, cfg.I, cfg.E, L.rows()
+    r, prow = _padded_rows(L, inp)
+    X = inp.f64("x")[r["perm"] // cfg.k]
+    dY = inp.f64("dy")[r["perm"] // cfg.k]
+    # activations: along the row (K-major use) and along the tokens of each expert group
+    q, sf = _mxview(L, "x_r", (R, H))
+    np.testing.assert_array_equal(decode_mx(q, sf, "row")[prow], oracle.mx_qdq(X, axis=1))
+    q, sf = _mxview(L, "x_c", (R, H))
+    np.testing.assert_array_equal(decode_mx(q, sf, "col")[prow], oracle.mx_qdq_segments(X, r["off"]))
+    q, sf = _mxview(L, "dy_c", (R, H))
+    np.testing.assert_array_equal(decode_mx(q, sf, "col")[prow], oracle.mx_qdq_segments(dY, r["off"]))
+    q, sf = _mxview(L, "dy_r", (R, H))
+    np.testing.assert_array_equal(decode_mx(q, sf, "row")[prow], oracle.mx_qdq(dY, axis=1))
+    # weights: W2 along H per expert (column blocks of [E*H, I]); W13 along H in gate/up row blocks
+    W2 = inp.f64("W2")
+    q, sf = _mxview(L, "w2_c", (E * H, I))
+    np.testing.assert_array_equal(decode_mx(q, sf, "col").reshape(E, H, I), oracle.mx_qdq(W2, axis=1))
+    q, sf = _mxview(L, "w2_r", (E * H, I))
+    np.testing.assert_array_equal(decode_mx(q, sf, "row").reshape(E, H, I), oracle.mx_qdq(W2, axis=2))
+    W13 = inp.f64("W13")
+    q, sf = _mxview(L, "w13_r", (E * 2 * I, H))
+    dq = decode_mx(q, sf, "row").reshape(E, 2 * I // 128, 2, 64, H)     # blocks of [64 gate | 64 up]
+    gate = dq[:, :, 0].reshape(E, I, H)
+    up = dq[:, :, 1].reshape(E, I, H)
+    ref = oracle.mx_qdq(W13, axis=2)
+    np.testing.assert_array_equal(gate, ref[:, :I])
+    np.testing.assert_array_equal(up, ref[:, I:])
+    q, sf = _mxview(L, "w13_c", (E * 2 * I, H))
+    np.testing.assert_array_equal(decode_mx(q, sf, "col").reshape(E, 2 * I, H), oracle.mx_qdq(W13, axis=1))
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward(cuda_lib, name):
+    inp = gen.make_inputs(SMALL[name])
+    L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
+    L.fwd()
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    y_ref = oracle.forward(*_args(inp), mxfp8=True)
+    err = rel_fro(f64(L.y), y_ref)
+    assert err < TOL, err
+    # and it is an MXFP8 result: closer to the quantised oracle than to the BF16 one
+    assert err < rel_fro(f64(L.y), oracle.forward(*_args(inp)))
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("reuse", [False, True])
+def test_backward(cuda_lib, name, reuse):
+    inp = gen.make_inputs(SMALL[name])
+    L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
+    flags = 0
+    if reuse:
+        L.fwd(flags=cuda_lib.MOE_FLAG_SAVE_GU)
+        flags = cuda_lib.MOE_FLAG_REUSE_FWD | cuda_lib.MOE_FLAG_REUSE_WEIGHTS
+    L.bwd(flags=flags)
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    ref = oracle.backward(inp.f64("dy"), *_args(inp), mxfp8=True)
+    for got, n in ((L.dx, "dx"), (L.dW13, "dW13"), (L.dW2, "dW2"), (L.dtw, "dtopk_w")):
+        err = rel_fro(f64(got), ref[n])
+        assert err < TOL, (n, err)
+
+
+def test_weight_reuse_is_exact_and_checked(cuda_lib):
+    inp = gen.make_inputs(SMALL["medium"])
+    A = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
+    A.fwd()
+    A.bwd()
+    B = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
+    with pytest.raises(cuda_lib.MoeError) as ei:
+        B.fwd(flags=cuda_lib.MOE_FLAG_REUSE_WEIGHTS)     # nothing quantised on this scratch yet
+    assert ei.value.code == cuda_lib.ERR["MOE_ERR_STATE"]
+    B.fwd()
+    B.fwd(flags=cuda_lib.MOE_FLAG_SAVE_GU | cuda_lib.MOE_FLAG_REUSE_WEIGHTS)
+    B.bwd(flags=cuda_lib.MOE_FLAG_REUSE_FWD | cuda_lib.MOE_FLAG_REUSE_WEIGHTS)
+    torch.cuda.synchronize()
+    for a, b in ((A.y, B.y), (A.dx, B.dx), (A.dW13, B.dW13), (A.dW2, B.dW2), (A.dtw, B.dtw)):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["qwen3_30b_a3b_mxfp8", "qwen3_235b_a22b_mxfp8"])
+def test_full_size_sampled(cuda_lib, name):
+    cfg = gen.CONFIGS[name]
+    inp = gen.make_inputs(cfg)
+    L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
+    L.fwd()
+    L.fwd(flags=cuda_lib.MOE_FLAG_SAVE_GU | cuda_lib.MOE_FLAG_REUSE_WEIGHTS)
+    L.bwd(flags=cuda_lib.MOE_FLAG_REUSE_FWD | cuda_lib.MOE_FLAG_REUSE_WEIGHTS)
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    rng = np.random.default_rng(1)
+    toks = np.sort(rng.choice(cfg.T, 8, replace=False))
+    x, dy, W13, W2 = inp.f32("x"), inp.f32("dy"), inp.f32("W13"), inp.f32("W2")
+    ti = torch.from_numpy(toks).cuda()
+    y_s = oracle.forward_tokens(x, inp.topk_idx, inp.topk_w, W13, W2, toks, mxfp8=True)
+    assert rel_fro(f64(L.y[ti]), y_s) < TOL
+    dx_s, dtw_s = oracle.backward_tokens(dy, x, inp.topk_idx, inp.topk_w, W13, W2, toks, mxfp8=True)
+    assert rel_fro(f64(L.dx[ti]), dx_s) < TOL
+    assert rel_fro(f64(L.dtw[ti]), dtw_s) < TOL
+    experts = [0, int(rng.integers(cfg.E))]
+    for e, (a13, a2) in zip(experts, oracle.wgrad_experts(dy, x, inp.topk_idx, inp.topk_w, W13, W2, experts,
+                                                          mxfp8=True)):
+        assert rel_fro(f64(L.dW13[e]), a13) < TOL, e
+        assert rel_fro(f64(L.dW2[e]), a2) < TOL, e
+    for t in (L.y, L.dx, L.dW13, L.dW2, L.dtw):
+        assert torch.isfinite(t).all()
