@@ -40,6 +40,7 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="qwen3_30b_a3b")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-mx", action="store_true", help="skip the MXFP8 measurement of the same layer")
     return p.parse_args()
 
 
@@ -136,7 +137,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------ ours
-GEMM_FLOPS = {  # algorithmic FLOPs per launch of each grouped GEMM, in units of S*H*I
+GEMM_FLOPS = {  # algorithmic FLOPs per launch of each grouped GEMM (BF16 or MXFP8), in units of S*H*I
     "gemm_fwd_gate_up_swiglu": 4, "gemm_fwd_gate_up_save": 4, "gemm_fwd_down_weighted": 2,
     "gemm_bwd_down_swiglu_bwd": 2, "gemm_bwd_gate_up": 4, "gemm_wgrad_down": 2, "gemm_wgrad_gate_up": 4,
 }
@@ -174,18 +175,12 @@ def cpu_baseline(cfg, budget_s: float, seed_tokens: int = 256):
             "seconds_per_layer_sample": sec}
 
 
-def run_ours(args, rank, ws, local):
+def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
+    """Times fwd, bwd and the checkpointed layer for one workload; returns a dict of results."""
     import numpy as np
     import torch
 
-    from moe_expert_layer_permute_gb300 import build as b
-    b.build()
-    from moe_expert_layer_permute_gb300 import binding as bd
-    from moe_expert_layer_permute_gb300 import inputs as gen
-
-    cfg = gen.CONFIGS[args.config]
     dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
     inp = gen.make_inputs(cfg)
 
     def host(a):
@@ -194,16 +189,19 @@ def run_ours(args, rank, ws, local):
         return torch.from_numpy(np.ascontiguousarray(a))
 
     h_in = {n: host(getattr(inp, n)).pin_memory() for n in ("x", "topk_idx", "topk_w", "W13", "W2", "dy")}
+    del inp
     d = {n: t.to(dev) for n, t in h_in.items()}
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
-    wdt = torch.bfloat16
+    mx = cfg.precision == "mxfp8"
+    wdt = torch.float32 if mx else torch.bfloat16      # MXFP8: master weight gradients in fp32
     d["y"] = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     d["dx"] = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     d["dW13"] = torch.empty(E, 2 * I, H, dtype=wdt, device=dev)
     d["dW2"] = torch.empty(E, H, I, dtype=wdt, device=dev)
     d["dtw"] = torch.empty(T, k, dtype=torch.float32, device=dev)
-    sc = bd.Scratch(T, H, I, E, k, device=dev)
+    sc = bd.Scratch(T, H, I, E, k, precision=bd.MOE_MXFP8 if mx else bd.MOE_BF16, device=dev)
     stream = torch.cuda.current_stream()
+    RW = bd.MOE_FLAG_REUSE_WEIGHTS if mx else 0
 
     def fwd(flags=0):
         bd.moe_fwd(d["x"], d["topk_idx"], d["topk_w"], d["W13"], d["W2"], d["y"], sc, flags=flags)
@@ -213,9 +211,11 @@ def run_ours(args, rank, ws, local):
                    d["dtw"], sc, flags=flags)
 
     def step():
+        # one training step of the checkpointed layer: the weights (and their MXFP8 copies) are
+        # made once, the recompute saves [g|u], the backward reuses both
         fwd()
-        fwd(bd.MOE_FLAG_SAVE_GU)
-        bwd(bd.MOE_FLAG_REUSE_FWD)
+        fwd(bd.MOE_FLAG_SAVE_GU | RW)
+        bwd(bd.MOE_FLAG_REUSE_FWD | RW)
 
     def timed(fn, n):
         barrier(ws)
@@ -229,7 +229,7 @@ def run_ours(args, rank, ws, local):
         barrier(ws)
         return allreduce_max(e0.elapsed_time(e1), ws)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize()
     if bd.moe_read_device_status(sc) != 0:
@@ -237,73 +237,114 @@ def run_ours(args, rank, ws, local):
 
     clocks = ClockSampler(local)
     clocks.start()
-    # forward alone and backward alone (the backward reuses a saved forward, as in the layer)
-    fwd_ms = timed(fwd, args.steps) / args.steps
+    # forward alone (each call makes its own MXFP8 weight copies) and backward alone (reusing a
+    # saved forward, as in the layer)
+    fwd_ms = timed(fwd, steps) / steps
     fwd(bd.MOE_FLAG_SAVE_GU)
-    bwd_ms = timed(lambda: bwd(bd.MOE_FLAG_REUSE_FWD), args.steps) / args.steps
+    bwd_ms = timed(lambda: bwd(bd.MOE_FLAG_REUSE_FWD | RW), steps) / steps
     # the checkpointed layer, with per-kernel CUDA events recorded on the launch stream
     bd.moe_trace_reset()
     bd.moe_trace_enable(True)
-    full_total = timed(step, args.steps)
+    full_total = timed(step, steps)
     bd.moe_trace_enable(False)
     kern = bd.moe_trace_read()
     clk = clocks.stop()
-    full_ms = full_total / args.steps
+    full_ms = full_total / steps
     status = bd.moe_read_device_status(sc)
+    out = {"cfg": cfg, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "full_ms": full_ms, "kern": kern, "clocks": clk,
+           "status": status}
+    if with_e2e:
+        # end to end through the public API: pinned host inputs in, outputs back to pinned host
+        h_out = {n: torch.empty(d[n].shape, dtype=d[n].dtype).pin_memory() for n in ("y", "dx", "dW13", "dW2", "dtw")}
+        h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
-    # end to end through the public API: pinned host inputs in, outputs back to pinned host
-    h_out = {n: torch.empty(d[n].shape, dtype=d[n].dtype).pin_memory() for n in ("y", "dx", "dW13", "dW2", "dtw")}
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+        def e2e_step():
+            for n, t in h_in.items():
+                d[n].copy_(t, non_blocking=True)
+            step()
+            for n, t in h_out.items():
+                t.copy_(d[n], non_blocking=True)
 
-    def e2e_step():
-        for n, t in h_in.items():
-            d[n].copy_(t, non_blocking=True)
-        step()
-        for n, t in h_out.items():
-            t.copy_(d[n], non_blocking=True)
+        e2e_steps = max(3, min(steps, 20))
+        e2e_step()
+        out["e2e_ms"] = timed(e2e_step, e2e_steps) / e2e_steps
+        out["h2d"], out["d2h"] = h2d, d2h
+    del d, sc
+    torch.cuda.empty_cache()
+    return out
 
-    e2e_steps = max(3, min(args.steps, 20))
-    e2e_step()
-    e2e_ms = timed(e2e_step, e2e_steps) / e2e_steps
 
-    peaks, peak_src = load_peaks()
+def summarize(m, peak, peak_src):
+    """Per-kernel table, dominant-GEMM roofline and layer throughput of one measurement."""
+    cfg, kern = m["cfg"], m["kern"]
     fwd_fl = cfg.fwd_flops()
-    full_fl = 4 * fwd_fl
-    shf = float(cfg.S) * H * I
-    rows = {}
+    shf = float(cfg.S) * cfg.H * cfg.I
     total_ms = sum(v[1] for v in kern.values())
-    for name, (n, ms) in kern.items():
-        rows[name] = {"launches": n, "avg_ms": ms / n, "share": ms / total_ms if total_ms else None}
-    gemms = {n: v for n, v in rows.items() if n in GEMM_FLOPS}
+    rows = {name: {"launches": n, "avg_ms": ms / n, "share": ms / total_ms if total_ms else None}
+            for name, (n, ms) in kern.items()}
+    gemms = {n: v for n, v in rows.items() if n.replace("gemm_mx_", "gemm_") in GEMM_FLOPS}
     top = max(gemms, key=lambda n: gemms[n]["avg_ms"] * gemms[n]["launches"]) if gemms else None
-    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     roof = None
     if top:
-        ach = GEMM_FLOPS[top] * shf / (gemms[top]["avg_ms"] * 1e-3) / 1e12
+        ach = GEMM_FLOPS[top.replace("gemm_mx_", "gemm_")] * shf / (gemms[top]["avg_ms"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
-                "traffic": None, "kernel": top,
-                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)"}
-    full_tf = full_fl / (full_ms * 1e-3) / 1e12
+                "traffic": None, "kernel": top, "peak_source": peak_src}
+    full_tf = 4 * fwd_fl / (m["full_ms"] * 1e-3) / 1e12
+    return {"fwd_ms": m["fwd_ms"], "bwd_ms": m["bwd_ms"], "full_ms": m["full_ms"],
+            "fwd_tflops": fwd_fl / (m["fwd_ms"] * 1e-3) / 1e12,
+            "bwd_tflops": 2 * fwd_fl / (m["bwd_ms"] * 1e-3) / 1e12,
+            "full_tflops": full_tf, "frac_of_peak": full_tf / peak,
+            "identity_2fwd_plus_bwd_ms": 2 * m["fwd_ms"] + m["bwd_ms"],
+            "roofline": roof, "gpu_launches": int(sum(v[0] for v in kern.values())), "kernels": rows,
+            "clocks": m["clocks"], "device_status": m["status"]}
+
+
+def run_ours(args, rank, ws, local):
+    import torch
+
+    from moe_expert_layer_permute_gb300 import build as b
+    b.build()
+    from moe_expert_layer_permute_gb300 import binding as bd
+    from moe_expert_layer_permute_gb300 import inputs as gen
+
+    torch.cuda.set_device(local)
+    cfg = gen.CONFIGS[args.config]
+    peaks, src = load_peaks()
+    bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # the recipe's nominal dense ratio MXFP8 : BF16 is 4.5 : 2.25
+    mx_peak = 2.0 * bf16_peak
+    is_mx = cfg.precision == "mxfp8"
+    peak = mx_peak if is_mx else bf16_peak
+    peak_src = (f"{src} bf16_tflops_sustained" + (" x 2 (nominal MXFP8:BF16 ratio)" if is_mx else "")
+                + " (kernel timed inside a long step)")
+    m = measure(bd, gen, cfg, args.steps, args.warmup, ws, local, with_e2e=True)
+    sm = summarize(m, peak, peak_src)
     line = {
-        "metric": METRIC, "value": full_tf * ws, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": full_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16",
+        "metric": METRIC, "value": sm["full_tflops"] * ws, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sm["full_ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp8-e4m3" if is_mx else "bf16",
         "data": "synthetic: seeded N(0,1) x/dy, N(0,1/sqrt(fan_in)) weights, uniform top-8 routing, softmax weights",
-        "config": {"workload": f"{cfg.name}: T={T} H={H} I={I} E={E} k={k} {cfg.precision} {cfg.routing} routing",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} k={cfg.k} {cfg.precision} "
+                               f"{cfg.routing} routing",
                    "step": "fwd + fwd(save [g|u]) + bwd(reuse)", "parallelism": "replicas" if ws > 1 else "single GPU",
                    "l2": "inputs larger than L2 (weights alone 1.13 GiB per step)"},
-        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "full_ms": full_ms,
-        "fwd_tflops": fwd_fl / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": 2 * fwd_fl / (bwd_ms * 1e-3) / 1e12,
-        "full_tflops": full_tf, "frac_of_peak": full_tf / peak,
-        "peak_tflops": {"value": peak, "source": f"{peak_src} bf16_tflops_sustained"},
-        "identity_2fwd_plus_bwd_ms": 2 * fwd_ms + bwd_ms,
-        "roofline": roof,
-        "e2e": {"value": full_fl / (e2e_ms * 1e-3) / 1e12 * ws, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": int(sum(v[0] for v in kern.values())),
-        "kernels": rows, "clocks": clk, "device_status": status,
+        "peak_tflops": {"value": peak, "source": peak_src},
     }
+    line.update({k: v for k, v in sm.items() if k not in ("clocks", "device_status")})
+    line["e2e"] = {"value": 4 * cfg.fwd_flops() / (m["e2e_ms"] * 1e-3) / 1e12 * ws, "unit": "TFLOP/s",
+                   "ms_per_step": m["e2e_ms"], "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"]}
+    line["clocks"] = sm["clocks"]
+    line["device_status"] = sm["device_status"]
+    if not args.no_mx and not is_mx and args.config + "_mxfp8" in gen.CONFIGS:
+        # the same layer in MXFP8 (E4M3 + E8M0 per 32 along K, fp32 weight gradients)
+        mcfg = gen.CONFIGS[args.config + "_mxfp8"]
+        mm = measure(bd, gen, mcfg, args.steps, args.warmup, ws, local, with_e2e=False)
+        msrc = f"{src} bf16_tflops_sustained x 2 (nominal MXFP8:BF16 ratio)"
+        ms = summarize(mm, mx_peak, msrc)
+        ms["workload"] = mcfg.name
+        ms["peak_tflops"] = {"value": mx_peak, "source": msrc}
+        line["mxfp8"] = ms
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, budget_s=20.0)
     elif rank == 0:
