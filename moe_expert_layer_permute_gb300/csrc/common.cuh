@@ -245,4 +245,93 @@ __device__ __forceinline__ void store_f32x32(float* dst, const float* v) {
 }
 __device__ __forceinline__ float sigmoidf_fast(float z) { return __frcp_rn(1.0f + __expf(-z)); }
 
+// ------------------------------------------------------------------------------------------
+// MXFP8 (OCP Microscaling v1.0): E4M3 values, one E8M0 scale per 32 values
+// ------------------------------------------------------------------------------------------
+// Byte of MN-row mn / K-block kblock in the scale-atom layout the block-scaled MMA reads after a
+// 32x128b.warpx4 copy: atoms of 128 MN-rows x 4 K-blocks (512 B), k_atoms = K / 128 per MN tile.
+__host__ __device__ __forceinline__ long long sf_index(long long mn, long long kblock, long long k_atoms) {
+    return ((mn >> 7) * k_atoms + (kblock >> 2)) * 512 + 16 * (mn & 31) + 4 * ((mn >> 5) & 3) + (kblock & 3);
+}
+
+// Shared exponent floor(log2(amax)) - 8 (8 = the largest E4M3 exponent), clamped to the E8M0
+// range and stored biased by 127, and the exact factor 2^-exp; an all-zero block gets byte 0.
+__device__ __forceinline__ void mx_scale(float amax, uint8_t* sf, float* inv) {
+    if (!(amax > 0.f)) {
+        *sf = 0;
+        *inv = 0.f;
+        return;
+    }
+    int se = ilogbf(amax) - 8;
+    se = max(-127, min(127, se));
+    *sf = (uint8_t)(se + 127);
+    *inv = scalbnf(1.0f, -se);
+}
+
+// The same scale from the bits of a non-negative amax: for a normal amax its biased exponent field
+// is floor(log2(amax)) + 127, so the scale byte is that field - 8 and 2^-exp has the biased
+// exponent 254 - byte; zero, subnormal and very large maxima take the general path.
+__device__ __forceinline__ void mx_scale_bits(uint32_t amax_bits, uint8_t* sf, float* inv) {
+    const int ebits = (int)(amax_bits >> 23);
+    if (ebits >= 9 && ebits <= 254 + 8 - 1) {  // byte in [1, 253]: 2^-exp is a normal float
+        const int b = ebits - 8;
+        *sf = (uint8_t)b;
+        *inv = __uint_as_float((uint32_t)(254 - b) << 23);
+    } else {
+        mx_scale(__uint_as_float(amax_bits), sf, inv);
+    }
+}
+
+// Two values to E4M3 (round to nearest even, saturated to +-448), packed low byte first.
+__device__ __forceinline__ uint16_t to_e4m3x2(float a, float b) {
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// 32 values scaled by inv[] (per value) to 32 E4M3 bytes at a 16-byte aligned destination.
+__device__ __forceinline__ void store_e4m3x32(uint8_t* dst, const float* v, const float* inv) {
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        w[j] = (uint32_t)to_e4m3x2(v[4 * j] * inv[4 * j], v[4 * j + 1] * inv[4 * j + 1]) |
+               ((uint32_t)to_e4m3x2(v[4 * j + 2] * inv[4 * j + 2], v[4 * j + 3] * inv[4 * j + 3]) << 16);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Row block: the thread's 32 consecutive values of one row share one scale.
+__device__ __forceinline__ void quant_row32(const float* v, uint8_t* dst, uint8_t* sf_dst) {
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    uint8_t sf;
+    float inv;
+    mx_scale_bits(__float_as_uint(amax), &sf, &inv);
+    float invs[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) invs[j] = inv;
+    store_e4m3x32(dst, v, invs);
+    *sf_dst = sf;
+}
+
+// Column blocks: the 32 lanes of a warp hold 32 consecutive rows (lane = row), each the same 32
+// columns; column j's scale is shared by the 32 rows.  The column maxima come from one warp
+// max-reduction each on the |value| bit patterns (non-negative floats order like integers).
+// Lane j writes the scale of column col0 + j; every lane writes its own row's 32 bytes.
+__device__ __forceinline__ void quant_col32_warp(const float* v, uint8_t* dst_row, uint8_t* sf_base,
+                                                 long long col0, long long kblock, long long k_atoms) {
+    const int lane = threadIdx.x & 31;
+    float inv[32];
+    uint8_t my_sf = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j])));
+        uint8_t sf;
+        mx_scale_bits(m, &sf, &inv[j]);
+        if (j == lane) my_sf = sf;
+    }
+    store_e4m3x32(dst_row, v, inv);
+    sf_base[sf_index(col0 + lane, kblock, k_atoms)] = my_sf;
+}
+
 }  // namespace moe

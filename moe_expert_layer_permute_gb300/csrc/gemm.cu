@@ -68,6 +68,16 @@ struct GemmArgs {
     const uint8_t* sfA;
     const uint8_t* sfB;
     int sfA_kt, sfB_kt;
+    // MXFP8 epilogue outputs (E4M3 values + scale atoms) written in place of bf16 ones:
+    // forward gate/up: q0 = h blocked along I; SwiGLU backward: q0 = [dg|du] blocked along 2I,
+    // q1 = [dg|du] blocked along the rows, q2 = w h blocked along the rows
+    uint8_t* q0;
+    uint8_t* q0_sf;
+    uint8_t* q1;
+    uint8_t* q1_sf;
+    uint8_t* q2;
+    uint8_t* q2_sf;
+    int r_atoms;               // padded row capacity / 128 (K atoms of the row-blocked scales)
 };
 
 struct Tile {
@@ -344,7 +354,12 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                     if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = v[j] * sigmoidf_fast(v[j]) * u[j];
-                        store_bf16x32(hid + grow * (long long)a.I + t.n0 + 32 * c, v);
+                        const int col = t.n0 + 32 * c;
+                        if constexpr (MX)
+                            quant_row32(v, a.q0 + grow * (long long)a.I + col,
+                                        a.q0_sf + sf_index(grow, col / 32, a.I / 128));
+                        else
+                            store_bf16x32(hid + grow * (long long)a.I + col, v);
                     }
                 }
             } else if constexpr (EPI == EPI_WEIGHTED) {
@@ -385,9 +400,20 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                         u[j] = du;
                         v[j] = w * h;
                     }
-                    store_bf16x32(dG + grow * (2LL * a.I) + col, g);
-                    store_bf16x32(dG + grow * (2LL * a.I) + a.I + col, u);
-                    store_bf16x32(hw + grow * (long long)a.I + col, v);
+                    if constexpr (MX) {
+                        const long long gi = grow * (2LL * a.I);
+                        const int kq = 2 * a.I / 128;
+                        const long long kblk = grow >> 5;       // the warp's 32 rows form one block
+                        quant_row32(g, a.q0 + gi + col, a.q0_sf + sf_index(grow, col / 32, kq));
+                        quant_row32(u, a.q0 + gi + a.I + col, a.q0_sf + sf_index(grow, (a.I + col) / 32, kq));
+                        quant_col32_warp(g, a.q1 + gi + col, a.q1_sf, col, kblk, a.r_atoms);
+                        quant_col32_warp(u, a.q1 + gi + a.I + col, a.q1_sf, a.I + col, kblk, a.r_atoms);
+                        quant_col32_warp(v, a.q2 + grow * (long long)a.I + col, a.q2_sf, col, kblk, a.r_atoms);
+                    } else {
+                        store_bf16x32(dG + grow * (2LL * a.I) + col, g);
+                        store_bf16x32(dG + grow * (2LL * a.I) + a.I + col, u);
+                        store_bf16x32(hw + grow * (long long)a.I + col, v);
+                    }
                 }
                 a.dtw[grow * (2 * a.n_tiles) + 2 * t.nt + half] = dot;
             } else if constexpr (EPI == EPI_PLAIN) {
@@ -554,6 +580,7 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.sfA = u8(M.x_r_sf); a.sfA_kt = (int)(H / 128);
             a.sfB = u8(M.w13_r_sf); a.sfB_kt = (int)(H / 128);
             a.out0 = b + L.hid; a.out1 = b + L.gu;
+            a.q0 = reinterpret_cast<uint8_t*>(b + M.h_r); a.q0_sf = reinterpret_cast<uint8_t*>(b + M.h_r_sf);
             return kind == GemmKind::FwdGateUp ? run<128, false, false, true, false, EPI_SWIGLU, true>(c, ta, tb, a)
                                                : run<128, false, false, true, false, EPI_GU_ONLY, true>(c, ta, tb, a);
         case GemmKind::FwdDown:
@@ -571,6 +598,10 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.sfA = u8(M.dy_r_sf); a.sfA_kt = (int)(H / 128);
             a.sfB = u8(M.w2_c_sf); a.sfB_kt = (int)(E * H / 128);
             a.out0 = b + L.dg; a.out1 = b + L.hw; a.dtw = reinterpret_cast<float*>(b + L.dtw);
+            a.q0 = reinterpret_cast<uint8_t*>(b + M.dg_r); a.q0_sf = reinterpret_cast<uint8_t*>(b + M.dg_r_sf);
+            a.q1 = reinterpret_cast<uint8_t*>(b + M.dg_c); a.q1_sf = reinterpret_cast<uint8_t*>(b + M.dg_c_sf);
+            a.q2 = reinterpret_cast<uint8_t*>(b + M.hw_c); a.q2_sf = reinterpret_cast<uint8_t*>(b + M.hw_c_sf);
+            a.r_atoms = (int)(R / 128);
             return run<128, false, true, false, false, EPI_SWIGLU_BWD, true>(c, ta, tb, a);
         case GemmKind::BwdGateUp:
             if (!tmap_2d(&ta, b + M.dg_r, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.w13_c, 1, H, E * 2 * I, 128))

@@ -75,8 +75,9 @@ int bwd_down_bn(int64_t I);
 // MXFP8 quantiser over a bf16 [R_max, C] array (R_max % 32 == 0, C % 128 == 0); with tiles_dev only
 // the first tiles_dev[0] * 128 rows.  Any of the outputs may be null.  gate_up_I > 0 stores the
 // row-blocked copy of a [E*2I, H] gate/up weight in [64 gate | 64 up] row blocks.
+// With row_slot (padded rows only) source row r is row_slot[r] / k, zero where row_slot[r] < 0.
 cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int C, const int* tiles_dev, void* q_row,
-                            void* sf_row, void* q_col, void* sf_col, int gate_up_I);
+                            void* sf_row, void* q_col, void* sf_col, int gate_up_I, const int* row_slot = nullptr);
 
 // tracing ids: one per kernel kind; the GEMM kinds follow kTraceGemm (BF16) and kTraceGemmMx
 enum TraceId : int {

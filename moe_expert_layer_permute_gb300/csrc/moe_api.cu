@@ -220,13 +220,16 @@ static int mx_weights(const Ctx& c, moe_scratch* s, const void* W13, const void*
     return MOE_OK;
 }
 
-// activation quantisation over the padded routed rows (count read on the device)
-static cudaError_t mx_rows(const Ctx& c, size_t src, int C, size_t qr, size_t qr_sf, size_t qc, size_t qc_sf) {
+// activation quantisation over the padded routed rows (count read on the device); with `gather`
+// the source is the caller's [T, C] tensor, dispatched on the fly through row_slot
+static cudaError_t mx_rows(const Ctx& c, const void* src, bool gather, int C, size_t qr, size_t qr_sf, size_t qc,
+                           size_t qc_sf) {
     const Layout& L = *c.L;
     char* b = c.base;
-    return launch_mx_quant(c, b + src, L.rows, C, reinterpret_cast<const int*>(b + L.mtile) + L.E,
+    return launch_mx_quant(c, src, L.rows, C, reinterpret_cast<const int*>(b + L.mtile) + L.E,
                            qr ? b + qr : nullptr, qr ? b + qr_sf : nullptr, qc ? b + qc : nullptr,
-                           qc ? b + qc_sf : nullptr, 0);
+                           qc ? b + qc_sf : nullptr, 0,
+                           gather ? reinterpret_cast<const int*>(b + L.row_slot) : nullptr);
 }
 
 }  // namespace moe
@@ -270,14 +273,16 @@ int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* t
     char* base = reinterpret_cast<char*>(scratch->data);
     Ctx c{st, base, &L, reinterpret_cast<int*>(base + L.ctrl), nsm, reinterpret_cast<const float*>(topk_w->data)};
     MOE_TRY_CUDA(launch_routing(c, reinterpret_cast<const int32_t*>(topk_idx->data)));
-    MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, nullptr, nullptr));
     if (L.mx_on) {
+        // dispatch and quantise in one pass; a forward that saves for the backward also makes the
+        // token-blocked copy the weight gradient of W13 reads
         const MxLayout& M = L.mx;
         if ((rc = mx_weights(c, scratch, W13->data, W2->data))) return rc;
-        MOE_TRY_CUDA(mx_rows(c, L.xperm, (int)H, M.x_r, M.x_r_sf, 0, 0));
+        MOE_TRY_CUDA(mx_rows(c, x->data, true, (int)H, M.x_r, M.x_r_sf, save ? M.x_c : 0, save ? M.x_c_sf : 0));
+    } else {
+        MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, nullptr, nullptr));
     }
-    MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUp, W13->data, nullptr, false, save));
-    if (L.mx_on) MOE_TRY_CUDA(mx_rows(c, L.hid, (int)I, L.mx.h_r, L.mx.h_r_sf, 0, 0));
+    MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUp, W13->data, nullptr, false, save));  // MXFP8: emits E4M3 h
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdDown, W2->data, nullptr, false, false));
     MOE_TRY_CUDA(launch_combine(c, base + L.ypart, y->data, nullptr));
     // routing and dispatched rows are rewritten identically for the same inputs, so an earlier
@@ -325,19 +330,17 @@ int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_id
     if (L.mx_on && (rc = mx_weights(c, scratch, W13->data, W2->data))) return rc;
     if (!reuse) {
         MOE_TRY_CUDA(launch_routing(c, reinterpret_cast<const int32_t*>(topk_idx->data)));
-        MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, dy->data, base + L.dyperm));
-        if (L.mx_on) MOE_TRY_CUDA(mx_rows(c, L.xperm, (int)H, M.x_r, M.x_r_sf, 0, 0));
+        if (L.mx_on)
+            MOE_TRY_CUDA(mx_rows(c, x->data, true, (int)H, M.x_r, M.x_r_sf, M.x_c, M.x_c_sf));
+        else
+            MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, dy->data, base + L.dyperm));
         MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUpSaveOnly, W13->data, nullptr, false, true));
-    } else {
+    } else if (!L.mx_on) {
         MOE_TRY_CUDA(launch_gather(c, dy->data, base + L.dyperm, nullptr, nullptr));
     }
-    if (L.mx_on) MOE_TRY_CUDA(mx_rows(c, L.dyperm, (int)H, M.dy_r, M.dy_r_sf, M.dy_c, M.dy_c_sf));
+    if (L.mx_on) MOE_TRY_CUDA(mx_rows(c, dy->data, true, (int)H, M.dy_r, M.dy_r_sf, M.dy_c, M.dy_c_sf));
+    // MXFP8: the SwiGLU-backward epilogue emits the E4M3 copies of [dg|du] and w h directly
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::BwdDown, W2->data, nullptr, false, false));
-    if (L.mx_on) {
-        MOE_TRY_CUDA(mx_rows(c, L.dg, (int)(2 * I), M.dg_r, M.dg_r_sf, M.dg_c, M.dg_c_sf));
-        MOE_TRY_CUDA(mx_rows(c, L.hw, (int)I, 0, 0, M.hw_c, M.hw_c_sf));
-        MOE_TRY_CUDA(mx_rows(c, L.xperm, (int)H, 0, 0, M.x_c, M.x_c_sf));
-    }
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::BwdGateUp, W13->data, nullptr, false, false));
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::WgradDown, nullptr, dW2->data, f32_2, false));
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::WgradGateUp, nullptr, dW13->data, f32_13, false));

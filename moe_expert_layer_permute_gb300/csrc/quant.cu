@@ -18,6 +18,9 @@
 // MN = columns, K = R.
 // Optionally the row-blocked output permutes rows within each expert's [2I, H] gate/up matrix so
 // that every 128-row block holds 64 gate rows followed by the 64 up rows of the same I columns.
+// With a row map (row_slot, k) the quantiser is also the dispatch: output row r takes source row
+// row_slot[r] / k, or zeros where row_slot[r] < 0 (padding), so the bf16 dispatched rows are
+// never written.
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,34 +28,12 @@ namespace moe {
 
 constexpr int kQRows = 32, kQCols = 128, kQThreads = 128;
 
-__device__ __forceinline__ long long sf_index(long long mn, long long kblock, long long k_atoms) {
-    // k_atoms = K / 128 (atoms along K per 128-row MN tile)
-    return ((mn >> 7) * k_atoms + (kblock >> 2)) * 512 + 16 * (mn & 31) + 4 * ((mn >> 5) & 3) + (kblock & 3);
-}
-
-// Shared exponent and the factor 2^-exp for a block maximum (exact power of two).
-__device__ __forceinline__ void mx_scale(float amax, uint8_t* sf, float* inv) {
-    if (!(amax > 0.f)) {
-        *sf = 0;
-        *inv = 0.f;
-        return;
-    }
-    int se = ilogbf(amax) - 8;
-    se = max(-127, min(127, se));
-    *sf = (uint8_t)(se + 127);
-    *inv = scalbnf(1.0f, -se);
-}
-
-__device__ __forceinline__ uint16_t to_e4m3x2(float a, float b) {
-    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-}
-
 // grid: (C / 128, R_max / 32).  rows_dev (optional): device count of valid 128-row tiles.
 __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16* __restrict__ src, long long R_max,
                                                              int C, const int* __restrict__ tiles_dev,
                                                              uint8_t* __restrict__ q_row, uint8_t* __restrict__ sf_row,
                                                              uint8_t* __restrict__ q_col, uint8_t* __restrict__ sf_col,
-                                                             int gate_up_I) {
+                                                             int gate_up_I, const int* __restrict__ row_slot, int k) {
     __shared__ __align__(16) __nv_bfloat16 tile[kQRows][kQCols + 8];
     __shared__ __align__(16) uint8_t qt[kQRows][kQCols + 16];
     const long long r0 = (long long)blockIdx.y * kQRows;
@@ -64,8 +45,13 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int rr = it * 8 + (t >> 4), cc = (t & 15) * 8;
+        long long sr = r0 + rr;
+        if (row_slot) {
+            const int slot = row_slot[sr];
+            sr = slot >= 0 ? slot / k : -1;
+        }
         *reinterpret_cast<uint4*>(&tile[rr][cc]) =
-            __ldg(reinterpret_cast<const uint4*>(src + (r0 + rr) * C + c0 + cc));
+            sr >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + sr * C + c0 + cc)) : make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
     if (q_row) {
@@ -126,14 +112,14 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
 }
 
 cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int C, const int* tiles_dev, void* q_row,
-                            void* sf_row, void* q_col, void* sf_col, int gate_up_I) {
+                            void* sf_row, void* q_col, void* sf_col, int gate_up_I, const int* row_slot) {
     if (R_max <= 0) return cudaSuccess;
     dim3 grid(C / kQCols, (unsigned)(R_max / kQRows));
     trace_begin(c.st, kTraceQuant);
     mx_quant_kernel<<<grid, kQThreads, 0, c.st>>>(
         reinterpret_cast<const __nv_bfloat16*>(src), R_max, C, tiles_dev, reinterpret_cast<uint8_t*>(q_row),
         reinterpret_cast<uint8_t*>(sf_row), reinterpret_cast<uint8_t*>(q_col), reinterpret_cast<uint8_t*>(sf_col),
-        gate_up_I);
+        gate_up_I, row_slot, (int)c.L->k);
     trace_end(c.st, kTraceQuant);
     return cudaGetLastError();
 }

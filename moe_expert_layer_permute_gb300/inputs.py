@@ -73,6 +73,8 @@ CONFIGS = {
     # the 30B layer's per-expert work (about 1024 routed rows per expert) on 32 experts: the
     # GEMMs' arithmetic intensity of the full workload at a quarter of its device footprint
     "profile_30b_e32": LayerConfig("profile_30b_e32", T=4096, H=2048, I=768, E=32, k=8, seed=1001),
+    "profile_30b_e32_mxfp8": LayerConfig("profile_30b_e32_mxfp8", T=4096, H=2048, I=768, E=32, k=8,
+                                         precision="mxfp8", seed=1001),
 }
 
 

@@ -165,3 +165,30 @@ def test_full_size_sampled(cuda_lib, name):
         assert rel_fro(f64(L.dW2[e]), a2) < TOL, e
     for t in (L.y, L.dx, L.dW13, L.dW2, L.dtw):
         assert torch.isfinite(t).all()
+
+
+def test_fused_epilogue_copies(cuda_lib):
+    """The E4M3 copies the GEMM epilogues emit (h along I; [dg|du] along 2I and along the tokens;
+    w h along the tokens) decode to the oracle's quantise-dequantise of the same quantities.
+    The epilogues quantise fp32 values and the oracle fp64 ones, so a near-tie can round the
+    other way (one E4M3 step, about 8%, on a few per cent of the values): compared in relative
+    Frobenius norm against the MXFP8 bound."""
+    inp = gen.make_inputs(SMALL["medium"])
+    cfg = inp.cfg
+    L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
+    L.fwd(flags=cuda_lib.MOE_FLAG_SAVE_GU)
+    L.bwd(flags=cuda_lib.MOE_FLAG_REUSE_FWD | cuda_lib.MOE_FLAG_REUSE_WEIGHTS)
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    I, R = cfg.I, L.rows()
+    r, prow = _padded_rows(L, inp)
+    ref = oracle.backward(inp.f64("dy"), *_args(inp), mxfp8=True, keep=True)
+    h = ref["fwd"]["h"]
+    q, sf = _mxview(L, "h_r", (R, I))
+    assert rel_fro(decode_mx(q, sf, "row")[prow], oracle.mx_qdq(h, axis=1)) < TOL
+    q, sf = _mxview(L, "dg_r", (R, 2 * I))
+    assert rel_fro(decode_mx(q, sf, "row")[prow], oracle.mx_qdq(ref["dG"], axis=1)) < TOL
+    q, sf = _mxview(L, "dg_c", (R, 2 * I))
+    assert rel_fro(decode_mx(q, sf, "col")[prow], oracle.mx_qdq_segments(ref["dG"], r["off"])) < TOL
+    q, sf = _mxview(L, "hw_c", (R, I))
+    assert rel_fro(decode_mx(q, sf, "col")[prow], oracle.mx_qdq_segments(ref["Hw"], r["off"])) < TOL
