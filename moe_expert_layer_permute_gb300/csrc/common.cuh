@@ -95,6 +95,36 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// ---- clusters of two CTAs: B tiles multicast to both, stage releases signalled to both ------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of both CTAs; orders every shared-memory access before it in either CTA before
+// every access after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// TMA tile load delivered to the same shared-memory offset in every CTA of `mask`; each
+// destination CTA's mbarrier at `bar`'s offset receives the transaction bytes.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1,
+                                               uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                             uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+
 // ------------------------------------------------------------------------------------------
 // tcgen05: tensor memory, MMA, commit, loads
 // ------------------------------------------------------------------------------------------
@@ -145,6 +175,15 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// As mma_commit, arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives lane (base + i).
@@ -268,18 +307,14 @@ __device__ __forceinline__ void mx_scale(float amax, uint8_t* sf, float* inv) {
     *inv = scalbnf(1.0f, -se);
 }
 
-// The same scale from the bits of a non-negative amax: for a normal amax its biased exponent field
-// is floor(log2(amax)) + 127, so the scale byte is that field - 8 and 2^-exp has the biased
-// exponent 254 - byte; zero, subnormal and very large maxima take the general path.
+// The same scale from the bits of a non-negative finite amax.  For a normal amax the biased
+// exponent field is floor(log2(amax)) + 127, so the scale byte floor(log2(amax)) - 8 + 127 is the
+// field - 8; fields below 9 (amax < 2^-118, subnormals and zero) all clamp to byte 0.  2^-exp
+// then has the biased exponent 254 - byte, always a normal float.
 __device__ __forceinline__ void mx_scale_bits(uint32_t amax_bits, uint8_t* sf, float* inv) {
-    const int ebits = (int)(amax_bits >> 23);
-    if (ebits >= 9 && ebits <= 254 + 8 - 1) {  // byte in [1, 253]: 2^-exp is a normal float
-        const int b = ebits - 8;
-        *sf = (uint8_t)b;
-        *inv = __uint_as_float((uint32_t)(254 - b) << 23);
-    } else {
-        mx_scale(__uint_as_float(amax_bits), sf, inv);
-    }
+    const int b = max((int)(amax_bits >> 23) - 8, 0);
+    *sf = (uint8_t)b;
+    *inv = __uint_as_float((uint32_t)(254 - b) << 23);
 }
 
 // Two values to E4M3 (round to nearest even, saturated to +-448), packed low byte first.
@@ -316,22 +351,26 @@ __device__ __forceinline__ void quant_row32(const float* v, uint8_t* dst, uint8_
 
 // Column blocks: the 32 lanes of a warp hold 32 consecutive rows (lane = row), each the same 32
 // columns; column j's scale is shared by the 32 rows.  The column maxima come from one warp
-// max-reduction each on the |value| bit patterns (non-negative floats order like integers).
-// Lane j writes the scale of column col0 + j; every lane writes its own row's 32 bytes.
+// max-reduction each on the |value| bit patterns (non-negative floats order like integers); lane
+// j keeps column j's maximum, derives its scale and 2^-exp, and the factors are broadcast back.
+// Lane j writes the scale byte of column col0 + j; every lane writes its own row's 32 bytes.
 __device__ __forceinline__ void quant_col32_warp(const float* v, uint8_t* dst_row, uint8_t* sf_base,
                                                  long long col0, long long kblock, long long k_atoms) {
     const int lane = threadIdx.x & 31;
-    float inv[32];
-    uint8_t my_sf = 0;
+    uint32_t mine = 0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j])));
-        uint8_t sf;
-        mx_scale_bits(m, &sf, &inv[j]);
-        if (j == lane) my_sf = sf;
+        if (j == lane) mine = m;
     }
+    uint8_t sf;
+    float my_inv;
+    mx_scale_bits(mine, &sf, &my_inv);
+    float inv[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) inv[j] = __shfl_sync(0xffffffffu, my_inv, j);
     store_e4m3x32(dst_row, v, inv);
-    sf_base[sf_index(col0 + lane, kblock, k_atoms)] = my_sf;
+    sf_base[sf_index(col0 + lane, kblock, k_atoms)] = sf;
 }
 
 }  // namespace moe

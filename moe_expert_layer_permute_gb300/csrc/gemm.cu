@@ -26,6 +26,7 @@
 // Tile lists: "grouped-M" products (forward and data gradients) enumerate
 // (m-tile, n-tile) with n fastest, so CTAs working at the same time share the A tile in L2;
 // weight gradients enumerate (expert, m-tile, n-tile), experts in decreasing token count.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -82,6 +83,7 @@ struct GemmArgs {
 
 struct Tile {
     int e, m0, n0, nt, kb, row0;
+    bool valid;   // false: the duplicate tile of an expert's odd last m-tile in a CTA pair (no store)
 };
 
 __device__ __forceinline__ int find_expert(const int* s_mtile, int E, int gm) {
@@ -95,23 +97,42 @@ __device__ __forceinline__ int find_expert(const int* s_mtile, int E, int gm) {
 
 // kElems: K elements per pipeline stage (64 bf16, 128 E4M3); a 128-row group holds
 // 128 / kElems stages of a weight-gradient contraction.
-template <int BN, bool WGRAD, bool SPLIT, int kElems>
-__device__ __forceinline__ Tile decode_tile(int L, const GemmArgs& a, const int* s_mtile) {
+// PAIR: the unit L is shared by the two CTAs of a cluster, which take two m-tiles of the same
+// expert (rank 0 the even, rank 1 the odd one) and the same n-tile, so they need the same B tile.
+// Grouped-M units enumerate the pairs of each expert (s_pair: prefix of ceil(m-tiles / 2)); an
+// expert with an odd m-tile count gives rank 1 a duplicate of rank 0's last tile, not stored.
+template <int BN, bool WGRAD, bool SPLIT, int kElems, bool PAIR>
+__device__ __forceinline__ Tile decode_tile(int L, const GemmArgs& a, const int* s_mtile, const int* s_pair,
+                                            int rank) {
     Tile t;
+    t.valid = true;
     if (!WGRAD) {
-        const int gm = L / a.n_tiles;
-        t.nt = L - gm * a.n_tiles;
+        int gm;
+        if (PAIR) {
+            const int P = L / a.n_tiles;
+            t.nt = L - P * a.n_tiles;
+            t.e = find_expert(s_pair, a.E, P);
+            const int mt_e = s_mtile[t.e + 1] - s_mtile[t.e];
+            const int lm = 2 * (P - s_pair[t.e]) + rank;
+            t.valid = lm < mt_e;
+            gm = s_mtile[t.e] + min(lm, mt_e - 1);
+        } else {
+            gm = L / a.n_tiles;
+            t.nt = L - gm * a.n_tiles;
+            t.e = find_expert(s_mtile, a.E, gm);
+        }
         t.m0 = gm * kBM;
-        t.e = find_expert(s_mtile, a.E, gm);
         t.n0 = t.nt * (SPLIT ? BN / 2 : BN);
         t.kb = a.k_blocks;
         t.row0 = 0;
     } else {
-        const int per = a.m_tiles * a.n_tiles;
+        const int mtp = PAIR ? a.m_tiles / 2 : a.m_tiles;
+        const int per = mtp * a.n_tiles;
         const int ei = L / per;
         const int rem = L - ei * per;
-        const int mt = rem / a.n_tiles;
-        t.nt = rem - mt * a.n_tiles;
+        const int mq = rem / a.n_tiles;
+        const int mt = PAIR ? 2 * mq + rank : mq;
+        t.nt = rem - mq * a.n_tiles;
         t.e = a.order[ei];
         t.m0 = mt * kBM;
         t.n0 = t.nt * BN;
@@ -128,7 +149,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
         if (clock64() - t0 > kWaitTimeoutCycles / 8) break;
 }
 
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool PAIR>
 __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs a) {
@@ -164,13 +185,23 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
     int* s_mtile = reinterpret_cast<int*>(tslot + 4);
+    int* s_pair = s_mtile + (a.E + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = PAIR ? (int)cluster_ctarank() : 0;
+    const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;   // cluster = 2 consecutive CTAs
+    const int unit_stride = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    constexpr uint16_t kPeers = 0x3;
     for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_mtile[i] = a.mtile[i];
+    __syncthreads();
     if (threadIdx.x == 0) {
+        if (PAIR && !WGRAD) {
+            s_pair[0] = 0;
+            for (int e = 0; e < a.E; ++e) s_pair[e + 1] = s_pair[e] + (s_mtile[e + 1] - s_mtile[e] + 1) / 2;
+        }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, 1);
+            mbar_init(empty + s, PAIR ? 2 : 1);   // PAIR: both CTAs' MMAs release each stage
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull + b, 1);
@@ -187,9 +218,11 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     if (warp == 1) tmem_alloc(tslot, kTmemCols);
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem_base = *tslot;
-    const int num_tiles = WGRAD ? a.E * a.m_tiles * a.n_tiles : s_mtile[a.E] * a.n_tiles;
+    const int num_tiles = WGRAD ? a.E * (PAIR ? a.m_tiles / 2 : a.m_tiles) * a.n_tiles
+                                : (PAIR ? s_pair[a.E] : s_mtile[a.E]) * a.n_tiles;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -198,8 +231,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
-            for (int L = blockIdx.x; L < num_tiles && ok; L += gridDim.x) {
-                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems>(L, a, s_mtile);
+            for (int L = unit0; L < num_tiles && ok; L += unit_stride) {
+                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
                 // first B row of the tile (K-major B); MXFP8 gate/up weights are stored with
                 // 128-row blocks of [64 gate | 64 up] rows, so the split tile is one block
                 const int b_row0 = t.e * a.b_rows_e + ((SPLIT && MX) ? t.nt * BN : t.n0);
@@ -216,7 +249,26 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                         for (int c = 0; c < kBM / kMnChunk; ++c)
                             tma_load_2d(dA + c * kMnLbo, &tmA, full + stage, t.m0 + kMnChunk * c, t.row0 + k0);
                     }
-                    if (!B_MN) {
+                    if (PAIR) {
+                        // each CTA loads half of the B tile and multicasts it to both
+                        if (!B_MN) {
+                            const int brow = (SPLIT && !MX) ? t.e * a.b_rows_e + rank * a.b_up + t.n0
+                                                            : b_row0 + rank * (BN / 2);
+                            tma_load_2d_mc(dB + rank * (BN / 2) * kRowBytes, &tmB, full + stage, k0, brow, kPeers);
+                        } else {
+                            const int krow = WGRAD ? t.row0 + k0 : t.e * a.b_rows_e + k0;
+                            constexpr int nch = BN / kMnChunk;
+                            if constexpr (nch >= 2) {
+#pragma unroll
+                                for (int c = rank * nch / 2; c < (rank + 1) * nch / 2; ++c)
+                                    tma_load_2d_mc(dB + c * kMnLbo, &tmB, full + stage, t.n0 + kMnChunk * c, krow,
+                                                   kPeers);
+                            } else {   // one MN chunk: half of its K rows each
+                                tma_load_2d_mc(dB + rank * (kElems / 2) * kRowBytes, &tmB, full + stage, t.n0,
+                                               krow + rank * (kElems / 2), kPeers);
+                            }
+                        }
+                    } else if (!B_MN) {
                         if (SPLIT && !MX) {
                             tma_load_2d(dB, &tmB, full + stage, k0, t.e * a.b_rows_e + t.n0);
                             tma_load_2d(dB + (BN / 2) * kRowBytes, &tmB, full + stage, k0,
@@ -249,8 +301,12 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                                 mn_tile = t.n0 / 128 + c;
                                 kt = t.row0 / 128 + kb;
                             }
-                            bulk_load(dS + kSfAtom * (1 + c), a.sfB + (mn_tile * a.sfB_kt + kt) * kSfAtom, kSfAtom,
-                                      full + stage);
+                            if (!PAIR)
+                                bulk_load(dS + kSfAtom * (1 + c), a.sfB + (mn_tile * a.sfB_kt + kt) * kSfAtom, kSfAtom,
+                                          full + stage);
+                            else if (rank == 0)   // B's scales go to both CTAs
+                                bulk_load_mc(dS + kSfAtom * (1 + c), a.sfB + (mn_tile * a.sfB_kt + kt) * kSfAtom,
+                                             kSfAtom, full + stage, kPeers);
                         }
                     }
                     ++issued;
@@ -276,8 +332,9 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB), sf_base = smem_u32(sSF);
-            for (int L = blockIdx.x; L < num_tiles && ok; L += gridDim.x) {
-                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems>(L, a, s_mtile);
+            long long consumed = 0;
+            for (int L = unit0; L < num_tiles && ok; L += unit_stride) {
+                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
                 if (!mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -310,7 +367,11 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                             mma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0);
                         }
                     }
-                    mma_commit(empty + stage);
+                    if (PAIR)
+                        mma_commit_mc(empty + stage, kPeers);
+                    else
+                        mma_commit(empty + stage);
+                    ++consumed;
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -321,6 +382,14 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             if (!ok) {
                 mma_commit(drain);
                 drain_wait(drain, 0);
+            } else if (PAIR) {
+                // both CTAs' releases of the last stages have landed here before the CTA may exit
+                for (int s = 0; s < kStages; ++s) {
+                    if (consumed > s) {
+                        const long long n = (consumed - s + kStages - 1) / kStages;
+                        drain_wait(empty + s, (uint32_t)((n - 1) & 1));
+                    }
+                }
             }
         }
     } else {
@@ -331,14 +400,16 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int L = blockIdx.x; L < num_tiles; L += gridDim.x) {
-            const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems>(L, a, s_mtile);
+        for (int L = unit0; L < num_tiles; L += unit_stride) {
+            const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
             if (!mbar_wait(tfull + acc, acc_phase, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + lane_addr + (uint32_t)(acc * BN);
             const long long grow = (long long)t.m0 + r;
             float v[32];
-            if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
+            if (!t.valid) {
+                // duplicate tile of a CTA pair: nothing to store
+            } else if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
                 // columns [0, BN/2) = gate, [BN/2, BN) = up, for I-columns [n0, n0 + BN/2)
                 __nv_bfloat16* hid = reinterpret_cast<__nv_bfloat16*>(a.out0);
                 __nv_bfloat16* gu = reinterpret_cast<__nv_bfloat16*>(a.out1);
@@ -448,6 +519,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();   // no multicast or release from the peer is still in flight
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
@@ -490,21 +562,63 @@ static bool tmap_2d(CUtensorMap* m, const void* ptr, int esize, uint64_t inner, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The weight-gradient products run as clusters of two CTAs sharing B tiles (PAIR): their m-tiles
+// (feature rows) always come in pairs of one expert.  For the grouped-M products a pair needs two
+// m-tiles of one expert, and the duplicate tile of every odd expert (about 6% more MMA work at
+// 1024 rows per expert) outweighed the saved L2 traffic on GB300, so they run one CTA per tile.
+template <bool WGRAD>
+constexpr bool use_pairs() { return WGRAD; }
+
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a) {
-    auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX>;
+    constexpr bool PAIR = use_pairs<WGRAD>();
+    auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR>;
     const size_t stage = (size_t)kATileBytes + BN * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
     const size_t fixed = 1024 + kStages * stage + 128;
-    const size_t smem = fixed + (size_t)(a.E + 1) * 4;
+    const size_t smem = fixed + (size_t)2 * (a.E + 1) * 4;
+    const size_t smem_max = fixed + (size_t)2 * (kMaxExperts + 1) * 4;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
+    static int grid = 0;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)(fixed + (kMaxExperts + 1) * 4));
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
+        grid = c.num_sms;
+        if (attr_err == cudaSuccess && PAIR) {
+            // as many two-CTA clusters as can be resident at once (one CTA per SM)
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(c.num_sms);
+            cfg.blockDim = dim3(gemm_threads<EPI>());
+            cfg.dynamicSmemBytes = smem_max;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            attr_err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+            if (attr_err == cudaSuccess) grid = 2 * std::max(1, std::min(clusters, c.num_sms / 2));
+        }
     });
     if (attr_err != cudaSuccess) return attr_err;
-    kern<<<c.num_sms, gemm_threads<EPI>(), smem, c.st>>>(ta, tb, a);
-    return cudaGetLastError();
+    if (!PAIR) {
+        kern<<<c.num_sms, gemm_threads<EPI>(), smem, c.st>>>(ta, tb, a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(gemm_threads<EPI>());
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, a);
 }
 
 int bwd_down_bn(int64_t I) { return (I % 256 == 0) ? 256 : 128; }
@@ -570,6 +684,9 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
     char* b = c.base;
     const int64_t H = L.H, I = L.I, E = L.E, R = L.rows;
     auto u8 = [&](size_t off) { return reinterpret_cast<const uint8_t*>(b + off); };
+    // B boxes: 128 rows (K-major) or 128 K-rows of one 128-wide MN chunk; halved for the
+    // weight gradients, where the two CTAs of a pair each load half of the tile
+    constexpr uint32_t kBoxBw = use_pairs<true>() ? 64 : 128;
     CUtensorMap ta, tb;
     switch (kind) {
         case GemmKind::FwdGateUp:
@@ -612,7 +729,7 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.out0 = b + L.ypart; a.ld0 = (int)H;
             return run<128, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a);
         case GemmKind::WgradDown:
-            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 128))
+            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, kBoxBw))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / 128);
             a.sfA = u8(M.dy_c_sf); a.sfA_kt = (int)(R / 128);
@@ -620,7 +737,7 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
             return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a);
         case GemmKind::WgradGateUp:
-            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 128))
+            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, kBoxBw))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 128);
             a.sfA = u8(M.dg_c_sf); a.sfA_kt = (int)(R / 128);
