@@ -43,10 +43,12 @@ enum Epi : int { EPI_SWIGLU = 0, EPI_GU_ONLY, EPI_WEIGHTED, EPI_SWIGLU_BWD, EPI_
 
 // Epilogue warps: the SwiGLU backward reads [g|u] and writes three outputs per element and needs
 // two warps per TMEM lane quarter to keep up with the MMAs; the other epilogues use one.
-template <int EPI>
-constexpr int epi_warps() { return EPI == EPI_SWIGLU_BWD ? 8 : 4; }
-template <int EPI>
-constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI>(); }
+// MXFP8 tiles 128 x 256 keep a single accumulator (two would leave no TMEM for the scales); their
+// epilogue first drains the accumulator into registers, which needs two warps per lane quarter.
+template <int EPI, bool SINGLE>
+constexpr int epi_warps() { return (EPI == EPI_SWIGLU_BWD || SINGLE) ? 8 : 4; }
+template <int EPI, bool SINGLE>
+constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI, SINGLE>(); }
 
 struct GemmArgs {
     const int* mtile;          // [E+1] prefix of 128-row tiles per expert
@@ -149,8 +151,61 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
         if (clock64() - t0 > kWaitTimeoutCycles / 8) break;
 }
 
+// Epilogue of a 128 x 256 MXFP8 tile from registers: d holds columns [128 h, 128 h + 128) of
+// the thread's row.  For the gate/up product these are one [64 gate | 64 up] block of the
+// interleaved weight, i.e. g and u of I-columns [n0 + 64 h, n0 + 64 h + 64).
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& t, long long grow, int h,
+                                                 float* d) {
+    if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
+        __nv_bfloat16* gu = reinterpret_cast<__nv_bfloat16*>(a.out1);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float* g = d + 32 * c;
+            float* u = d + 64 + 32 * c;
+            const int col = t.n0 + 64 * h + 32 * c;
+            if (EPI == EPI_GU_ONLY || a.save_gu) {
+                store_bf16x32(gu + grow * (2LL * a.I) + col, g);
+                store_bf16x32(gu + grow * (2LL * a.I) + a.I + col, u);
+            }
+            if constexpr (EPI == EPI_SWIGLU) {
+                float hv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) hv[j] = g[j] * sigmoidf_fast(g[j]) * u[j];
+                quant_row32(hv, a.q0 + grow * (long long)a.I + col, a.q0_sf + sf_index(grow, col / 32, a.I / 128));
+            }
+        }
+    } else if constexpr (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN) {
+        float w = 1.f;
+        if constexpr (EPI == EPI_WEIGHTED) {
+            const int slot = a.row_slot[grow];
+            w = slot >= 0 ? a.topk_w[slot] : 0.f;
+        }
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out0) + grow * (long long)a.ld0 + t.n0 + 128 * h;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float o[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = w * d[32 * c + j];
+            store_bf16x32(out + 32 * c, o);
+        }
+    } else if constexpr (EPI == EPI_WGRAD) {
+        const long long off = (long long)t.e * a.out_e_stride + grow * a.ld0 + t.n0 + 128 * h;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float o[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = t.kb > 0 ? d[32 * c + j] : 0.f;
+            if (a.out_f32)
+                store_f32x32(reinterpret_cast<float*>(a.out0) + off + 32 * c, o);
+            else
+                store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.out0) + off + 32 * c, o);
+        }
+    }
+}
+
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool PAIR>
-__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
+__global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs a) {
     constexpr int kElems = MX ? 128 : 64;                // K elements per stage
@@ -162,14 +217,17 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     constexpr int kStageBytes = kATileBytes + kBTileBytes + kSfBytes;
     constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, A_MN, B_MN);
     constexpr uint32_t kSfCols = 4 * (1 + kSfBAtoms);    // TMEM columns of one stage's scales
+    constexpr bool kSingle = MX && BN == 256;            // one accumulator, drained to registers
+    constexpr int kAccStages = kSingle ? 1 : 2;
     constexpr uint32_t kTmemCols = MX ? 512 : 2 * BN;
-    constexpr int kEpiWarps = epi_warps<EPI>();
+    constexpr int kEpiWarps = epi_warps<EPI, kSingle>();
     constexpr int kHalves = kEpiWarps / 4;
     // MN-major operands: the next kMnChunk MN values start one chunk (kElems rows of 128 B) on
     constexpr uint32_t kMnLbo = kElems * kRowBytes;
     constexpr uint32_t kMnStep = kMmaK * kRowBytes;      // MN-major: bytes per MMA K step
     constexpr uint32_t kKStep = kMmaK * (MX ? 1 : 2);    // K-major: bytes per MMA K step
-    static_assert(!MX || BN == 128, "MXFP8 tiles are 128 x 128 (accumulators and scales share TMEM)");
+    static_assert(!MX || BN == 128 || BN == 256, "MXFP8 tiles are 128 x 128 or 128 x 256");
+    static_assert(!kSingle || EPI != EPI_SWIGLU_BWD, "the SwiGLU backward keeps 128-wide MXFP8 tiles");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -343,7 +401,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                     tc_fence_after();
                     const uint32_t sa = a_base + stage * kATileBytes, sb = b_base + stage * kBTileBytes;
                     if constexpr (MX) {
-                        const uint32_t sf_cols = tmem_base + 2 * BN + stage * kSfCols;
+                        const uint32_t sf_cols = tmem_base + kAccStages * BN + stage * kSfCols;
                         const uint32_t ss = sf_base + stage * kSfBytes;
 #pragma unroll
                         for (int c = 0; c <= kSfBAtoms; ++c)
@@ -376,8 +434,12 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                 }
                 if (!ok) break;
                 if (t.kb > 0) mma_commit(tfull + acc); else mbar_arrive(tfull + acc);
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
+                if (kAccStages == 2) {
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1u;
+                } else {
+                    acc_phase ^= 1u;
+                }
             }
             if (!ok) {
                 mma_commit(drain);
@@ -407,6 +469,21 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
             const uint32_t tacc = tmem_base + lane_addr + (uint32_t)(acc * BN);
             const long long grow = (long long)t.m0 + r;
             float v[32];
+            if constexpr (kSingle) {
+                // drain this thread's 128 columns [128 * half, 128 * half + 128), release the
+                // accumulator to the next tile's MMAs, then compute and store from registers
+                float d[128];
+                const uint32_t tcol = tacc + 128 * half;
+                tmem_ld32(tcol, d);
+                tmem_ld32(tcol + 32, d + 32);
+                tmem_ld32(tcol + 64, d + 64);
+                tmem_ld32(tcol + 96, d + 96);
+                tc_fence_before();
+                mbar_arrive(tempty + acc);
+                if (t.valid) epilogue_drained<BN, EPI>(a, t, grow, half, d);
+                acc_phase ^= 1u;
+                continue;
+            }
             if (!t.valid) {
                 // duplicate tile of a CTA pair: nothing to store
             } else if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
@@ -573,6 +650,7 @@ template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a) {
     constexpr bool PAIR = use_pairs<WGRAD>();
     auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR>;
+    constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + BN * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
     const size_t fixed = 1024 + kStages * stage + 128;
     const size_t smem = fixed + (size_t)2 * (a.E + 1) * 4;
@@ -592,7 +670,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
             at[0].val.clusterDim.y = 1;
             at[0].val.clusterDim.z = 1;
             cfg.gridDim = dim3(c.num_sms);
-            cfg.blockDim = dim3(gemm_threads<EPI>());
+            cfg.blockDim = dim3(kThreads);
             cfg.dynamicSmemBytes = smem_max;
             cfg.attrs = at;
             cfg.numAttrs = 1;
@@ -603,7 +681,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (!PAIR) {
-        kern<<<c.num_sms, gemm_threads<EPI>(), smem, c.st>>>(ta, tb, a);
+        kern<<<c.num_sms, kThreads, smem, c.st>>>(ta, tb, a);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -613,7 +691,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(gemm_threads<EPI>());
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = c.st;
     cfg.attrs = at;
@@ -677,37 +755,37 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
     return cudaErrorInvalidValue;
 }
 
-// MXFP8: 128 x 128 tiles; operands are the E4M3 copies made by the quantiser (quant.cu).
+// MXFP8: 128 x 256 tiles (one accumulator) for the forward and data-gradient products except the
+// SwiGLU backward; 128 x 128 tiles (two accumulators) for it and the weight gradients; operands are the E4M3 copies made by the quantiser and
+// the epilogues (quant.cu, the fused epilogues above).
 static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmArgs& a) {
     const Layout& L = *c.L;
     const MxLayout& M = L.mx;
     char* b = c.base;
     const int64_t H = L.H, I = L.I, E = L.E, R = L.rows;
     auto u8 = [&](size_t off) { return reinterpret_cast<const uint8_t*>(b + off); };
-    // B boxes: 128 rows (K-major) or 128 K-rows of one 128-wide MN chunk; halved for the
-    // weight gradients, where the two CTAs of a pair each load half of the tile
-    constexpr uint32_t kBoxBw = use_pairs<true>() ? 64 : 128;
     CUtensorMap ta, tb;
     switch (kind) {
         case GemmKind::FwdGateUp:
         case GemmKind::FwdGateUpSaveOnly:
-            if (!tmap_2d(&ta, b + M.x_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w13_r, 1, H, E * 2 * I, 128))
+            // 256 weight rows = two [64 gate | 64 up] blocks = 128 I-columns per tile
+            if (!tmap_2d(&ta, b + M.x_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w13_r, 1, H, E * 2 * I, 256))
                 return cudaErrorInvalidValue;
-            a.n_tiles = (int)(I / 64); a.k_blocks = (int)(H / 128); a.b_rows_e = (int)(2 * I);
+            a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 128); a.b_rows_e = (int)(2 * I);
             a.sfA = u8(M.x_r_sf); a.sfA_kt = (int)(H / 128);
             a.sfB = u8(M.w13_r_sf); a.sfB_kt = (int)(H / 128);
             a.out0 = b + L.hid; a.out1 = b + L.gu;
             a.q0 = reinterpret_cast<uint8_t*>(b + M.h_r); a.q0_sf = reinterpret_cast<uint8_t*>(b + M.h_r_sf);
-            return kind == GemmKind::FwdGateUp ? run<128, false, false, true, false, EPI_SWIGLU, true>(c, ta, tb, a)
-                                               : run<128, false, false, true, false, EPI_GU_ONLY, true>(c, ta, tb, a);
+            return kind == GemmKind::FwdGateUp ? run<256, false, false, true, false, EPI_SWIGLU, true>(c, ta, tb, a)
+                                               : run<256, false, false, true, false, EPI_GU_ONLY, true>(c, ta, tb, a);
         case GemmKind::FwdDown:
-            if (!tmap_2d(&ta, b + M.h_r, 1, I, R, 128) || !tmap_2d(&tb, b + M.w2_r, 1, I, E * H, 128))
+            if (!tmap_2d(&ta, b + M.h_r, 1, I, R, 128) || !tmap_2d(&tb, b + M.w2_r, 1, I, E * H, 256))
                 return cudaErrorInvalidValue;
-            a.n_tiles = (int)(H / 128); a.k_blocks = (int)(I / 128); a.b_rows_e = (int)H;
+            a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 128); a.b_rows_e = (int)H;
             a.sfA = u8(M.h_r_sf); a.sfA_kt = (int)(I / 128);
             a.sfB = u8(M.w2_r_sf); a.sfB_kt = (int)(I / 128);
             a.out0 = b + L.ypart; a.ld0 = (int)H;
-            return run<128, false, false, false, false, EPI_WEIGHTED, true>(c, ta, tb, a);
+            return run<256, false, false, false, false, EPI_WEIGHTED, true>(c, ta, tb, a);
         case GemmKind::BwdDown:
             if (!tmap_2d(&ta, b + M.dy_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w2_c, 1, I, E * H, 128))
                 return cudaErrorInvalidValue;
@@ -723,13 +801,16 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
         case GemmKind::BwdGateUp:
             if (!tmap_2d(&ta, b + M.dg_r, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.w13_c, 1, H, E * 2 * I, 128))
                 return cudaErrorInvalidValue;
-            a.n_tiles = (int)(H / 128); a.k_blocks = (int)(2 * I / 128); a.b_rows_e = (int)(2 * I);
+            a.n_tiles = (int)(H / 256); a.k_blocks = (int)(2 * I / 128); a.b_rows_e = (int)(2 * I);
             a.sfA = u8(M.dg_r_sf); a.sfA_kt = (int)(2 * I / 128);
             a.sfB = u8(M.w13_c_sf); a.sfB_kt = (int)(E * 2 * I / 128);
             a.out0 = b + L.ypart; a.ld0 = (int)H;
-            return run<128, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a);
+            return run<256, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a);
         case GemmKind::WgradDown:
-            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, kBoxBw))
+            // weight gradients keep 128 x 128 tiles with two accumulators: their contraction over an
+            // expert's rows is short, so a drained single accumulator would stall the MMAs, and the
+            // fp32 output stores need the epilogue to overlap the next tile; a pair splits B's K rows
+            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 64))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / 128);
             a.sfA = u8(M.dy_c_sf); a.sfA_kt = (int)(R / 128);
@@ -737,7 +818,7 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
             return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a);
         case GemmKind::WgradGateUp:
-            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, kBoxBw))
+            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 64))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 128);
             a.sfA = u8(M.dg_c_sf); a.sfA_kt = (int)(R / 128);

@@ -28,7 +28,23 @@ namespace moe {
 
 constexpr int kQRows = 32, kQCols = 128, kQThreads = 128;
 
-// grid: (C / 128, R_max / 32).  rows_dev (optional): device count of valid 128-row tiles.
+// Maximum |x| of packed bf16 pairs: |bf16| bit patterns order like unsigned 16-bit integers, so a
+// per-halfword unsigned max of the sign-cleared words gives both halves' maxima at once.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) { return __vmaxu2(acc, w & 0x7FFF7FFFu); }
+__device__ __forceinline__ uint32_t absmax_to_f32_bits(uint32_t m2) {
+    return max(m2 & 0xFFFFu, m2 >> 16) << 16;   // the larger half, as fp32 bits
+}
+// 8 bf16 (one uint4) scaled by inv into 8 E4M3 bytes (two 32-bit words)
+__device__ __forceinline__ uint2 e4m3x8(uint4 w, float inv) {
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        p[i] = to_e4m3x2(__uint_as_float(in[i] << 16) * inv, __uint_as_float(in[i] & 0xFFFF0000u) * inv);
+    return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+// grid: (C / 128, R_max / 32).  tiles_dev (optional): device count of valid 128-row tiles.
 __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16* __restrict__ src, long long R_max,
                                                              int C, const int* __restrict__ tiles_dev,
                                                              uint8_t* __restrict__ q_row, uint8_t* __restrict__ sf_row,
@@ -41,7 +57,7 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
     if (r0 >= R) return;
     const int c0 = blockIdx.x * kQCols;
     const int t = threadIdx.x;
-    // load 32 x 128 bf16 with 16-byte accesses
+    // load 32 x 128 bf16 with 16-byte accesses (through the row map when dispatching)
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int rr = it * 8 + (t >> 4), cc = (t & 15) * 8;
@@ -55,59 +71,58 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
     }
     __syncthreads();
     if (q_row) {
-        // thread -> (row t/4, block t%4)
+        // thread -> (row t/4, block t%4): 32 consecutive values of one row
         const int rr = t >> 2, b = t & 3;
-        float v[32];
-        float amax = 0.f;
+        const uint4* src4 = reinterpret_cast<const uint4*>(&tile[rr][32 * b]);
+        uint4 w[4];
+        uint32_t m2 = 0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            v[j] = __bfloat162float(tile[rr][32 * b + j]);
-            amax = fmaxf(amax, fabsf(v[j]));
+        for (int q = 0; q < 4; ++q) {
+            w[q] = src4[q];
+            m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, w[q].x), w[q].y), w[q].z), w[q].w);
         }
         uint8_t sf;
         float inv;
-        mx_scale(amax, &sf, &inv);
-        uint32_t w[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            w[j] = (uint32_t)to_e4m3x2(v[4 * j] * inv, v[4 * j + 1] * inv) |
-                   ((uint32_t)to_e4m3x2(v[4 * j + 2] * inv, v[4 * j + 3] * inv) << 16);
+        mx_scale_bits(absmax_to_f32_bits(m2), &sf, &inv);
         long long r = r0 + rr;
         if (gate_up_I > 0) {  // 128-row blocks of [64 gate rows | 64 up rows] per expert
             const long long e = r / (2 * gate_up_I), j = r % (2 * gate_up_I);
             const long long jj = j < gate_up_I ? j : j - gate_up_I;
             r = e * 2 * gate_up_I + 128 * (jj / 64) + (j < gate_up_I ? 0 : 64) + jj % 64;
         }
+        uint2 o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = e4m3x8(w[q], inv);
         uint4* dst = reinterpret_cast<uint4*>(q_row + r * C + c0 + 32 * b);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        dst[0] = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
+        dst[1] = make_uint4(o[2].x, o[2].y, o[3].x, o[3].y);
         sf_row[sf_index(r, (c0 >> 5) + b, C / 128)] = sf;
     }
     if (q_col) {
-        // thread -> column t, 32 rows
-        float v[32];
-        float amax = 0.f;
+        // thread -> column t: 32 rows of one column
+        uint32_t m = 0;
+        uint32_t v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            v[j] = __bfloat162float(tile[j][t]);
-            amax = fmaxf(amax, fabsf(v[j]));
+            v[j] = reinterpret_cast<const uint16_t*>(&tile[j][0])[t];
+            m = max(m, v[j] & 0x7FFFu);
         }
         uint8_t sf;
         float inv;
-        mx_scale(amax, &sf, &inv);
+        mx_scale_bits(m << 16, &sf, &inv);
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-            const uint16_t p = to_e4m3x2(v[j] * inv, v[j + 1] * inv);
+            const uint16_t p = to_e4m3x2(__uint_as_float(v[j] << 16) * inv, __uint_as_float(v[j + 1] << 16) * inv);
             qt[j][t] = (uint8_t)(p & 0xFF);
             qt[j + 1][t] = (uint8_t)(p >> 8);
         }
         sf_col[sf_index(c0 + t, r0 >> 5, R_max / 128)] = sf;
         __syncthreads();
         const int rr = t >> 2, q = t & 3;
-        const uint4* s = reinterpret_cast<const uint4*>(&qt[rr][32 * q]);
+        const uint4* s4 = reinterpret_cast<const uint4*>(&qt[rr][32 * q]);
         uint4* dst = reinterpret_cast<uint4*>(q_col + (r0 + rr) * C + c0 + 32 * q);
-        dst[0] = s[0];
-        dst[1] = s[1];
+        dst[0] = s4[0];
+        dst[1] = s4[1];
     }
 }
 
