@@ -44,7 +44,10 @@ __device__ __forceinline__ uint2 e4m3x8(uint4 w, float inv) {
     return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
-// grid: (C / 128, R_max / 32).  tiles_dev (optional): device count of valid 128-row tiles.
+// grid: (C / 128, R_max / 128); one block quantises a 128 x 128 tile in four passes of 32 rows.
+// Its row-blocked scales (128 rows x 4 column blocks) and column-blocked scales (128 columns x 4
+// row blocks) are each exactly one 512-byte atom: staged in shared memory and written with 16-byte
+// stores.  tiles_dev (optional): device count of valid 128-row tiles.
 __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16* __restrict__ src, long long R_max,
                                                              int C, const int* __restrict__ tiles_dev,
                                                              uint8_t* __restrict__ q_row, uint8_t* __restrict__ sf_row,
@@ -52,84 +55,98 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
                                                              int gate_up_I, const int* __restrict__ row_slot, int k) {
     __shared__ __align__(16) __nv_bfloat16 tile[kQRows][kQCols + 8];
     __shared__ __align__(16) uint8_t qt[kQRows][kQCols + 16];
-    const long long r0 = (long long)blockIdx.y * kQRows;
+    __shared__ __align__(16) uint8_t s_sfr[512];
+    __shared__ __align__(16) uint8_t s_sfc[512];
+    const long long rt = (long long)blockIdx.y * 128;
     const long long R = tiles_dev ? (long long)(*tiles_dev) * kBM : R_max;
-    if (r0 >= R) return;
+    if (rt >= R) return;
     const int c0 = blockIdx.x * kQCols;
     const int t = threadIdx.x;
-    // load 32 x 128 bf16 with 16-byte accesses (through the row map when dispatching)
+    for (int sub = 0; sub < 4; ++sub) {
+        const long long r0 = rt + 32 * sub;
+        // load 32 x 128 bf16 with 16-byte accesses (through the row map when dispatching)
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int rr = it * 8 + (t >> 4), cc = (t & 15) * 8;
-        long long sr = r0 + rr;
-        if (row_slot) {
-            const int slot = row_slot[sr];
-            sr = slot >= 0 ? slot / k : -1;
+        for (int it = 0; it < 4; ++it) {
+            const int rr = it * 8 + (t >> 4), cc = (t & 15) * 8;
+            long long sr = r0 + rr;
+            if (row_slot) {
+                const int slot = row_slot[sr];
+                sr = slot >= 0 ? slot / k : -1;
+            }
+            *reinterpret_cast<uint4*>(&tile[rr][cc]) =
+                sr >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + sr * C + c0 + cc)) : make_uint4(0, 0, 0, 0);
         }
-        *reinterpret_cast<uint4*>(&tile[rr][cc]) =
-            sr >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + sr * C + c0 + cc)) : make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
-    if (q_row) {
-        // thread -> (row t/4, block t%4): 32 consecutive values of one row
-        const int rr = t >> 2, b = t & 3;
-        const uint4* src4 = reinterpret_cast<const uint4*>(&tile[rr][32 * b]);
-        uint4 w[4];
-        uint32_t m2 = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            w[q] = src4[q];
-            m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, w[q].x), w[q].y), w[q].z), w[q].w);
-        }
-        uint8_t sf;
-        float inv;
-        mx_scale_bits(absmax_to_f32_bits(m2), &sf, &inv);
-        long long r = r0 + rr;
-        if (gate_up_I > 0) {  // 128-row blocks of [64 gate rows | 64 up rows] per expert
-            const long long e = r / (2 * gate_up_I), j = r % (2 * gate_up_I);
-            const long long jj = j < gate_up_I ? j : j - gate_up_I;
-            r = e * 2 * gate_up_I + 128 * (jj / 64) + (j < gate_up_I ? 0 : 64) + jj % 64;
-        }
-        uint2 o[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) o[q] = e4m3x8(w[q], inv);
-        uint4* dst = reinterpret_cast<uint4*>(q_row + r * C + c0 + 32 * b);
-        dst[0] = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
-        dst[1] = make_uint4(o[2].x, o[2].y, o[3].x, o[3].y);
-        sf_row[sf_index(r, (c0 >> 5) + b, C / 128)] = sf;
-    }
-    if (q_col) {
-        // thread -> column t: 32 rows of one column
-        uint32_t m = 0;
-        uint32_t v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            v[j] = reinterpret_cast<const uint16_t*>(&tile[j][0])[t];
-            m = max(m, v[j] & 0x7FFFu);
-        }
-        uint8_t sf;
-        float inv;
-        mx_scale_bits(m << 16, &sf, &inv);
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            const uint16_t p = to_e4m3x2(__uint_as_float(v[j] << 16) * inv, __uint_as_float(v[j + 1] << 16) * inv);
-            qt[j][t] = (uint8_t)(p & 0xFF);
-            qt[j + 1][t] = (uint8_t)(p >> 8);
-        }
-        sf_col[sf_index(c0 + t, r0 >> 5, R_max / 128)] = sf;
         __syncthreads();
-        const int rr = t >> 2, q = t & 3;
-        const uint4* s4 = reinterpret_cast<const uint4*>(&qt[rr][32 * q]);
-        uint4* dst = reinterpret_cast<uint4*>(q_col + (r0 + rr) * C + c0 + 32 * q);
-        dst[0] = s4[0];
-        dst[1] = s4[1];
+        if (q_row) {
+            // thread -> (row t/4, block t%4): 32 consecutive values of one row
+            const int rr = t >> 2, b = t & 3;
+            const uint4* src4 = reinterpret_cast<const uint4*>(&tile[rr][32 * b]);
+            uint4 w[4];
+            uint32_t m2 = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                w[q] = src4[q];
+                m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, w[q].x), w[q].y), w[q].z), w[q].w);
+            }
+            uint8_t sf;
+            float inv;
+            mx_scale_bits(absmax_to_f32_bits(m2), &sf, &inv);
+            long long r = r0 + rr;
+            if (gate_up_I > 0) {  // 128-row blocks of [64 gate rows | 64 up rows] per expert
+                const long long e = r / (2 * gate_up_I), j = r % (2 * gate_up_I);
+                const long long jj = j < gate_up_I ? j : j - gate_up_I;
+                r = e * 2 * gate_up_I + 128 * (jj / 64) + (j < gate_up_I ? 0 : 64) + jj % 64;
+                sf_row[sf_index(r, (c0 >> 5) + b, C / 128)] = sf;   // rows scatter across atoms
+            } else {
+                s_sfr[16 * rr + 4 * sub + b] = sf;                  // row 32 sub + rr of the atom
+            }
+            uint2 o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[q] = e4m3x8(w[q], inv);
+            uint4* dst = reinterpret_cast<uint4*>(q_row + r * C + c0 + 32 * b);
+            dst[0] = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
+            dst[1] = make_uint4(o[2].x, o[2].y, o[3].x, o[3].y);
+        }
+        if (q_col) {
+            // thread -> column t: 32 rows of one column
+            uint32_t m = 0;
+            uint32_t v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                v[j] = reinterpret_cast<const uint16_t*>(&tile[j][0])[t];
+                m = max(m, v[j] & 0x7FFFu);
+            }
+            uint8_t sf;
+            float inv;
+            mx_scale_bits(m << 16, &sf, &inv);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const uint16_t p = to_e4m3x2(__uint_as_float(v[j] << 16) * inv, __uint_as_float(v[j + 1] << 16) * inv);
+                qt[j][t] = (uint8_t)(p & 0xFF);
+                qt[j + 1][t] = (uint8_t)(p >> 8);
+            }
+            s_sfc[16 * (t & 31) + 4 * (t >> 5) + sub] = sf;           // column t, row block sub
+            __syncthreads();
+            const int rr = t >> 2, q = t & 3;
+            const uint4* s4 = reinterpret_cast<const uint4*>(&qt[rr][32 * q]);
+            uint4* dst = reinterpret_cast<uint4*>(q_col + (r0 + rr) * C + c0 + 32 * q);
+            dst[0] = s4[0];
+            dst[1] = s4[1];
+        }
+        __syncthreads();
     }
+    // the tile's two scale atoms, 16 bytes per thread
+    if (q_row && gate_up_I <= 0 && t < 32)
+        reinterpret_cast<uint4*>(sf_row + sf_index(rt, c0 >> 5, C / 128))[t] = reinterpret_cast<const uint4*>(s_sfr)[t];
+    if (q_col && t >= 32 && t < 64)
+        reinterpret_cast<uint4*>(sf_col + sf_index(c0, rt >> 5, R_max / 128))[t - 32] =
+            reinterpret_cast<const uint4*>(s_sfc)[t - 32];
 }
 
 cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int C, const int* tiles_dev, void* q_row,
                             void* sf_row, void* q_col, void* sf_col, int gate_up_I, const int* row_slot) {
     if (R_max <= 0) return cudaSuccess;
-    dim3 grid(C / kQCols, (unsigned)(R_max / kQRows));
+    dim3 grid(C / kQCols, (unsigned)(R_max / 128));
     trace_begin(c.st, kTraceQuant);
     mx_quant_kernel<<<grid, kQThreads, 0, c.st>>>(
         reinterpret_cast<const __nv_bfloat16*>(src), R_max, C, tiles_dev, reinterpret_cast<uint8_t*>(q_row),
