@@ -204,18 +204,29 @@ __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& 
     }
 }
 
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool PAIR>
+// Stages of the smem ring: a CTA pair driving one MMA (TWO) holds only half of each B tile per
+// CTA, which leaves room for six.
+template <bool TWO>
+constexpr int ring_stages() { return TWO ? 6 : kStages; }
+
+// PAIR: clusters of two CTAs on two m-tiles of one expert and the same n-tile.  Without TWO each
+// CTA runs its own MMAs and the pair only shares B by TMA multicast; with TWO the leader CTA
+// issues cta_group::2 MMAs (M = 256) over both CTAs' shared memory and tensor memory, each CTA
+// holding half of every B tile.
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool PAIR, bool TWO>
 __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmArgs a) {
+    static_assert(!TWO || (PAIR && !MX), "two-SM MMAs run in CTA pairs, BF16 only");
+    constexpr int kStages = ring_stages<TWO>();
     constexpr int kElems = MX ? 128 : 64;                // K elements per stage
     constexpr int kMmaK = MX ? 32 : 16;                  // K elements per MMA
     constexpr int kMnChunk = MX ? 128 : 64;              // MN elements per 128-byte row (MN-major)
-    constexpr int kBTileBytes = BN * kRowBytes;
+    constexpr int kBTileBytes = (TWO ? BN / 2 : BN) * kRowBytes;   // TWO: this CTA's half of B
     constexpr int kSfBAtoms = BN / 128;
     constexpr int kSfBytes = MX ? kSfAtom * (1 + kSfBAtoms) : 0;
     constexpr int kStageBytes = kATileBytes + kBTileBytes + kSfBytes;
-    constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, A_MN, B_MN);
+    constexpr uint32_t kIdesc = idesc_bf16(TWO ? 2 * kBM : kBM, BN, A_MN, B_MN);
     constexpr uint32_t kSfCols = 4 * (1 + kSfBAtoms);    // TMEM columns of one stage's scales
     constexpr bool kSingle = MX && BN == 256;            // one accumulator, drained to registers
     constexpr int kAccStages = kSingle ? 1 : 2;
@@ -259,11 +270,11 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
         }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, PAIR ? 2 : 1);   // PAIR: both CTAs' MMAs release each stage
+            mbar_init(empty + s, (PAIR && !TWO) ? 2 : 1);   // PAIR: both CTAs' MMAs release each stage
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull + b, 1);
-            mbar_init(tempty + b, kEpiWarps * 32);
+            mbar_init(tempty + b, (TWO ? 2 : 1) * kEpiWarps);   // one arrival per epilogue warp (TWO: both CTAs')
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -273,7 +284,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    if (warp == 1) tmem_alloc(tslot, kTmemCols);
+    if (warp == 1) {
+        if constexpr (TWO) tmem_alloc_pair(tslot, kTmemCols);
+        else tmem_alloc(tslot, kTmemCols);
+    }
     tc_fence_before();
     __syncthreads();
     if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast reaches them
@@ -298,8 +312,33 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                     if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
                     uint8_t* dA = sA + stage * kATileBytes;
                     uint8_t* dB = sB + stage * kBTileBytes;
-                    mbar_arrive_expect_tx(full + stage, kStageBytes);
                     const int k0 = kb * kElems;
+                    if (TWO) {
+                        // both CTAs' copies land on the leader's barrier, which expects both
+                        const uint32_t lbar = cluster_addr(full + stage, 0);
+                        if (rank == 0) mbar_arrive_expect_tx(full + stage, 2 * kStageBytes);
+                        if (!A_MN) {
+                            tma_load_2d_pair(dA, &tmA, lbar, k0, t.m0);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < kBM / kMnChunk; ++c)
+                                tma_load_2d_pair(dA + c * kMnLbo, &tmA, lbar, t.m0 + kMnChunk * c, t.row0 + k0);
+                        }
+                        if (!B_MN) {
+                            const int brow = SPLIT ? t.e * a.b_rows_e + rank * a.b_up + t.n0 : b_row0 + rank * (BN / 2);
+                            tma_load_2d_pair(dB, &tmB, lbar, k0, brow);
+                        } else {
+                            const int krow = WGRAD ? t.row0 + k0 : t.e * a.b_rows_e + k0;
+                            constexpr int nch = BN / kMnChunk;
+#pragma unroll
+                            for (int c = 0; c < nch / 2; ++c)
+                                tma_load_2d_pair(dB + c * kMnLbo, &tmB, lbar, t.n0 + kMnChunk * (rank * nch / 2 + c), krow);
+                        }
+                        ++issued;
+                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
+                    mbar_arrive_expect_tx(full + stage, kStageBytes);
                     if (!A_MN) {
                         tma_load_2d(dA, &tmA, full + stage, k0, t.m0);
                     } else {
@@ -383,7 +422,19 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && TWO && rank == 1) {
+            // peer of a two-SM pair: its copies complete on the leader's barriers and the leader
+            // issues the MMAs; before exiting, wait for the leader's releases of its last stages
+            long long consumed = 0;
+            for (int L = unit0; L < num_tiles; L += unit_stride)
+                consumed += decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank).kb;
+            for (int s = 0; s < kStages; ++s) {
+                if (consumed > s) {
+                    const long long n = (consumed - s + kStages - 1) / kStages;
+                    drain_wait(empty + s, (uint32_t)((n - 1) & 1));
+                }
+            }
+        } else if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -393,7 +444,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             long long consumed = 0;
             for (int L = unit0; L < num_tiles && ok; L += unit_stride) {
                 const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
-                if (!mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                if (!(TWO ? mbar_wait_cluster(tempty + acc, acc_phase ^ 1u, abort_flag, a.status)
+                          : mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag, a.status))) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < t.kb; ++kb) {
@@ -422,10 +474,13 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                                                      : sdesc_sw128(sa + ks * kKStep, 16, 1024);
                             const uint64_t bd = B_MN ? sdesc_sw128(sb + ks * kMnStep, kMnLbo, 1024)
                                                      : sdesc_sw128(sb + ks * kKStep, 16, 1024);
-                            mma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0);
+                            if constexpr (TWO) mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | ks) != 0);
+                            else mma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0);
                         }
                     }
-                    if (PAIR)
+                    if (TWO)
+                        mma_commit_pair_mc(empty + stage, kPeers);
+                    else if (PAIR)
                         mma_commit_mc(empty + stage, kPeers);
                     else
                         mma_commit(empty + stage);
@@ -433,7 +488,18 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                if (t.kb > 0) mma_commit(tfull + acc); else mbar_arrive(tfull + acc);
+                if (TWO) {
+                    if (t.kb > 0) {
+                        mma_commit_pair_mc(tfull + acc, kPeers);
+                    } else {
+                        mbar_arrive(tfull + acc);
+                        mbar_arrive_cluster(tfull + acc, 1);
+                    }
+                } else if (t.kb > 0) {
+                    mma_commit(tfull + acc);
+                } else {
+                    mbar_arrive(tfull + acc);
+                }
                 if (kAccStages == 2) {
                     acc ^= 1;
                     if (acc == 0) acc_phase ^= 1u;
@@ -442,7 +508,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 }
             }
             if (!ok) {
-                mma_commit(drain);
+                if constexpr (TWO) mma_commit_pair_mc(drain, 0x1);
+                else mma_commit(drain);
                 drain_wait(drain, 0);
             } else if (PAIR) {
                 // both CTAs' releases of the last stages have landed here before the CTA may exit
@@ -479,7 +546,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 tmem_ld32(tcol + 64, d + 64);
                 tmem_ld32(tcol + 96, d + 96);
                 tc_fence_before();
-                mbar_arrive(tempty + acc);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty + acc);
                 if (t.valid) epilogue_drained<BN, EPI>(a, t, grow, half, d);
                 acc_phase ^= 1u;
                 continue;
@@ -588,7 +656,11 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(tempty + acc);
+            __syncwarp();
+            if (lane == 0) {
+                if (TWO && rank == 1) mbar_arrive_cluster(tempty + acc, 0);   // the leader's MMAs reuse it
+                else mbar_arrive(tempty + acc);
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -599,7 +671,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     if (PAIR) cluster_sync();   // no multicast or release from the peer is still in flight
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (TWO) tmem_dealloc_pair(tmem_base, kTmemCols);
+        else tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -645,14 +718,21 @@ static bool tmap_2d(CUtensorMap* m, const void* ptr, int esize, uint64_t inner, 
 // 1024 rows per expert) outweighed the saved L2 traffic on GB300, so they run one CTA per tile.
 template <bool WGRAD>
 constexpr bool use_pairs() { return WGRAD; }
+// Two-SM MMAs (256 x 256 per CTA pair, each SM holding half of every B tile) for the BF16 weight
+// gradients and the backward gate/up product, where they measured 6-10% faster on GB300; the
+// forward products and the SwiGLU backward keep one CTA per 128 x 256 tile (a grouped-M pair
+// needs two m-tiles of one expert, and the duplicated odd tiles cancel the gain there).
+template <int BN, bool MX, bool WGRAD, int EPI>
+constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN); }
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a) {
-    constexpr bool PAIR = use_pairs<WGRAD>();
-    auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR>;
+    constexpr bool TWO = use_two<BN, MX, WGRAD, EPI>();
+    constexpr bool PAIR = TWO || use_pairs<WGRAD>();
+    auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR, TWO>;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
-    const size_t stage = (size_t)kATileBytes + BN * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
-    const size_t fixed = 1024 + kStages * stage + 128;
+    const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
+    const size_t fixed = 1024 + ring_stages<TWO>() * stage + 256;
     const size_t smem = fixed + (size_t)2 * (a.E + 1) * 4;
     const size_t smem_max = fixed + (size_t)2 * (kMaxExperts + 1) * 4;
     static std::once_flag once;
