@@ -49,6 +49,9 @@ template <int EPI, bool SINGLE>
 constexpr int epi_warps() { return (EPI == EPI_SWIGLU_BWD || SINGLE) ? 8 : 4; }
 template <int EPI, bool SINGLE>
 constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI, SINGLE>(); }
+// BF16 epilogues whose only output is a 256-column bf16 row block (down-projection, data gradient)
+template <int EPI, bool MX>
+constexpr bool tma_out() { return !MX && (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN); }
 
 struct GemmArgs {
     const int* mtile;          // [E+1] prefix of 128-row tiles per expert
@@ -216,7 +219,7 @@ constexpr int ring_stages() { return TWO ? 6 : kStages; }
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool PAIR, bool TWO>
 __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmArgs a) {
+                        const __grid_constant__ CUtensorMap tmC, const GemmArgs a) {
     static_assert(!TWO || (PAIR && !MX), "two-SM MMAs run in CTA pairs, BF16 only");
     constexpr int kStages = ring_stages<TWO>();
     constexpr int kElems = MX ? 128 : 64;                // K elements per stage
@@ -239,13 +242,19 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     constexpr uint32_t kKStep = kMmaK * (MX ? 1 : 2);    // K-major: bytes per MMA K step
     static_assert(!MX || BN == 128 || BN == 256, "MXFP8 tiles are 128 x 128 or 128 x 256");
     static_assert(!kSingle || EPI != EPI_SWIGLU_BWD, "the SwiGLU backward keeps 128-wide MXFP8 tiles");
+    // BF16 row outputs of the down and data-gradient products: each epilogue warp stages 32 rows x
+    // 64 columns (4 KB, 128-byte swizzle) in shared memory and writes them with a TMA store (tmC),
+    // so that L2 receives whole lines rather than 16-byte halves of sectors
+    constexpr bool kTmaOut = tma_out<EPI, MX>();
+    constexpr int kOutBytes = kTmaOut ? kEpiWarps * 4096 : 0;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + kStages * kATileBytes;
     uint8_t* sSF = sB + kStages * kBTileBytes;           // MXFP8: per stage A atom then B atoms
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sSF + kStages * kSfBytes);
+    uint8_t* sOut = sSF + kStages * kSfBytes;           // TMA-stored outputs: a 4 KB box per epilogue warp
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kOutBytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
     uint64_t* tfull = bars + 2 * kStages;
@@ -578,6 +587,37 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                             store_bf16x32(hid + grow * (long long)a.I + col, v);
                     }
                 }
+            } else if constexpr (kTmaOut) {
+                float w = 1.f;
+                if constexpr (EPI == EPI_WEIGHTED) {
+                    const int slot = a.row_slot[grow];
+                    w = slot >= 0 ? a.topk_w[slot] : 0.f;
+                }
+                uint8_t* box = sOut + (warp - 2) * 4096;
+                const uint32_t sbox = smem_u32(box);
+#pragma unroll 1
+                for (int b = 0; b < BN / 64; ++b) {
+                    if (lane == 0) bulk_wait_read<0>();   // the previous box has been read out
+                    __syncwarp();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        tmem_ld32(tacc + 64 * b + 32 * h, v);
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const float* f = v + 8 * cc;
+                            const uint4 pk = make_uint4(pack_bf16x2(w * f[0], w * f[1]), pack_bf16x2(w * f[2], w * f[3]),
+                                                        pack_bf16x2(w * f[4], w * f[5]), pack_bf16x2(w * f[6], w * f[7]));
+                            // row `lane`, 16-byte chunk 4 h + cc, 128-byte swizzle
+                            st_shared_v4(sbox + lane * 128 + (((4 * h + cc) ^ (lane & 7)) << 4), pk);
+                        }
+                    }
+                    fence_proxy_async_cta();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, box, t.n0 + 64 * b, t.m0 + 32 * quarter);
+                        bulk_commit();
+                    }
+                }
             } else if constexpr (EPI == EPI_WEIGHTED) {
                 const int slot = a.row_slot[grow];
                 const float w = slot >= 0 ? a.topk_w[slot] : 0.f;
@@ -664,6 +704,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (kTmaOut && lane == 0) bulk_wait_all();   // the stores are complete before the CTA exits
     }
     __syncwarp();
     tc_fence_before();
@@ -726,13 +767,17 @@ template <int BN, bool MX, bool WGRAD, int EPI>
 constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN); }
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
-static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a) {
+static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                       const CUtensorMap* tc = nullptr) {
+    static_assert(!tma_out<EPI, MX>() || BN == 256, "TMA-stored outputs are 256-column tiles");
     constexpr bool TWO = use_two<BN, MX, WGRAD, EPI>();
     constexpr bool PAIR = TWO || use_pairs<WGRAD>();
     auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR, TWO>;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
-    const size_t fixed = 1024 + ring_stages<TWO>() * stage + 256;
+    const size_t fixed = 1024 + ring_stages<TWO>() * stage + (tma_out<EPI, MX>() ? 4 * 4096 : 0) + 256;
+    if (tma_out<EPI, MX>() && !tc) return cudaErrorInvalidValue;
+    const CUtensorMap& tcm = tc ? *tc : ta;   // kernels without a TMA-stored output never read it
     const size_t smem = fixed + (size_t)2 * (a.E + 1) * 4;
     const size_t smem_max = fixed + (size_t)2 * (kMaxExperts + 1) * 4;
     static std::once_flag once;
@@ -761,7 +806,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (!PAIR) {
-        kern<<<c.num_sms, kThreads, smem, c.st>>>(ta, tb, a);
+        kern<<<c.num_sms, kThreads, smem, c.st>>>(ta, tb, tcm, a);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -776,7 +821,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     cfg.stream = c.st;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, a);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tcm, a);
 }
 
 int bwd_down_bn(int64_t I) { return (I % 256 == 0) ? 256 : 128; }
@@ -785,7 +830,7 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
     const Layout& L = *c.L;
     char* b = c.base;
     const int64_t H = L.H, I = L.I, E = L.E, R = L.rows;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tc;
     switch (kind) {
         case GemmKind::FwdGateUp:
         case GemmKind::FwdGateUpSaveOnly:
@@ -797,10 +842,12 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
                        ? run<256, false, false, true, false, EPI_SWIGLU, false>(c, ta, tb, a)
                        : run<256, false, false, true, false, EPI_GU_ONLY, false>(c, ta, tb, a);
         case GemmKind::FwdDown:
-            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 256)) return cudaErrorInvalidValue;
+            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 256) ||
+                !tmap_2d(&tc, b + L.ypart, 2, H, R, 32))
+                return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 64); a.b_rows_e = (int)H;
             a.out0 = b + L.ypart; a.ld0 = (int)H;
-            return run<256, false, false, false, false, EPI_WEIGHTED, false>(c, ta, tb, a);
+            return run<256, false, false, false, false, EPI_WEIGHTED, false>(c, ta, tb, a, &tc);
         case GemmKind::BwdDown: {
             const int bn = bwd_down_bn(I);
             if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 64))
@@ -811,11 +858,12 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
                              : run<128, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a);
         }
         case GemmKind::BwdGateUp:
-            if (!tmap_2d(&ta, b + L.dg, 2, 2 * I, R, 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 64))
+            if (!tmap_2d(&ta, b + L.dg, 2, 2 * I, R, 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 64) ||
+                !tmap_2d(&tc, b + L.ypart, 2, H, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(2 * I / 64); a.b_rows_e = (int)(2 * I);
             a.out0 = b + L.ypart; a.ld0 = (int)H;
-            return run<256, false, true, false, false, EPI_PLAIN, false>(c, ta, tb, a);
+            return run<256, false, true, false, false, EPI_PLAIN, false>(c, ta, tb, a, &tc);
         case GemmKind::WgradDown: {
             const int bn = bwd_down_bn(I);
             if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 64) || !tmap_2d(&tb, b + L.hw, 2, I, R, 64))
