@@ -49,9 +49,51 @@ template <int EPI, bool SINGLE>
 constexpr int epi_warps() { return (EPI == EPI_SWIGLU_BWD || SINGLE) ? 8 : 4; }
 template <int EPI, bool SINGLE>
 constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI, SINGLE>(); }
-// BF16 epilogues whose only output is a 256-column bf16 row block (down-projection, data gradient)
-template <int EPI, bool MX>
-constexpr bool tma_out() { return !MX && (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN); }
+// Epilogues of four warps that write bf16 / fp32 row blocks from the accumulator: they stage
+// them in shared memory and store them by TMA (the drained MXFP8 128 x 256 tiles keep direct stores)
+template <int EPI, bool MX, int BN>
+constexpr bool tma_out() {
+    return !(MX && BN == 256) && epi_warps<EPI, MX && BN == 256>() == 4 &&
+           (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WGRAD);
+}
+
+// ---- staged TMA stores: one 32-row x 128-byte box per epilogue warp, row = lane ----------------
+// waits until the warp's previous box has been read out by its TMA store
+__device__ __forceinline__ void box_acquire(int lane) {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+}
+// 16-byte chunk `chunk` of the lane's row, 128-byte swizzle (the box is 1024-byte aligned)
+__device__ __forceinline__ void box_put(uint32_t sbox, int lane, int chunk, uint4 v) {
+    st_shared_v4(sbox + lane * 128 + ((chunk ^ (lane & 7)) << 4), v);
+}
+// 32 values as bf16 into chunks [4 h, 4 h + 4) (columns [32 h, 32 h + 32) of a 64-column box)
+__device__ __forceinline__ void box_put_bf16x32(uint32_t sbox, int lane, int h, const float* v, float scale) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const float* f = v + 8 * cc;
+        box_put(sbox, lane, 4 * h + cc,
+                make_uint4(pack_bf16x2(scale * f[0], scale * f[1]), pack_bf16x2(scale * f[2], scale * f[3]),
+                           pack_bf16x2(scale * f[4], scale * f[5]), pack_bf16x2(scale * f[6], scale * f[7])));
+    }
+}
+// 32 fp32 values: the whole 128-byte row of a 32-column box
+__device__ __forceinline__ void box_put_f32x32(uint32_t sbox, int lane, const float* v) {
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc)
+        box_put(sbox, lane, cc,
+                make_uint4(__float_as_uint(v[4 * cc]), __float_as_uint(v[4 * cc + 1]), __float_as_uint(v[4 * cc + 2]),
+                           __float_as_uint(v[4 * cc + 3])));
+}
+// hands the staged box to the async proxy and stores it at {c0 (column), c1 (row)}
+__device__ __forceinline__ void box_store(const CUtensorMap* m, uint8_t* box, int lane, int c0, int c1) {
+    fence_proxy_async_cta();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(m, box, c0, c1);
+        bulk_commit();
+    }
+}
 
 struct GemmArgs {
     const int* mtile;          // [E+1] prefix of 128-row tiles per expert
@@ -219,7 +261,8 @@ constexpr int ring_stages() { return TWO ? 6 : kStages; }
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool PAIR, bool TWO>
 __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const GemmArgs a) {
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                        const GemmArgs a) {
     static_assert(!TWO || (PAIR && !MX), "two-SM MMAs run in CTA pairs, BF16 only");
     constexpr int kStages = ring_stages<TWO>();
     constexpr int kElems = MX ? 128 : 64;                // K elements per stage
@@ -242,10 +285,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     constexpr uint32_t kKStep = kMmaK * (MX ? 1 : 2);    // K-major: bytes per MMA K step
     static_assert(!MX || BN == 128 || BN == 256, "MXFP8 tiles are 128 x 128 or 128 x 256");
     static_assert(!kSingle || EPI != EPI_SWIGLU_BWD, "the SwiGLU backward keeps 128-wide MXFP8 tiles");
-    // BF16 row outputs of the down and data-gradient products: each epilogue warp stages 32 rows x
-    // 64 columns (4 KB, 128-byte swizzle) in shared memory and writes them with a TMA store (tmC),
-    // so that L2 receives whole lines rather than 16-byte halves of sectors
-    constexpr bool kTmaOut = tma_out<EPI, MX>();
+    // Row outputs of four-warp epilogues: each warp stages 32 rows x 128 bytes (64 bf16 or 32 fp32
+    // columns, 128-byte swizzle) in shared memory and writes them with a TMA store (tmC; tmD for the
+    // saved [g|u]), so that L2 receives whole lines rather than 16-byte halves of sectors
+    constexpr bool kTmaOut = tma_out<EPI, MX, BN>();
     constexpr int kOutBytes = kTmaOut ? kEpiWarps * 4096 : 0;
 
     extern __shared__ uint8_t smem_raw[];
@@ -563,6 +606,91 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             }
             if (!t.valid) {
                 // duplicate tile of a CTA pair: nothing to store
+            } else if constexpr (kTmaOut) {
+                uint8_t* box = sOut + (warp - 2) * 4096;
+                const uint32_t sbox = smem_u32(box);
+                const int brow = t.m0 + 32 * quarter;   // first row of the warp's boxes
+                if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
+                    // columns [0, BN/2) = gate, [BN/2, BN) = up, for I-columns [n0, n0 + BN/2); per
+                    // 64 I-columns: the h box, then (saving) the g and u boxes, re-read from TMEM
+#pragma unroll 1
+                    for (int b = 0; b < BN / 128; ++b) {
+                        if (EPI == EPI_SWIGLU) {
+                            box_acquire(lane);
+#pragma unroll 1
+                            for (int h = 0; h < 2; ++h) {
+                                float u[32];
+                                tmem_ld32(tacc + 64 * b + 32 * h, v);
+                                tmem_ld32(tacc + BN / 2 + 64 * b + 32 * h, u);
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] = v[j] * sigmoidf_fast(v[j]) * u[j];
+                                box_put_bf16x32(sbox, lane, h, v, 1.f);
+                            }
+                            box_store(&tmC, box, lane, t.n0 + 64 * b, brow);
+                        }
+                        if (EPI == EPI_GU_ONLY || a.save_gu) {
+#pragma unroll 1
+                            for (int p = 0; p < 2; ++p) {   // g, then u
+                                box_acquire(lane);
+#pragma unroll 1
+                                for (int h = 0; h < 2; ++h) {
+                                    tmem_ld32(tacc + (BN / 2) * p + 64 * b + 32 * h, v);
+                                    box_put_bf16x32(sbox, lane, h, v, 1.f);
+                                }
+                                box_store(&tmD, box, lane, a.I * p + t.n0 + 64 * b, brow);
+                            }
+                        }
+                    }
+                } else if constexpr (EPI == EPI_WGRAD) {
+                    // rows of this expert's block of the weight gradient [E * M, N]
+                    const int orow = t.e * a.m_tiles * kBM + brow;
+                    if (a.out_f32) {
+#pragma unroll 1
+                        for (int b = 0; b < BN / 32; ++b) {
+                            box_acquire(lane);
+                            if (t.kb > 0) {
+                                tmem_ld32(tacc + 32 * b, v);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                            }
+                            box_put_f32x32(sbox, lane, v);
+                            box_store(&tmC, box, lane, t.n0 + 32 * b, orow);
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int b = 0; b < BN / 64; ++b) {
+                            box_acquire(lane);
+#pragma unroll 1
+                            for (int h = 0; h < 2; ++h) {
+                                if (t.kb > 0) {
+                                    tmem_ld32(tacc + 64 * b + 32 * h, v);
+                                } else {
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                                }
+                                box_put_bf16x32(sbox, lane, h, v, 1.f);
+                            }
+                            box_store(&tmC, box, lane, t.n0 + 64 * b, orow);
+                        }
+                    }
+                } else {   // EPI_WEIGHTED, EPI_PLAIN: one bf16 row block
+                    float w = 1.f;
+                    if constexpr (EPI == EPI_WEIGHTED) {
+                        const int slot = a.row_slot[grow];
+                        w = slot >= 0 ? a.topk_w[slot] : 0.f;
+                    }
+#pragma unroll 1
+                    for (int b = 0; b < BN / 64; ++b) {
+                        box_acquire(lane);
+#pragma unroll 1
+                        for (int h = 0; h < 2; ++h) {
+                            tmem_ld32(tacc + 64 * b + 32 * h, v);
+                            box_put_bf16x32(sbox, lane, h, v, w);
+                        }
+                        box_store(&tmC, box, lane, t.n0 + 64 * b, brow);
+                    }
+                }
             } else if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
                 // columns [0, BN/2) = gate, [BN/2, BN) = up, for I-columns [n0, n0 + BN/2)
                 __nv_bfloat16* hid = reinterpret_cast<__nv_bfloat16*>(a.out0);
@@ -585,37 +713,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                                         a.q0_sf + sf_index(grow, col / 32, a.I / 128));
                         else
                             store_bf16x32(hid + grow * (long long)a.I + col, v);
-                    }
-                }
-            } else if constexpr (kTmaOut) {
-                float w = 1.f;
-                if constexpr (EPI == EPI_WEIGHTED) {
-                    const int slot = a.row_slot[grow];
-                    w = slot >= 0 ? a.topk_w[slot] : 0.f;
-                }
-                uint8_t* box = sOut + (warp - 2) * 4096;
-                const uint32_t sbox = smem_u32(box);
-#pragma unroll 1
-                for (int b = 0; b < BN / 64; ++b) {
-                    if (lane == 0) bulk_wait_read<0>();   // the previous box has been read out
-                    __syncwarp();
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        tmem_ld32(tacc + 64 * b + 32 * h, v);
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            const float* f = v + 8 * cc;
-                            const uint4 pk = make_uint4(pack_bf16x2(w * f[0], w * f[1]), pack_bf16x2(w * f[2], w * f[3]),
-                                                        pack_bf16x2(w * f[4], w * f[5]), pack_bf16x2(w * f[6], w * f[7]));
-                            // row `lane`, 16-byte chunk 4 h + cc, 128-byte swizzle
-                            st_shared_v4(sbox + lane * 128 + (((4 * h + cc) ^ (lane & 7)) << 4), pk);
-                        }
-                    }
-                    fence_proxy_async_cta();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmC, box, t.n0 + 64 * b, t.m0 + 32 * quarter);
-                        bulk_commit();
                     }
                 }
             } else if constexpr (EPI == EPI_WEIGHTED) {
@@ -747,7 +844,9 @@ static bool tmap_2d(CUtensorMap* m, const void* ptr, int esize, uint64_t inner, 
     const cuuint64_t strides[1] = {inner * esize};
     const cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / esize), box_rows};
     const cuuint32_t es[2] = {1, 1};
-    const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const CUtensorMapDataType dt = esize == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -768,16 +867,16 @@ constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                       const CUtensorMap* tc = nullptr) {
-    static_assert(!tma_out<EPI, MX>() || BN == 256, "TMA-stored outputs are 256-column tiles");
+                       const CUtensorMap* tc = nullptr, const CUtensorMap* td = nullptr) {
     constexpr bool TWO = use_two<BN, MX, WGRAD, EPI>();
     constexpr bool PAIR = TWO || use_pairs<WGRAD>();
     auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR, TWO>;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
-    const size_t fixed = 1024 + ring_stages<TWO>() * stage + (tma_out<EPI, MX>() ? 4 * 4096 : 0) + 256;
-    if (tma_out<EPI, MX>() && !tc) return cudaErrorInvalidValue;
+    const size_t fixed = 1024 + ring_stages<TWO>() * stage + (tma_out<EPI, MX, BN>() ? 4 * 4096 : 0) + 256;
+    if (tma_out<EPI, MX, BN>() && !tc) return cudaErrorInvalidValue;
     const CUtensorMap& tcm = tc ? *tc : ta;   // kernels without a TMA-stored output never read it
+    const CUtensorMap& tdm = td ? *td : tcm;
     const size_t smem = fixed + (size_t)2 * (a.E + 1) * 4;
     const size_t smem_max = fixed + (size_t)2 * (kMaxExperts + 1) * 4;
     static std::once_flag once;
@@ -806,7 +905,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (!PAIR) {
-        kern<<<c.num_sms, kThreads, smem, c.st>>>(ta, tb, tcm, a);
+        kern<<<c.num_sms, kThreads, smem, c.st>>>(ta, tb, tcm, tdm, a);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -821,7 +920,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     cfg.stream = c.st;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tcm, a);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tcm, tdm, a);
 }
 
 int bwd_down_bn(int64_t I) { return (I % 256 == 0) ? 256 : 128; }
@@ -830,17 +929,19 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
     const Layout& L = *c.L;
     char* b = c.base;
     const int64_t H = L.H, I = L.I, E = L.E, R = L.rows;
-    CUtensorMap ta, tb, tc;
+    const int oes = a.out_f32 ? 4 : 2;   // weight-gradient output element size
+    CUtensorMap ta, tb, tc, td;
     switch (kind) {
         case GemmKind::FwdGateUp:
         case GemmKind::FwdGateUpSaveOnly:
-            if (!tmap_2d(&ta, b + L.xperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 128))
+            if (!tmap_2d(&ta, b + L.xperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 128) ||
+                !tmap_2d(&tc, b + L.hid, 2, I, R, 32) || !tmap_2d(&td, b + L.gu, 2, 2 * I, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 64); a.b_rows_e = (int)(2 * I); a.b_up = (int)I;
             a.out0 = b + L.hid; a.out1 = b + L.gu;
             return kind == GemmKind::FwdGateUp
-                       ? run<256, false, false, true, false, EPI_SWIGLU, false>(c, ta, tb, a)
-                       : run<256, false, false, true, false, EPI_GU_ONLY, false>(c, ta, tb, a);
+                       ? run<256, false, false, true, false, EPI_SWIGLU, false>(c, ta, tb, a, &tc, &td)
+                       : run<256, false, false, true, false, EPI_GU_ONLY, false>(c, ta, tb, a, &tc, &td);
         case GemmKind::FwdDown:
             if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 256) ||
                 !tmap_2d(&tc, b + L.ypart, 2, H, R, 32))
@@ -866,19 +967,21 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
             return run<256, false, true, false, false, EPI_PLAIN, false>(c, ta, tb, a, &tc);
         case GemmKind::WgradDown: {
             const int bn = bwd_down_bn(I);
-            if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 64) || !tmap_2d(&tb, b + L.hw, 2, I, R, 64))
+            if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 64) || !tmap_2d(&tb, b + L.hw, 2, I, R, 64) ||
+                !tmap_2d(&tc, out, oes, I, E * H, 32))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / bn);
             a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
-            return bn == 256 ? run<256, true, true, false, true, EPI_WGRAD, false>(c, ta, tb, a)
-                             : run<128, true, true, false, true, EPI_WGRAD, false>(c, ta, tb, a);
+            return bn == 256 ? run<256, true, true, false, true, EPI_WGRAD, false>(c, ta, tb, a, &tc)
+                             : run<128, true, true, false, true, EPI_WGRAD, false>(c, ta, tb, a, &tc);
         }
         case GemmKind::WgradGateUp:
-            if (!tmap_2d(&ta, b + L.dg, 2, 2 * I, R, 64) || !tmap_2d(&tb, b + L.xperm, 2, H, R, 64))
+            if (!tmap_2d(&ta, b + L.dg, 2, 2 * I, R, 64) || !tmap_2d(&tb, b + L.xperm, 2, H, R, 64) ||
+                !tmap_2d(&tc, out, oes, H, E * 2 * I, 32))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 256);
             a.out0 = out; a.ld0 = (int)H; a.out_e_stride = 2 * I * H;
-            return run<256, true, true, false, true, EPI_WGRAD, false>(c, ta, tb, a);
+            return run<256, true, true, false, true, EPI_WGRAD, false>(c, ta, tb, a, &tc);
     }
     return cudaErrorInvalidValue;
 }
@@ -892,7 +995,8 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
     char* b = c.base;
     const int64_t H = L.H, I = L.I, E = L.E, R = L.rows;
     auto u8 = [&](size_t off) { return reinterpret_cast<const uint8_t*>(b + off); };
-    CUtensorMap ta, tb;
+    const int oes = a.out_f32 ? 4 : 2;   // weight-gradient output element size
+    CUtensorMap ta, tb, tc;
     switch (kind) {
         case GemmKind::FwdGateUp:
         case GemmKind::FwdGateUpSaveOnly:
@@ -938,21 +1042,23 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             // weight gradients keep 128 x 128 tiles with two accumulators: their contraction over an
             // expert's rows is short, so a drained single accumulator would stall the MMAs, and the
             // fp32 output stores need the epilogue to overlap the next tile; a pair splits B's K rows
-            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 64))
+            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 64) ||
+                !tmap_2d(&tc, out, oes, I, E * H, 32))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / 128);
             a.sfA = u8(M.dy_c_sf); a.sfA_kt = (int)(R / 128);
             a.sfB = u8(M.hw_c_sf); a.sfB_kt = (int)(R / 128);
             a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
-            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a);
+            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
         case GemmKind::WgradGateUp:
-            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 64))
+            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 64) ||
+                !tmap_2d(&tc, out, oes, H, E * 2 * I, 32))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 128);
             a.sfA = u8(M.dg_c_sf); a.sfA_kt = (int)(R / 128);
             a.sfB = u8(M.x_c_sf); a.sfB_kt = (int)(R / 128);
             a.out0 = out; a.ld0 = (int)H; a.out_e_stride = 2 * I * H;
-            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a);
+            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
     }
     return cudaErrorInvalidValue;
 }
