@@ -53,9 +53,14 @@ constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI, SINGLE>(); }
 // them in shared memory and store them by TMA (the drained MXFP8 128 x 256 tiles keep direct stores)
 template <int EPI, bool MX, int BN>
 constexpr bool tma_out() {
-    return !(MX && BN == 256) && epi_warps<EPI, MX && BN == 256>() == 4 &&
-           (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WGRAD);
+    return (!(MX && BN == 256) && epi_warps<EPI, MX && BN == 256>() == 4 &&
+            (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WGRAD)) ||
+           (!MX && EPI == EPI_SWIGLU_BWD);
 }
+// bytes of one warp's staging box: 32 rows x 128 bytes, or 32 x 64 (64-byte swizzle) for the
+// eight warps of the SwiGLU backward, whose 4 KB boxes would not fit beside the ring
+template <int EPI>
+constexpr int out_box_bytes() { return EPI == EPI_SWIGLU_BWD ? 2048 : 4096; }
 
 // ---- staged TMA stores: one 32-row x 128-byte box per epilogue warp, row = lane ----------------
 // waits until the warp's previous box has been read out by its TMA store
@@ -84,6 +89,16 @@ __device__ __forceinline__ void box_put_f32x32(uint32_t sbox, int lane, const fl
         box_put(sbox, lane, cc,
                 make_uint4(__float_as_uint(v[4 * cc]), __float_as_uint(v[4 * cc + 1]), __float_as_uint(v[4 * cc + 2]),
                            __float_as_uint(v[4 * cc + 3])));
+}
+// 32 values as bf16 into a 32-row x 64-byte box (64-byte swizzle; the box is 512-byte aligned)
+__device__ __forceinline__ void box64_put_bf16x32(uint32_t sbox, int lane, const float* v) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const float* f = v + 8 * cc;
+        st_shared_v4(sbox + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4),
+                     make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                pack_bf16x2(f[6], f[7])));
+    }
 }
 // hands the staged box to the async proxy and stores it at {c0 (column), c1 (row)}
 __device__ __forceinline__ void box_store(const CUtensorMap* m, uint8_t* box, int lane, int c0, int c1) {
@@ -289,7 +304,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     // columns, 128-byte swizzle) in shared memory and writes them with a TMA store (tmC; tmD for the
     // saved [g|u]), so that L2 receives whole lines rather than 16-byte halves of sectors
     constexpr bool kTmaOut = tma_out<EPI, MX, BN>();
-    constexpr int kOutBytes = kTmaOut ? kEpiWarps * 4096 : 0;
+    constexpr int kOutBytes = kTmaOut ? kEpiWarps * out_box_bytes<EPI>() : 0;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -606,7 +621,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             }
             if (!t.valid) {
                 // duplicate tile of a CTA pair: nothing to store
-            } else if constexpr (kTmaOut) {
+            } else if constexpr (kTmaOut && EPI != EPI_SWIGLU_BWD) {
                 uint8_t* box = sOut + (warp - 2) * 4096;
                 const uint32_t sbox = smem_u32(box);
                 const int brow = t.m0 + 32 * quarter;   // first row of the warp's boxes
@@ -762,6 +777,20 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         quant_col32_warp(g, a.q1 + gi + col, a.q1_sf, col, kblk, a.r_atoms);
                         quant_col32_warp(u, a.q1 + gi + a.I + col, a.q1_sf, a.I + col, kblk, a.r_atoms);
                         quant_col32_warp(v, a.q2 + grow * (long long)a.I + col, a.q2_sf, col, kblk, a.r_atoms);
+                    } else if constexpr (kTmaOut) {
+                        // dg, du and w h through the warp's 2 KB box, one after the other
+                        uint8_t* box = sOut + (warp - 2) * 2048;
+                        const uint32_t sbox = smem_u32(box);
+                        const int brow = t.m0 + 32 * quarter;
+                        box_acquire(lane);
+                        box64_put_bf16x32(sbox, lane, g);
+                        box_store(&tmC, box, lane, col, brow);
+                        box_acquire(lane);
+                        box64_put_bf16x32(sbox, lane, u);
+                        box_store(&tmC, box, lane, a.I + col, brow);
+                        box_acquire(lane);
+                        box64_put_bf16x32(sbox, lane, v);
+                        box_store(&tmD, box, lane, col, brow);
                     } else {
                         store_bf16x32(dG + grow * (2LL * a.I) + col, g);
                         store_bf16x32(dG + grow * (2LL * a.I) + a.I + col, u);
@@ -852,6 +881,20 @@ static bool tmap_2d(CUtensorMap* m, const void* ptr, int esize, uint64_t inner, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D tensor map with box {64 bytes, box_rows} and 64-byte swizzle (staged SwiGLU-backward outputs)
+static bool tmap_2d_sw64(CUtensorMap* m, const void* ptr, int esize, uint64_t inner, uint64_t outer,
+                         uint32_t box_rows) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * esize};
+    const cuuint32_t box[2] = {(cuuint32_t)(64 / esize), box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The weight-gradient products run as clusters of two CTAs sharing B tiles (PAIR): their m-tiles
 // (feature rows) always come in pairs of one expert.  For the grouped-M products a pair needs two
 // m-tiles of one expert, and the duplicate tile of every odd expert (about 6% more MMA work at
@@ -873,7 +916,8 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR, TWO>;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
-    const size_t fixed = 1024 + ring_stages<TWO>() * stage + (tma_out<EPI, MX, BN>() ? 4 * 4096 : 0) + 256;
+    const size_t out_bytes = tma_out<EPI, MX, BN>() ? (size_t)epi_warps<EPI, MX && BN == 256>() * out_box_bytes<EPI>() : 0;
+    const size_t fixed = 1024 + ring_stages<TWO>() * stage + out_bytes + 256;
     if (tma_out<EPI, MX, BN>() && !tc) return cudaErrorInvalidValue;
     const CUtensorMap& tcm = tc ? *tc : ta;   // kernels without a TMA-stored output never read it
     const CUtensorMap& tdm = td ? *td : tcm;
@@ -951,12 +995,13 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
             return run<256, false, false, false, false, EPI_WEIGHTED, false>(c, ta, tb, a, &tc);
         case GemmKind::BwdDown: {
             const int bn = bwd_down_bn(I);
-            if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 64))
+            if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 64) ||
+                !tmap_2d_sw64(&tc, b + L.dg, 2, 2 * I, R, 32) || !tmap_2d_sw64(&td, b + L.hw, 2, I, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(I / bn); a.k_blocks = (int)(H / 64); a.b_rows_e = (int)H;
             a.out0 = b + L.dg; a.out1 = b + L.hw; a.dtw = reinterpret_cast<float*>(b + L.dtw);
-            return bn == 256 ? run<256, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a)
-                             : run<128, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a);
+            return bn == 256 ? run<256, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a, &tc, &td)
+                             : run<128, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a, &tc, &td);
         }
         case GemmKind::BwdGateUp:
             if (!tmap_2d(&ta, b + L.dg, 2, 2 * I, R, 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 64) ||
