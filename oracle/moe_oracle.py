@@ -23,7 +23,11 @@ Readings where the pages are silent (each is also listed with the design notes):
 
 MXFP8 (OCP Microscaling v1.0, E4M3 elements, one E8M0 scale per 32 elements along the
 contraction axis): the oracle quantises and dequantises each GEMM operand at the point where the
-CUDA path feeds the block-scaled MMA, then computes in fp64.  The shared exponent of a block is
+CUDA path feeds the block-scaled MMA, then computes in fp64.  The pages also name an fp8_bwd
+precision, a BF16 forward with an FP8 backward (MarkTechPost, "Prime Intellect Releases Prime
+Mega MoE", section "How does the fused kernel work?"); on Blackwell its FP8 is read as MXFP8, so
+`fp8_bwd=True` keeps the forward operands exact and quantises only the four backward GEMMs'
+operands, at the same points as the MXFP8 backward.  The shared exponent of a block is
 floor(log2(amax)) - 8 (8 is the largest E4M3 exponent); elements are divided by 2^exp, rounded to
 the nearest E4M3 value (ties to even) and saturated to +-448.
 """
@@ -202,7 +206,7 @@ def forward(x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, keep: bool = F
 # ----------------------------------------------------------------------------------------------
 # backward of the loss L = <dy, y>
 # ----------------------------------------------------------------------------------------------
-def backward(dy, x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, keep: bool = False):
+def backward(dy, x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, fp8_bwd: bool = False, keep: bool = False):
     """Gradients of <dy, y> with respect to x, W13, W2 and topk_w.
 
     Per slot (t, j) routed to expert e, with g, u, h from the forward:
@@ -211,13 +215,15 @@ def backward(dy, x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, keep: boo
       du = dh * silu(g)                     dx[t] += W13[e,:I]^T dg + W13[e,I:]^T du
       dW2[e] += dy[t] (w h)^T               dW13[e,:I] += dg x[t]^T,  dW13[e,I:] += du x[t]^T
     In MXFP8 mode each GEMM operand is quantised along that GEMM's contraction axis first
-    (for the weight gradients the contraction runs over the tokens of one expert group).
+    (for the weight gradients the contraction runs over the tokens of one expert group); with
+    fp8_bwd only the backward GEMMs' operands are, the forward (g, u, h) staying exact.
     """
     dy, x, W13, W2 = _as64(dy), _as64(x), _as64(W13), _as64(W2)
     T, H = x.shape
     E, I2, _ = W13.shape
     I = I2 // 2
     k = topk_idx.shape[1]
+    qb = mxfp8 or fp8_bwd                    # backward GEMM operands quantised
     _, fw = forward(x, topk_idx, topk_w, W13, W2, mxfp8=mxfp8, keep=True)
     r = fw["route"]
     off = r["off"]
@@ -225,7 +231,7 @@ def backward(dy, x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, keep: boo
     X = fw["X_perm"]                         # already quantised along H in MXFP8 mode
     X_raw = permute_rows(x, r["perm"], k)
     dY = permute_rows(dy, r["perm"], k)
-    dYq = mx_qdq(dY, axis=1) if mxfp8 else dY
+    dYq = mx_qdq(dY, axis=1) if qb else dY
     S = T * k
     dA = np.zeros((S, I)); dG = np.zeros((S, 2 * I)); Hw = np.zeros((S, I)); dXp = np.zeros((S, H))
     dW13 = np.zeros_like(W13); dW2 = np.zeros_like(W2)
@@ -233,18 +239,18 @@ def backward(dy, x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, keep: boo
         lo, hi = off[e], off[e + 1]
         if hi == lo:
             continue
-        Wd = mx_qdq(W2[e], axis=0) if mxfp8 else W2[e]       # contraction over H: blocks along H
+        Wd = mx_qdq(W2[e], axis=0) if qb else W2[e]          # contraction over H: blocks along H
         dA[lo:hi] = dYq[lo:hi] @ Wd
         sg = sigmoid(g[lo:hi])
         dh = w_s[lo:hi, None] * dA[lo:hi]
         dG[lo:hi, :I] = dh * u[lo:hi] * sg * (1.0 + g[lo:hi] * (1.0 - sg))
         dG[lo:hi, I:] = dh * g[lo:hi] * sg
         Hw[lo:hi] = w_s[lo:hi, None] * h[lo:hi]
-        W = mx_qdq(W13[e], axis=0) if mxfp8 else W13[e]     # contraction over 2I: blocks along 2I
-        dGq = mx_qdq(dG[lo:hi], axis=1) if mxfp8 else dG[lo:hi]
+        W = mx_qdq(W13[e], axis=0) if qb else W13[e]        # contraction over 2I: blocks along 2I
+        dGq = mx_qdq(dG[lo:hi], axis=1) if qb else dG[lo:hi]
         dXp[lo:hi] = dGq @ W
     dtw_sorted = np.einsum("si,si->s", dA, h)
-    if mxfp8:
+    if qb:
         a6, b6 = mx_qdq_segments(dY, off), mx_qdq_segments(Hw, off)
         a7, b7 = mx_qdq_segments(dG, off), mx_qdq_segments(X_raw, off)
     else:
@@ -294,24 +300,27 @@ def _row_qdq(v):
     return mx_qdq(v[None], axis=1)[0]
 
 
-def backward_tokens(dy, x, topk_idx, topk_w, W13, W2, tokens, *, mxfp8: bool = False):
+def backward_tokens(dy, x, topk_idx, topk_w, W13, W2, tokens, *, mxfp8: bool = False, fp8_bwd: bool = False):
     """dx[t] and dtopk_w[t, :] for the listed tokens only (fp64), with the quantisation points of
-    `backward` in MXFP8 mode: x and dy along H, W13 along H (forward) and along 2I (dgrad), W2
-    along H (dgrad), [dg|du] along 2I."""
+    `backward`: in MXFP8 mode x along H and W13 along H (forward); in MXFP8 and fp8_bwd modes dy
+    along H, W13 along 2I and W2 along H (dgrad), [dg|du] along 2I."""
     I = W13.shape[1] // 2
     k = topk_idx.shape[1]
+    qb = mxfp8 or fp8_bwd
     dx = np.zeros((len(tokens), x.shape[1]))
     dtw = np.zeros((len(tokens), k))
     for n, t in enumerate(tokens):
         xt, dyt = _as64(x[t]), _as64(dy[t])
         if mxfp8:
-            xt, dyt = _row_qdq(xt), _row_qdq(dyt)
+            xt = _row_qdq(xt)
+        if qb:
+            dyt = _row_qdq(dyt)
         for j in range(k):
             e = int(topk_idx[t, j])
             W = _as64(W13[e]); Wd = _as64(W2[e])
             Wf = mx_qdq(W, axis=1) if mxfp8 else W          # forward: contraction over H
-            Wb = mx_qdq(W, axis=0) if mxfp8 else W          # dgrad: contraction over 2I
-            Wdb = mx_qdq(Wd, axis=0) if mxfp8 else Wd       # dgrad: contraction over H
+            Wb = mx_qdq(W, axis=0) if qb else W             # dgrad: contraction over 2I
+            Wdb = mx_qdq(Wd, axis=0) if qb else Wd          # dgrad: contraction over H
             g = Wf[:I] @ xt
             u = Wf[I:] @ xt
             sg = sigmoid(g)
@@ -319,18 +328,20 @@ def backward_tokens(dy, x, topk_idx, topk_w, W13, W2, tokens, *, mxfp8: bool = F
             dtw[n, j] = dA @ (silu(g) * u)
             dh = float(topk_w[t, j]) * dA
             dG = np.concatenate([dh * u * sg * (1.0 + g * (1.0 - sg)), dh * g * sg])
-            if mxfp8:
+            if qb:
                 dG = _row_qdq(dG)
             dx[n] += Wb.T @ dG
     return dx, dtw
 
 
-def wgrad_experts(dy, x, topk_idx, topk_w, W13, W2, experts, *, mxfp8: bool = False):
-    """(dW13[e], dW2[e]) for the listed experts only (fp64).  In MXFP8 mode the forward and dgrad
-    operands are quantised as in `backward`, and the weight-gradient operands along the expert's
-    tokens in slot order (blocks of 32 from the group's first token, zero-padded tail)."""
+def wgrad_experts(dy, x, topk_idx, topk_w, W13, W2, experts, *, mxfp8: bool = False, fp8_bwd: bool = False):
+    """(dW13[e], dW2[e]) for the listed experts only (fp64).  The forward (MXFP8 mode) and dgrad
+    (MXFP8 and fp8_bwd modes) operands are quantised as in `backward`, and the weight-gradient
+    operands along the expert's tokens in slot order (blocks of 32 from the group's first token,
+    zero-padded tail)."""
     I = W13.shape[1] // 2
     k = topk_idx.shape[1]
+    qb = mxfp8 or fp8_bwd
     flat = np.asarray(topk_idx).reshape(-1)
     wflat = _as64(topk_w).reshape(-1)
     res = []
@@ -341,8 +352,9 @@ def wgrad_experts(dy, x, topk_idx, topk_w, W13, W2, experts, *, mxfp8: bool = Fa
         W = _as64(W13[e]); Wd = _as64(W2[e])
         Xf, dYb, Wf, Wdb = X, dY, W, Wd
         if mxfp8:
-            Xf, dYb = mx_qdq(X, axis=1), mx_qdq(dY, axis=1)
-            Wf, Wdb = mx_qdq(W, axis=1), mx_qdq(Wd, axis=0)
+            Xf, Wf = mx_qdq(X, axis=1), mx_qdq(W, axis=1)
+        if qb:
+            dYb, Wdb = mx_qdq(dY, axis=1), mx_qdq(Wd, axis=0)
         g = Xf @ Wf[:I].T
         u = Xf @ Wf[I:].T
         sg = sigmoid(g)
@@ -351,7 +363,7 @@ def wgrad_experts(dy, x, topk_idx, topk_w, W13, W2, experts, *, mxfp8: bool = Fa
         dh = w * dA
         dG = np.concatenate([dh * u * sg * (1.0 + g * (1.0 - sg)), dh * g * sg], axis=1)
         Hw = w * h
-        if mxfp8 and len(slots):
+        if qb and len(slots):
             seg = np.array([0, len(slots)])
             dY, Hw = mx_qdq_segments(dY, seg), mx_qdq_segments(Hw, seg)
             dG, X = mx_qdq_segments(dG, seg), mx_qdq_segments(X, seg)

@@ -326,3 +326,79 @@ def test_mxfp8_error_is_at_quantisation_scale():
     yq = oracle.forward(x, idx, w, W13, W2, mxfp8=True)
     e = _rel(yq, y)
     assert 2e-3 < e < 8e-2
+
+
+# ---------------------------------------------------------------- fp8_bwd: BF16 forward, MXFP8 backward
+def _record_quantiser_calls(monkeypatch):
+    calls, in_seg = [], []
+    real, real_seg = oracle.moe_oracle.mx_qdq, oracle.moe_oracle.mx_qdq_segments
+
+    def rec(a, axis):
+        if not in_seg:
+            calls.append(("ax", np.shape(a), axis))
+        return real(a, axis)
+
+    def rec_seg(a, st):
+        calls.append(("seg", np.shape(a), 0))
+        in_seg.append(1)
+        try:
+            return real_seg(a, st)
+        finally:
+            in_seg.pop()
+    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", rec)
+    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq_segments", rec_seg)
+    return calls
+
+
+def test_fp8_bwd_quantises_only_the_backward_contractions(monkeypatch):
+    """fp8_bwd: the forward's X, W13 (along H), h and W2 (along I) stay exact; dY along H, W2 along
+    H, W13 and [dg|du] along 2I and the four weight-gradient operands along tokens are quantised."""
+    cfg = _small_cfg(T=40, H=64, I=96, E=3, k=2, seed=14)
+    x, idx, w, W13, W2, dy = _f64(gen.make_inputs(cfg))
+    calls = _record_quantiser_calls(monkeypatch)
+    oracle.backward(dy, x, idx, w, W13, W2, fp8_bwd=True)
+    H, I, S = 64, 96, 80
+    ax = [c for c in calls if c[0] == "ax"]
+    assert sum(1 for c in ax if c[1] == (S, H) and c[2] == 1) == 1       # dY_perm only, not X_perm
+    assert not any(c[1] == (H, I) and c[2] == 1 for c in ax)             # no forward W2 blocks
+    assert not any(c[1] == (I, H) and c[2] == 1 for c in ax)             # no forward W13 blocks
+    assert any(c[1] == (H, I) and c[2] == 0 for c in ax)                 # W2 along H (dgrad)
+    assert any(c[1] == (2 * I, H) and c[2] == 0 for c in ax)             # W13 along 2I (dgrad)
+    assert any(len(c[1]) == 2 and c[1][1] == 2 * I and c[2] == 1 for c in ax)   # [dg|du] along 2I
+    assert not any(len(c[1]) == 2 and c[1][1] == I and c[1][0] != H and c[2] == 1 for c in ax)  # no h
+    assert sum(1 for c in calls if c[0] == "seg") == 4
+
+
+def test_fp8_bwd_with_identity_quantiser_equals_bf16_path(monkeypatch):
+    cfg = _small_cfg(T=48, H=32, I=32, E=4, k=2, seed=15)
+    x, idx, w, W13, W2, dy = _f64(gen.make_inputs(cfg))
+    ref = oracle.backward(dy, x, idx, w, W13, W2)
+    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", lambda a, axis: np.asarray(a, dtype=np.float64))
+    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq_segments", lambda a, st: np.asarray(a, dtype=np.float64))
+    got = oracle.backward(dy, x, idx, w, W13, W2, fp8_bwd=True)
+    for k_ in ("dx", "dW13", "dW2", "dtopk_w"):
+        np.testing.assert_allclose(got[k_], ref[k_], rtol=1e-13, atol=1e-13)
+
+
+def test_fp8_bwd_sampled_forms_agree_with_full():
+    cfg = _small_cfg(T=80, H=32, I=16, E=6, k=3, seed=12)
+    x, idx, w, W13, W2, dy = _f64(gen.make_inputs(cfg))
+    g = oracle.backward(dy, x, idx, w, W13, W2, fp8_bwd=True)
+    toks = [0, 17, 79]
+    dx, dtw = oracle.backward_tokens(dy, x, idx, w, W13, W2, toks, fp8_bwd=True)
+    np.testing.assert_allclose(dx, g["dx"][toks], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dtw, g["dtopk_w"][toks], rtol=1e-11, atol=1e-12)
+    for e, (a, b) in zip([1, 4], oracle.wgrad_experts(dy, x, idx, w, W13, W2, [1, 4], fp8_bwd=True)):
+        np.testing.assert_allclose(a, g["dW13"][e], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(b, g["dW2"][e], rtol=1e-11, atol=1e-12)
+
+
+def test_fp8_bwd_error_is_at_quantisation_scale_and_differs_from_mxfp8():
+    cfg = gen.CONFIGS["tiny"]
+    x, idx, w, W13, W2, dy = _f64(gen.make_inputs(cfg))
+    ref = oracle.backward(dy, x, idx, w, W13, W2)
+    got = oracle.backward(dy, x, idx, w, W13, W2, fp8_bwd=True)
+    mx = oracle.backward(dy, x, idx, w, W13, W2, mxfp8=True)
+    for k_ in ("dx", "dW13", "dW2", "dtopk_w"):
+        assert 1e-3 < _rel(got[k_], ref[k_]) < 8e-2, k_
+        assert _rel(got[k_], mx[k_]) > 1e-4, k_       # the forward differs (exact vs quantised)
