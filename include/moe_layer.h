@@ -48,7 +48,10 @@ extern "C" {
 #endif
 
 /* ---- types ------------------------------------------------------------------------------- */
-typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
+/* MOE_FP8_BWD: the forward in BF16 and the backward in MXFP8 (the pages' fp8_bwd precision, a BF16
+ * forward with an FP8 backward: MarkTechPost, "Prime Intellect Releases Prime Mega MoE", section
+ * "How does the fused kernel work?"); y is bit-identical to MOE_BF16's. */
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_FP8_BWD = 2 } moe_precision;
 typedef enum { MOE_DT_BF16 = 0, MOE_DT_F32 = 1, MOE_DT_I32 = 2 } moe_dtype;
 
 /* A view of a caller-owned buffer: `data` is a device pointer for the layer calls. */
@@ -175,7 +178,8 @@ enum {
     MOE_VIEW_XPERM, MOE_VIEW_HID, MOE_VIEW_GU, MOE_VIEW_YPART, MOE_VIEW_DG, MOE_VIEW_HW,
     MOE_VIEW_DYPERM, MOE_VIEW_COUNT_
 };
-/* MXFP8 operand copies (precision MOE_MXFP8 only): for each operand a uint8 E4M3 value array in
+/* MXFP8 operand copies (MOE_MXFP8; MOE_FP8_BWD has only the backward's: X_C, DY_R, DY_C, DG_R, DG_C,
+ * HW_C, W13_C, W2_C, the others are 0 bytes): for each operand a uint8 E4M3 value array in
  * the source's layout, then its E8M0 scales (one byte per 32 values) in tensor-core atoms of 128
  * MN-rows x 4 K-blocks (512 bytes: MN-row m, K-block b at byte 16*(m%32) + 4*((m/32)%4) + b%4;
  * atom (m/128, b/4) at ((m/128) * (K/128) + b/4) * 512).  "_R" copies are blocked along the row

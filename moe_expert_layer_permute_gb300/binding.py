@@ -15,7 +15,7 @@ import torch
 from . import build as _build
 
 # ---- C structures ---------------------------------------------------------------------------
-MOE_BF16, MOE_MXFP8 = 0, 1
+MOE_BF16, MOE_MXFP8, MOE_FP8_BWD = 0, 1, 2
 MOE_DT_BF16, MOE_DT_F32, MOE_DT_I32 = 0, 1, 2
 MOE_FLAG_SAVE_GU, MOE_FLAG_REUSE_FWD, MOE_FLAG_REUSE_WEIGHTS = 0x1, 0x2, 0x4
 (MOE_VIEW_COUNTS, MOE_VIEW_OFFSETS, MOE_VIEW_PERM, MOE_VIEW_INV, MOE_VIEW_PAD_OFFSETS, MOE_VIEW_XPERM,
@@ -117,6 +117,15 @@ def moe_scratch_bytes(desc: MoeDesc) -> int:
     return int(LIB.moe_scratch_bytes(ctypes.byref(desc)))
 
 
+def view_span(desc: MoeDesc, which: int) -> tuple:
+    """(byte offset, byte count) of a named scratch region for `desc` (moe_scratch_view)."""
+    off, nbytes = ctypes.c_uint64(), ctypes.c_uint64()
+    rc = LIB.moe_scratch_view(ctypes.byref(desc), which, ctypes.byref(off), ctypes.byref(nbytes))
+    if rc:
+        raise MoeError(rc, "moe_scratch_view")
+    return off.value, nbytes.value
+
+
 class Scratch:
     """A caller-owned device scratch buffer (a torch uint8 tensor) and its C handle."""
 
@@ -136,11 +145,8 @@ class Scratch:
         return self.handle.desc
 
     def view(self, which: int, dtype: torch.dtype, shape) -> torch.Tensor:
-        off, nbytes = ctypes.c_uint64(), ctypes.c_uint64()
-        rc = LIB.moe_scratch_view(ctypes.byref(self.handle.desc), which, ctypes.byref(off), ctypes.byref(nbytes))
-        if rc:
-            raise MoeError(rc, "moe_scratch_view")
-        raw = self.buffer[off.value:off.value + nbytes.value]
+        off, nbytes = view_span(self.handle.desc, which)
+        raw = self.buffer[off:off + nbytes]
         return raw.view(dtype).view(*shape)
 
 

@@ -1122,9 +1122,11 @@ cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, b
     a.I = (int)L.I;
     a.out_f32 = out_f32 ? 1 : 0;
     a.save_gu = save_gu ? 1 : 0;
-    const int trace_id = (L.mx_on ? kTraceGemmMx : kTraceGemm) + (int)kind;
+    const bool fwd = kind == GemmKind::FwdGateUp || kind == GemmKind::FwdGateUpSaveOnly || kind == GemmKind::FwdDown;
+    const bool mx = fwd ? L.mx_fwd : L.mx_bwd;   // fp8_bwd: BF16 forward products, MXFP8 backward ones
+    const int trace_id = (mx ? kTraceGemmMx : kTraceGemm) + (int)kind;
     trace_begin(c.st, trace_id);
-    const cudaError_t err = L.mx_on ? launch_gemm_mx(c, kind, out, a) : launch_gemm_bf16(c, kind, W, out, a);
+    const cudaError_t err = mx ? launch_gemm_mx(c, kind, out, a) : launch_gemm_bf16(c, kind, W, out, a);
     trace_end(c.st, trace_id);
     return err;
 }

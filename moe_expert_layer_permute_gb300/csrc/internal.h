@@ -34,7 +34,7 @@ struct Layout {
     int64_t T, H, I, E, k, S, rows, nb_route, n_dtw;
     size_t ctrl, hist, cnt, off, pad_off, mtile, order, base, perm, inv, pos, row_slot;
     size_t xperm, hid, gu, ypart, dyperm, dg, hw, dtw;
-    bool mx_on;
+    bool mx_fwd, mx_bwd, mx_on;   // forward / backward GEMMs in MXFP8; either (MXFP8 regions exist)
     MxLayout mx;
     size_t total;
 };

@@ -31,8 +31,10 @@ bool make_layout(const moe_desc* d, Layout* L) {
     if (rows >= (int64_t)INT32_MAX / 2) return false;
     L->T = d->T; L->H = d->H; L->I = d->I; L->E = d->E; L->k = d->k; L->S = S; L->rows = rows;
     L->nb_route = (S + kRouteChunk - 1) / kRouteChunk;
-    L->mx_on = d->precision == MOE_MXFP8;
-    L->n_dtw = 2 * (d->I / (L->mx_on ? 128 : bwd_down_bn(d->I)));  // two column halves per n-tile
+    L->mx_fwd = d->precision == MOE_MXFP8;
+    L->mx_bwd = d->precision == MOE_MXFP8 || d->precision == MOE_FP8_BWD;
+    L->mx_on = L->mx_fwd || L->mx_bwd;
+    L->n_dtw = 2 * (d->I / (L->mx_bwd ? 128 : bwd_down_bn(d->I)));  // two column halves per n-tile
     const size_t A = 4096;
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, A); return at; };
@@ -61,17 +63,18 @@ bool make_layout(const moe_desc* d, Layout* L) {
         MxLayout& M = L->mx;
         const size_t H = d->H, I = d->I, E = d->E, R = rows;
         auto q = [&](size_t elems, size_t* data, size_t* sf) { *data = take(elems); *sf = take(elems / 32); };
-        q(R * H, &M.x_r, &M.x_r_sf);
+        const size_t F = L->mx_fwd ? 1 : 0;   // the forward-only copies are empty without an MXFP8 forward
+        q(F * R * H, &M.x_r, &M.x_r_sf);
         q(R * H, &M.x_c, &M.x_c_sf);
-        q(R * I, &M.h_r, &M.h_r_sf);
+        q(F * R * I, &M.h_r, &M.h_r_sf);
         q(R * H, &M.dy_r, &M.dy_r_sf);
         q(R * H, &M.dy_c, &M.dy_c_sf);
         q(R * 2 * I, &M.dg_r, &M.dg_r_sf);
         q(R * 2 * I, &M.dg_c, &M.dg_c_sf);
         q(R * I, &M.hw_c, &M.hw_c_sf);
-        q(E * 2 * I * H, &M.w13_r, &M.w13_r_sf);
+        q(F * E * 2 * I * H, &M.w13_r, &M.w13_r_sf);
         q(E * 2 * I * H, &M.w13_c, &M.w13_c_sf);
-        q(E * H * I, &M.w2_r, &M.w2_r_sf);
+        q(F * E * H * I, &M.w2_r, &M.w2_r_sf);
         q(E * H * I, &M.w2_c, &M.w2_c_sf);
     }
     L->total = o;
@@ -170,7 +173,7 @@ static int check_weight_grad(const moe_tensor* t, int ndim, int64_t a, int64_t b
 static int check_desc_scratch(moe_scratch* s, Layout* L) {
     if (!s) return MOE_ERR_NULL;
     const moe_desc* d = &s->desc;
-    if (d->precision != MOE_BF16 && d->precision != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+    if (d->precision != MOE_BF16 && d->precision != MOE_MXFP8 && d->precision != MOE_FP8_BWD) return MOE_ERR_UNSUPPORTED;
     if (!make_layout(d, L)) return MOE_ERR_SHAPE;
     if (!s->data) return MOE_ERR_SCRATCH;
     if (reinterpret_cast<uintptr_t>(s->data) % 256 != 0) return MOE_ERR_SCRATCH;
@@ -200,9 +203,10 @@ static uint64_t weights_tag(const moe_desc* d, const void* w13, const void* w2) 
     return h | 1ull;
 }
 
-// MXFP8 copies of the weights: W13 blocked along H (gate/up row blocks) and along 2I, W2 blocked
-// along I and along H.  Skipped when the caller states the weights are unchanged since the call
-// that made these copies on this scratch (MOE_FLAG_REUSE_WEIGHTS).
+// MXFP8 copies of the weights: for an MXFP8 forward W13 blocked along H (gate/up row blocks) and
+// W2 along I; for an MXFP8 backward W13 blocked along 2I and W2 along H.  Skipped when the caller
+// states the weights are unchanged since the call that made these copies on this scratch
+// (MOE_FLAG_REUSE_WEIGHTS).
 static int mx_weights(const Ctx& c, moe_scratch* s, const void* W13, const void* W2) {
     const Layout& L = *c.L;
     const MxLayout& M = L.mx;
@@ -210,10 +214,11 @@ static int mx_weights(const Ctx& c, moe_scratch* s, const void* W13, const void*
     const uint64_t tag = weights_tag(d, W13, W2);
     if (d->flags & MOE_FLAG_REUSE_WEIGHTS) return s->state[1] == tag ? MOE_OK : MOE_ERR_STATE;
     char* b = c.base;
-    if (launch_mx_quant(c, W13, L.E * 2 * L.I, (int)L.H, nullptr, b + M.w13_r, b + M.w13_r_sf, b + M.w13_c,
+    auto fw = [&](size_t off) { return L.mx_fwd ? b + off : nullptr; };
+    if (launch_mx_quant(c, W13, L.E * 2 * L.I, (int)L.H, nullptr, fw(M.w13_r), fw(M.w13_r_sf), b + M.w13_c,
                         b + M.w13_c_sf, (int)L.I) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (launch_mx_quant(c, W2, L.E * L.H, (int)L.I, nullptr, b + M.w2_r, b + M.w2_r_sf, b + M.w2_c, b + M.w2_c_sf,
+    if (launch_mx_quant(c, W2, L.E * L.H, (int)L.I, nullptr, fw(M.w2_r), fw(M.w2_r_sf), b + M.w2_c, b + M.w2_c_sf,
                         0) != cudaSuccess)
         return MOE_ERR_CUDA;
     s->state[1] = tag;
@@ -273,7 +278,7 @@ int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* t
     char* base = reinterpret_cast<char*>(scratch->data);
     Ctx c{st, base, &L, reinterpret_cast<int*>(base + L.ctrl), nsm, reinterpret_cast<const float*>(topk_w->data)};
     MOE_TRY_CUDA(launch_routing(c, reinterpret_cast<const int32_t*>(topk_idx->data)));
-    if (L.mx_on) {
+    if (L.mx_fwd) {
         // dispatch and quantise in one pass; a forward that saves for the backward also makes the
         // token-blocked copy the weight gradient of W13 reads
         const MxLayout& M = L.mx;
@@ -330,15 +335,21 @@ int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_id
     if (L.mx_on && (rc = mx_weights(c, scratch, W13->data, W2->data))) return rc;
     if (!reuse) {
         MOE_TRY_CUDA(launch_routing(c, reinterpret_cast<const int32_t*>(topk_idx->data)));
-        if (L.mx_on)
+        if (L.mx_fwd)
             MOE_TRY_CUDA(mx_rows(c, x->data, true, (int)H, M.x_r, M.x_r_sf, M.x_c, M.x_c_sf));
+        else if (L.mx_bwd)
+            MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, nullptr, nullptr));
         else
             MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, dy->data, base + L.dyperm));
         MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUpSaveOnly, W13->data, nullptr, false, true));
-    } else if (!L.mx_on) {
+    } else if (!L.mx_bwd) {
         MOE_TRY_CUDA(launch_gather(c, dy->data, base + L.dyperm, nullptr, nullptr));
     }
-    if (L.mx_on) MOE_TRY_CUDA(mx_rows(c, dy->data, true, (int)H, M.dy_r, M.dy_r_sf, M.dy_c, M.dy_c_sf));
+    if (L.mx_bwd) {
+        // a BF16 forward (fp8_bwd) made no MXFP8 copy of x: the W13 weight gradient's comes here
+        if (!L.mx_fwd) MOE_TRY_CUDA(mx_rows(c, x->data, true, (int)H, 0, 0, M.x_c, M.x_c_sf));
+        MOE_TRY_CUDA(mx_rows(c, dy->data, true, (int)H, M.dy_r, M.dy_r_sf, M.dy_c, M.dy_c_sf));
+    }
     // MXFP8: the SwiGLU-backward epilogue emits the E4M3 copies of [dg|du] and w h directly
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::BwdDown, W2->data, nullptr, false, false));
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::BwdGateUp, W13->data, nullptr, false, false));
@@ -399,8 +410,9 @@ int moe_scratch_view(const moe_desc* desc, int view, uint64_t* offset, uint64_t*
             if (!L.mx_on || view < MOE_VIEW_MX_X_R || view >= MOE_VIEW_MX_END_) return MOE_ERR_SHAPE;
             // MxLayout lists the regions in view order: value array then scales, per operand
             const int i = view - MOE_VIEW_MX_X_R;
-            const uint64_t elems[12] = {R * H, R * H, R * I, R * H, R * H, R * 2 * I,
-                                        R * 2 * I, R * I, E * 2 * I * H, E * 2 * I * H, E * H * I, E * H * I};
+            const uint64_t F = L.mx_fwd ? 1 : 0;   // x_r, h_r, w13_r, w2_r: MXFP8 forward only
+            const uint64_t elems[12] = {F * R * H, R * H,     F * R * I,     R * H,         R * H,     R * 2 * I,
+                                        R * 2 * I, R * I, F * E * 2 * I * H, E * 2 * I * H, F * E * H * I, E * H * I};
             *offset = reinterpret_cast<const size_t*>(&L.mx)[i];
             *bytes = (i % 2 == 0) ? elems[i / 2] : elems[i / 2] / 32;
         }

@@ -41,7 +41,7 @@ class DeviceLayer:
         self.dW13 = torch.full((E, 2 * I, H), float("nan"), dtype=wgrad_dtype, device=dev)
         self.dW2 = torch.full((E, H, I), float("nan"), dtype=wgrad_dtype, device=dev)
         self.dtw = torch.full((T, k), float("nan"), dtype=torch.float32, device=dev)
-        prec = bd.MOE_MXFP8 if cfg.precision == "mxfp8" else bd.MOE_BF16
+        prec = {"bf16": bd.MOE_BF16, "mxfp8": bd.MOE_MXFP8, "fp8_bwd": bd.MOE_FP8_BWD}[cfg.precision]
         self.scratch = bd.Scratch(T, H, I, E, k, precision=prec, device=dev)
 
     def fwd(self, flags=0):

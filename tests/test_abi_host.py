@@ -167,3 +167,16 @@ def test_strerror_and_trace_api(bd):
     assert "unknown" in bd.strerror(-1234)
     bd.moe_trace_reset()
     assert bd.moe_trace_read() == {}
+
+
+def test_fp8_bwd_layout_has_only_the_backward_mxfp8_copies(bd):
+    """fp8_bwd (BF16 forward, MXFP8 backward): the forward-only E4M3 copies take no scratch."""
+    d = bd.make_desc(2048, 512, 256, 16, 4, bd.MOE_FP8_BWD)
+    m = bd.make_desc(2048, 512, 256, 16, 4, bd.MOE_MXFP8)
+    b = bd.make_desc(2048, 512, 256, 16, 4, bd.MOE_BF16)
+    for name in ("x_r", "x_r_sf", "h_r", "h_r_sf", "w13_r", "w13_r_sf", "w2_r", "w2_r_sf"):
+        assert bd.view_span(d, bd.MX_VIEWS[name])[1] == 0, name
+        assert bd.view_span(m, bd.MX_VIEWS[name])[1] > 0, name
+    for name in ("x_c", "dy_r", "dy_c", "dg_r", "dg_c", "hw_c", "w13_c", "w2_c"):
+        assert bd.view_span(d, bd.MX_VIEWS[name])[1] == bd.view_span(m, bd.MX_VIEWS[name])[1] > 0, name
+    assert bd.moe_scratch_bytes(b) < bd.moe_scratch_bytes(d) < bd.moe_scratch_bytes(m)
