@@ -137,6 +137,12 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------ ours
+# DRAM bytes (read + write) per launch from one ncu capture of the current build, scaled to the
+# named workload: profiles/gemm_fwd_gate_up_bf16_profile_30b_e32.md (profile_30b_e32, the forward
+# that saves [g|u]: 343.6 MB read + 124.6 MB written; every size scales with E at equal per-expert
+# work, so x4 for the 128-expert layer).  Kernels not captured since their last change are absent.
+PROFILED_TRAFFIC = {("qwen3_30b_a3b", "gemm_fwd_gate_up_swiglu"): 4 * (343.563e6 + 124.586e6)}
+
 GEMM_FLOPS = {  # algorithmic FLOPs per launch of each grouped GEMM (BF16 or MXFP8), in units of S*H*I
     "gemm_fwd_gate_up_swiglu": 4, "gemm_fwd_gate_up_save": 4, "gemm_fwd_down_weighted": 2,
     "gemm_bwd_down_swiglu_bwd": 2, "gemm_bwd_gate_up": 4, "gemm_wgrad_down": 2, "gemm_wgrad_gate_up": 4,
@@ -292,8 +298,12 @@ def summarize(m, peak, peak_src):
     roof = None
     if top:
         ach = GEMM_FLOPS[top.replace("gemm_mx_", "gemm_")] * shf / (gemms[top]["avg_ms"] * 1e-3) / 1e12
+        traffic = PROFILED_TRAFFIC.get((cfg.name, top))
         roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
-                "traffic": None, "kernel": top, "peak_source": peak_src}
+                "traffic": traffic, "kernel": top, "peak_source": peak_src}
+        if traffic is not None:
+            roof["traffic_source"] = ("dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture on "
+                                      "profile_30b_e32, x4 to the 128-expert layer (bytes per launch)")
     full_tf = 4 * fwd_fl / (m["full_ms"] * 1e-3) / 1e12
     return {"fwd_ms": m["fwd_ms"], "bwd_ms": m["bwd_ms"], "full_ms": m["full_ms"],
             "fwd_tflops": fwd_fl / (m["fwd_ms"] * 1e-3) / 1e12,
