@@ -27,7 +27,7 @@ import dataclasses
 import numpy as np
 
 # stream ids of the per-tensor generators
-_S_ROUTE, _S_LOGIT, _S_X, _S_W13, _S_W2, _S_DY, _S_PERM = range(7)
+_S_ROUTE, _S_LOGIT, _S_X, _S_W13, _S_W2, _S_DY, _S_PERM, _S_RLOGIT, _S_DTW = range(9)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -170,6 +170,19 @@ def make_inputs(cfg: LayerConfig | str, *, with_weights: bool = True, with_dy: b
     W2 = _normal_bf16(_rng(cfg.seed, _S_W2), (E, H, I), 1.0 / np.sqrt(I)) if with_weights else None
     dy = _normal_bf16(_rng(cfg.seed, _S_DY), (T, H), 1.0) if with_dy else None
     return LayerInputs(cfg, x, idx, w, W13, W2, dy)
+
+
+def router_inputs(cfg: LayerConfig | str, *, tie_step: float = 0.0) -> tuple[np.ndarray, np.ndarray]:
+    """(router logits float32 [T, E] ~ N(0, 1), upstream gradient of the top-k weights float32
+    [T, k] ~ N(0, 1)) for the router that precedes the layer.  tie_step > 0 rounds the logits to
+    multiples of it, so that tokens carry equal logits (ties)."""
+    if isinstance(cfg, str):
+        cfg = CONFIGS[cfg]
+    logits = _rng(cfg.seed, _S_RLOGIT).standard_normal((cfg.T, cfg.E), dtype=np.float32)
+    if tie_step > 0:
+        logits = (np.round(logits / np.float32(tie_step)) * np.float32(tie_step)).astype(np.float32)
+    dtw = _rng(cfg.seed, _S_DTW).standard_normal((cfg.T, cfg.k), dtype=np.float32)
+    return np.ascontiguousarray(logits), np.ascontiguousarray(dtw)
 
 
 def custom_config(name="custom", **kw) -> LayerConfig:

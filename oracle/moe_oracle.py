@@ -39,6 +39,7 @@ __all__ = [
     "route", "permute_rows", "unpermute_sum", "sigmoid", "silu",
     "e4m3_round", "mx_block_exponent", "mx_qdq", "mx_qdq_segments",
     "forward", "backward", "forward_tokens", "backward_tokens", "wgrad_experts",
+    "router_forward", "router_backward",
 ]
 
 
@@ -369,3 +370,33 @@ def wgrad_experts(dy, x, topk_idx, topk_w, W13, W2, experts, *, mxfp8: bool = Fa
             dG, X = mx_qdq_segments(dG, seg), mx_qdq_segments(X, seg)
         res.append((dG.T @ X, dY.T @ Hw))
     return res
+
+
+# ----------------------------------------------------------------------------------------------
+# router: the step before the layer (the pages' layer benchmark leaves it out: ic.work analysis,
+# section "跑分背后的理想假设与闭源软肋"); each token's routing weights aggregate the expert
+# outputs (kongchang.com, "为什么 MoE 训练特别需要融合内核").  Readings where the pages are silent:
+# the k largest logits are selected, ties to the lower expert index, listed in descending order;
+# the weights are the softmax over the selected logits (the full softmax renormalised over the
+# top-k); the selection is piecewise constant, so the backward reaches only the selected logits.
+# ----------------------------------------------------------------------------------------------
+def router_forward(logits, k: int):
+    """(topk_idx int32 [T, k], topk_w fp64 [T, k]) of router logits [T, E]."""
+    L = _as64(logits)
+    T, E = L.shape
+    cols = np.broadcast_to(np.arange(E), L.shape)
+    order = np.lexsort((cols, -L), axis=1)          # by logit descending, then index ascending
+    idx = order[:, :k]
+    sel = np.take_along_axis(L, idx, axis=1)
+    z = np.exp(sel - sel[:, :1])                    # the first selected logit is the largest
+    return idx.astype(np.int32), z / z.sum(axis=1, keepdims=True)
+
+
+def router_backward(topk_idx, topk_w, dtopk_w, E: int):
+    """dlogits [T, E] of sum_j dtopk_w[t, j] * topk_w[t, j]: through the softmax over the selected
+    logits, dl_j = w_j (dw_j - sum_i w_i dw_i); zero for experts a token did not select."""
+    w, dw = _as64(topk_w), _as64(dtopk_w)
+    g = w * (dw - (w * dw).sum(axis=1, keepdims=True))
+    dl = np.zeros((w.shape[0], E))
+    np.put_along_axis(dl, np.asarray(topk_idx, dtype=np.int64), g, axis=1)
+    return dl

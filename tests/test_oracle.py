@@ -402,3 +402,64 @@ def test_fp8_bwd_error_is_at_quantisation_scale_and_differs_from_mxfp8():
     for k_ in ("dx", "dW13", "dW2", "dtopk_w"):
         assert 1e-3 < _rel(got[k_], ref[k_]) < 8e-2, k_
         assert _rel(got[k_], mx[k_]) > 1e-4, k_       # the forward differs (exact vs quantised)
+
+
+# ---------------------------------------------------------------- router (the step before the layer)
+def test_router_selects_the_largest_logits_ties_to_lower_index():
+    rng = np.random.default_rng(31)
+    L = np.round(rng.standard_normal((200, 24)) * 2) / 2          # many ties
+    idx, w = oracle.router_forward(L.astype(np.float32), 5)
+    for t in range(200):
+        sel = list(idx[t])
+        assert len(set(sel)) == 5
+        rest = [e for e in range(24) if e not in sel]
+        assert L[t, sel].min() >= L[t, rest].max()
+        assert all(L[t, sel[j]] >= L[t, sel[j + 1]] for j in range(4))   # descending
+        for j in range(4):                                              # equal logits: lower index first
+            if L[t, sel[j]] == L[t, sel[j + 1]]:
+                assert sel[j] < sel[j + 1]
+        # a tie across the cut keeps the lower indices
+        cut = L[t, sel[-1]]
+        tied = [e for e in range(24) if L[t, e] == cut]
+        kept = [e for e in sel if L[t, e] == cut]
+        assert kept == tied[:len(kept)]
+
+
+def test_router_weights_are_the_softmax_of_the_selected_logits():
+    from scipy.special import softmax
+    rng = np.random.default_rng(32)
+    L = rng.standard_normal((50, 16)).astype(np.float32)
+    idx, w = oracle.router_forward(L, 16)                         # k = E: the full softmax
+    full = softmax(L.astype(np.float64), axis=1)
+    np.testing.assert_allclose(w, np.take_along_axis(full, idx.astype(np.int64), 1), rtol=1e-13)
+    idx, w = oracle.router_forward(L, 4)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=1e-14)
+    sel = np.take_along_axis(L.astype(np.float64), idx.astype(np.int64), 1)
+    np.testing.assert_allclose(w[:, 1:] / w[:, :1], np.exp(sel[:, 1:] - sel[:, :1]), rtol=1e-12)
+
+
+def test_router_backward_matches_finite_differences_and_autograd():
+    import torch
+    rng = np.random.default_rng(33)
+    T, E, k = 6, 12, 3
+    # well-separated logits: a step of 1e-6 never changes the selection
+    L = np.stack([rng.permutation(E) * 0.5 + rng.uniform(-0.1, 0.1) for _ in range(T)])
+    dw = rng.standard_normal((T, k))
+    idx, w = oracle.router_forward(L, k)
+    dl = oracle.router_backward(idx, w, dw, E)
+
+    def loss(LL):
+        i2, w2 = oracle.router_forward(LL, k)
+        assert np.array_equal(i2, idx)
+        return float((w2 * dw).sum())
+    h = 1e-6
+    for t in range(T):
+        for e in range(E):
+            P, M = L.copy(), L.copy()
+            P[t, e] += h
+            M[t, e] -= h
+            assert abs((loss(P) - loss(M)) / (2 * h) - dl[t, e]) < 1e-8
+    lt = torch.tensor(L, requires_grad=True)
+    sel = torch.gather(lt, 1, torch.tensor(idx, dtype=torch.int64))
+    (torch.softmax(sel, 1) * torch.tensor(dw)).sum().backward()
+    np.testing.assert_allclose(dl, lt.grad.numpy(), rtol=1e-12, atol=1e-14)
