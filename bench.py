@@ -285,6 +285,58 @@ def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
     return out
 
 
+def router_measure(bd, gen, cfg, reps, hbm_peak):
+    """The router before the layer (top-k + softmax over the selected, and its backward) on the
+    workload's T x E logits.  One timed iteration is a CUDA graph of NB launches over NB distinct
+    buffers (together larger than L2, so no flush is needed and no host launch cost is timed);
+    per-launch time = iteration time / NB.  Algorithmic bytes: forward T*E*4 read + T*k*8
+    written, backward T*k*12 read + T*E*4 written."""
+    import torch
+    logits, dtw = gen.router_inputs(cfg)
+    T, E, k = cfg.T, cfg.E, cfg.k
+    NB = max(2, -(-(256 << 20) // (T * E * 4)))        # >= 256 MiB of logits (and of dlogits)
+    lg = [torch.from_numpy(logits).cuda() for _ in range(NB)]
+    dw = torch.from_numpy(dtw).cuda()
+    idx = [torch.empty(T, k, dtype=torch.int32, device="cuda") for _ in range(NB)]
+    w = [torch.empty(T, k, dtype=torch.float32, device="cuda") for _ in range(NB)]
+    dl = [torch.empty(T, E, dtype=torch.float32, device="cuda") for _ in range(NB)]
+    side = torch.cuda.Stream()
+
+    def graph(fn):
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                fn(side)
+            side.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                fn(side)
+        return g
+
+    g_f = graph(lambda st: [bd.moe_router_fwd(lg[i], idx[i], w[i], stream=st) for i in range(NB)])
+    g_b = graph(lambda st: [bd.moe_router_bwd(idx[i], w[i], dw, dl[i], stream=st) for i in range(NB)])
+    stream = torch.cuda.current_stream()
+
+    def time_graph(g):
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * NB)
+    f_ms, b_ms = time_graph(g_f), time_graph(g_b)
+    fb, bb = T * E * 4 + T * k * 8, T * k * 12 + T * E * 4
+    return {"workload": f"T={T} E={E} k={k} fp32 logits ~ N(0,1)", "fwd_us": f_ms * 1e3, "bwd_us": b_ms * 1e3,
+            "fwd_gbs": fb / (f_ms * 1e-3) / 1e9, "bwd_gbs": bb / (b_ms * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "peak": hbm_peak, "unit": "GB/s",
+                         "fwd_frac": fb / (f_ms * 1e-3) / 1e9 / hbm_peak, "bwd_frac": bb / (b_ms * 1e-3) / 1e9 / hbm_peak},
+            "timing": f"CUDA graph of {NB} launches on {NB} distinct buffers (> L2), {reps} replays, per launch",
+            "gpu_launches": 2 * NB * reps}
+
+
 def summarize(m, peak, peak_src):
     """Per-kernel table, dominant-GEMM roofline and layer throughput of one measurement."""
     cfg, kern = m["cfg"], m["kern"]
@@ -373,6 +425,8 @@ def run_ours(args, rank, ws, local):
         fs["workload"] = fcfg.name
         fs["peak_tflops"] = {"value": blend_peak, "source": fsrc}
         line["fp8_bwd"] = fs
+    # the router that precedes the layer (outside the layer step, as in the pages' benchmark)
+    line["router"] = router_measure(bd, gen, cfg, 20, peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, budget_s=20.0)
     elif rank == 0:

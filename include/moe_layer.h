@@ -138,6 +138,28 @@ int moe_read_device_status(moe_scratch* scratch, void* stream, int* status);
 /* Static message for a MOE_ERR_* code. */
 const char* moe_strerror(int code);
 
+/* ---- the router that precedes the layer ----------------------------------------------------- */
+/* The pages' single-layer benchmark leaves the router out (ic.work analysis, section
+ * "跑分背后的理想假设与闭源软肋"); its outputs are the layer's topk_idx and topk_w, the routing
+ * weights that aggregate each token's expert outputs (kongchang.com, "Prime Intellect推出Prime Mega
+ * MoE", section "为什么 MoE 训练特别需要融合内核").  Where the pages are silent: the k largest
+ * logits of each token are selected (ties to the lower expert index), listed in descending
+ * order, and weighted by the softmax over the selected logits.
+ *
+ * moe_router_fwd: logits fp32 [T, E] -> topk_idx int32 [T, k], topk_w fp32 [T, k] (overwritten).
+ * moe_router_bwd: dlogits fp32 [T, E] (overwritten) of sum_j dtopk_w[t,j] * topk_w[t,j]:
+ *   dlogits[t, topk_idx[t,j]] = w_j (dw_j - sum_i w_i dw_i), zero for experts a token did not
+ *   select; topk_idx and topk_w as moe_router_fwd wrote them (distinct experts per token).
+ * All tensors are row-contiguous device buffers, 16-byte aligned, owned by the caller; T and E are
+ * the logits' / dlogits' shape and k the second dimension of topk_idx.  1 <= k <= 32,
+ * k <= E <= 1024, T >= 0 (T = 0 launches nothing).  Returns MOE_ERR_* before any launch on bad
+ * arguments, MOE_ERR_UNSUPPORTED for k or E outside those bounds, MOE_ERR_CUDA on a launch error.
+ * Asynchronous on `stream`.  Logits must be finite: NaN logits give unspecified experts (always
+ * in [0, E)) and NaN weights; expert ids outside [0, E) given to moe_router_bwd are skipped. */
+int moe_router_fwd(const moe_tensor* logits, moe_tensor* topk_idx, moe_tensor* topk_w, void* stream);
+int moe_router_bwd(const moe_tensor* topk_idx, const moe_tensor* topk_w, const moe_tensor* dtopk_w,
+                   moe_tensor* dlogits, void* stream);
+
 /* ---- routing without caller-provided scratch ---------------------------------------------- */
 /* The pages have no counterpart to this entry point; it exists for callers that cannot allocate
  * device memory or hand over a scratch buffer (code running inside an allocator's hooks, runtimes

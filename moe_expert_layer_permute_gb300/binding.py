@@ -32,7 +32,8 @@ ERR = {v: k for k, v in ERRORS.items()}
 
 # every symbol the header declares
 EXPORTS = ("moe_scratch_bytes", "moe_fwd", "moe_bwd", "moe_read_device_status", "moe_strerror",
-           "moe_scratch_view", "moe_trace_enable", "moe_trace_reset", "moe_trace_read", "moe_route_static")
+           "moe_scratch_view", "moe_trace_enable", "moe_trace_reset", "moe_trace_read", "moe_route_static",
+           "moe_router_fwd", "moe_router_bwd")
 
 
 class MoeTensor(ctypes.Structure):
@@ -79,6 +80,10 @@ def _load() -> ctypes.CDLL:
     lib.moe_route_static.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + \
         [ctypes.c_void_p] * 5
     lib.moe_route_static.restype = ctypes.c_int
+    lib.moe_router_fwd.argtypes = [_P(MoeTensor)] * 3 + [ctypes.c_void_p]
+    lib.moe_router_fwd.restype = ctypes.c_int
+    lib.moe_router_bwd.argtypes = [_P(MoeTensor)] * 4 + [ctypes.c_void_p]
+    lib.moe_router_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -213,3 +218,19 @@ def moe_route_static(topk_idx, E: int, counts, offsets, perm, inv, stream=None) 
                               perm.data_ptr(), inv.data_ptr(), _stream_ptr(stream))
     if rc:
         raise MoeError(rc, "moe_route_static")
+
+
+def moe_router_fwd(logits, topk_idx, topk_w, stream=None) -> None:
+    """Top-k router: logits fp32 [T, E] -> topk_idx int32 [T, k], topk_w fp32 [T, k]."""
+    args = [as_moe_tensor(t) for t in (logits, topk_idx, topk_w)]
+    rc = LIB.moe_router_fwd(*[ctypes.byref(a) for a in args], _stream_ptr(stream))
+    if rc:
+        raise MoeError(rc, "moe_router_fwd")
+
+
+def moe_router_bwd(topk_idx, topk_w, dtopk_w, dlogits, stream=None) -> None:
+    """Router backward: dlogits fp32 [T, E] from the weights' gradient dtopk_w fp32 [T, k]."""
+    args = [as_moe_tensor(t) for t in (topk_idx, topk_w, dtopk_w, dlogits)]
+    rc = LIB.moe_router_bwd(*[ctypes.byref(a) for a in args], _stream_ptr(stream))
+    if rc:
+        raise MoeError(rc, "moe_router_bwd")

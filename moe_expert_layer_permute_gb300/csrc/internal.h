@@ -58,6 +58,12 @@ cudaError_t launch_gather(const Ctx& c, const void* src0, void* dst0, const void
 // out[t] = sum_j part[pos[t*k+j]] (fixed j order); optionally dtopk_w[s] = sum_n dtw[pos[s], n]
 cudaError_t launch_combine(const Ctx& c, const void* part, void* out, float* dtopk_w);
 
+// router (the step before the layer): top-k of fp32 logits with the softmax over the selected,
+// and its backward; T = 0 launches nothing
+cudaError_t launch_router_fwd(cudaStream_t st, const float* logits, int T, int E, int k, int* topk_idx, float* topk_w);
+cudaError_t launch_router_bwd(cudaStream_t st, const int* topk_idx, const float* topk_w, const float* dtopk_w, int T,
+                              int E, int k, float* dlogits);
+
 // grouped GEMMs (persistent, TMA + tcgen05)
 enum class GemmKind : int {
     FwdGateUp = 0,     // [g|u] = X_perm W13[e]^T, epilogue h = silu(g) u  (optionally saves [g|u])

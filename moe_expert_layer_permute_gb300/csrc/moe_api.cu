@@ -371,6 +371,46 @@ int moe_read_device_status(moe_scratch* scratch, void* stream, int* status) {
     return MOE_OK;
 }
 
+static int router_shape(const moe_tensor* logits_like, const moe_tensor* idx, int64_t* T, int64_t* E, int64_t* k) {
+    if (!logits_like || !idx) return MOE_ERR_NULL;
+    if (logits_like->ndim != 2 || idx->ndim != 2) return MOE_ERR_SHAPE;
+    *T = logits_like->shape[0];
+    *E = logits_like->shape[1];
+    *k = idx->shape[1];
+    if (*T < 0 || *T >= (int64_t)INT32_MAX / 32 || idx->shape[0] != *T) return MOE_ERR_SHAPE;
+    if (*k < 1 || *k > 32 || *E < *k || *E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int moe_router_fwd(const moe_tensor* logits, moe_tensor* topk_idx, moe_tensor* topk_w, void* stream) {
+    int64_t T, E, k;
+    int rc = router_shape(logits, topk_idx, &T, &E, &k);
+    if (rc) return rc;
+    if ((rc = check_tensor(logits, MOE_DT_F32, 2, T, E, 0))) return rc;
+    if ((rc = check_tensor(topk_idx, MOE_DT_I32, 2, T, k, 0))) return rc;
+    if ((rc = check_tensor(topk_w, MOE_DT_F32, 2, T, k, 0))) return rc;
+    MOE_TRY_CUDA(launch_router_fwd(reinterpret_cast<cudaStream_t>(stream), reinterpret_cast<const float*>(logits->data),
+                                   (int)T, (int)E, (int)k, reinterpret_cast<int*>(topk_idx->data),
+                                   reinterpret_cast<float*>(topk_w->data)));
+    return MOE_OK;
+}
+
+int moe_router_bwd(const moe_tensor* topk_idx, const moe_tensor* topk_w, const moe_tensor* dtopk_w, moe_tensor* dlogits,
+                   void* stream) {
+    int64_t T, E, k;
+    int rc = router_shape(dlogits, topk_idx, &T, &E, &k);
+    if (rc) return rc;
+    if ((rc = check_tensor(topk_idx, MOE_DT_I32, 2, T, k, 0))) return rc;
+    if ((rc = check_tensor(topk_w, MOE_DT_F32, 2, T, k, 0))) return rc;
+    if ((rc = check_tensor(dtopk_w, MOE_DT_F32, 2, T, k, 0))) return rc;
+    if ((rc = check_tensor(dlogits, MOE_DT_F32, 2, T, E, 0))) return rc;
+    MOE_TRY_CUDA(launch_router_bwd(reinterpret_cast<cudaStream_t>(stream), reinterpret_cast<const int*>(topk_idx->data),
+                                   reinterpret_cast<const float*>(topk_w->data),
+                                   reinterpret_cast<const float*>(dtopk_w->data), (int)T, (int)E, (int)k,
+                                   reinterpret_cast<float*>(dlogits->data)));
+    return MOE_OK;
+}
+
 const char* moe_strerror(int code) {
     switch (code) {
         case MOE_OK: return "ok";

@@ -180,3 +180,30 @@ def test_fp8_bwd_layout_has_only_the_backward_mxfp8_copies(bd):
     for name in ("x_c", "dy_r", "dy_c", "dg_r", "dg_c", "hw_c", "w13_c", "w2_c"):
         assert bd.view_span(d, bd.MX_VIEWS[name])[1] == bd.view_span(m, bd.MX_VIEWS[name])[1] > 0, name
     assert bd.moe_scratch_bytes(b) < bd.moe_scratch_bytes(d) < bd.moe_scratch_bytes(m)
+
+
+def test_router_argument_checks(bd):
+    """Every bad argument of the router entry points is refused before any launch (no GPU)."""
+    f = _Fake(bd)
+    F32, I32, B16 = bd.MOE_DT_F32, bd.MOE_DT_I32, bd.MOE_DT_BF16
+    E = bd.ERR
+
+    def fwd(lg, idx, w):
+        return bd.LIB.moe_router_fwd(ctypes.byref(lg), ctypes.byref(idx), ctypes.byref(w), None)
+
+    def bwd(idx, w, dw, dl):
+        return bd.LIB.moe_router_bwd(ctypes.byref(idx), ctypes.byref(w), ctypes.byref(dw), ctypes.byref(dl), None)
+    assert fwd(f.t((64, 128), F32), f.t((64, 33), I32), f.t((64, 33), F32)) == E["MOE_ERR_UNSUPPORTED"]   # k > 32
+    assert fwd(f.t((64, 4), F32), f.t((64, 8), I32), f.t((64, 8), F32)) == E["MOE_ERR_UNSUPPORTED"]       # k > E
+    assert fwd(f.t((64, 2048), F32), f.t((64, 8), I32), f.t((64, 8), F32)) == E["MOE_ERR_UNSUPPORTED"]    # E > 1024
+    assert fwd(f.t((64, 128), F32), f.t((32, 8), I32), f.t((64, 8), F32)) == E["MOE_ERR_SHAPE"]
+    assert fwd(f.t((64, 128), F32), f.t((64, 8), I32), f.t((64, 4), F32)) == E["MOE_ERR_SHAPE"]
+    assert fwd(f.t((64, 128), B16), f.t((64, 8), I32), f.t((64, 8), F32)) == E["MOE_ERR_DTYPE"]
+    assert fwd(f.t((64, 128), F32), f.t((64, 8), F32), f.t((64, 8), F32)) == E["MOE_ERR_DTYPE"]
+    assert fwd(f.t((64, 128), F32, contiguous=False), f.t((64, 8), I32), f.t((64, 8), F32)) == E["MOE_ERR_LAYOUT"]
+    assert fwd(f.t((64, 128), F32, misalign=4), f.t((64, 8), I32), f.t((64, 8), F32)) == E["MOE_ERR_ALIGN"]
+    assert bd.LIB.moe_router_fwd(None, None, None, None) == E["MOE_ERR_NULL"]
+    assert bwd(f.t((64, 8), I32), f.t((64, 8), F32), f.t((64, 8), F32), f.t((64, 100), B16)) == E["MOE_ERR_DTYPE"]
+    assert bwd(f.t((64, 8), I32), f.t((64, 8), F32), f.t((64, 7), F32), f.t((64, 100), F32)) == E["MOE_ERR_SHAPE"]
+    assert bwd(f.t((64, 8), I32), f.t((64, 8), F32), f.t((64, 8), F32), f.t((63, 100), F32)) == E["MOE_ERR_SHAPE"]
+    assert bd.LIB.moe_router_bwd(None, None, None, None, None) == E["MOE_ERR_NULL"]
