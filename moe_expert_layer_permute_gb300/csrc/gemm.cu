@@ -55,12 +55,14 @@ template <int EPI, bool MX, int BN>
 constexpr bool tma_out() {
     return (!(MX && BN == 256) && epi_warps<EPI, MX && BN == 256>() == 4 &&
             (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WGRAD)) ||
-           (!MX && EPI == EPI_SWIGLU_BWD);
+           (!MX && EPI == EPI_SWIGLU_BWD) ||
+           (MX && BN == 256 && (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY));
 }
 // bytes of one warp's staging box: 32 rows x 128 bytes, or 32 x 64 (64-byte swizzle) for the
-// eight warps of the SwiGLU backward, whose 4 KB boxes would not fit beside the ring
-template <int EPI>
-constexpr int out_box_bytes() { return EPI == EPI_SWIGLU_BWD ? 2048 : 4096; }
+// eight-warp epilogues (the SwiGLU backward, the drained MXFP8 128 x 256 tiles), whose 4 KB
+// boxes would not fit beside the ring
+template <int EPI, bool SINGLE>
+constexpr int out_box_bytes() { return (EPI == EPI_SWIGLU_BWD || SINGLE) ? 2048 : 4096; }
 
 // ---- staged TMA stores: one 32-row x 128-byte box per epilogue warp, row = lane ----------------
 // waits until the warp's previous box has been read out by its TMA store
@@ -90,14 +92,15 @@ __device__ __forceinline__ void box_put_f32x32(uint32_t sbox, int lane, const fl
                 make_uint4(__float_as_uint(v[4 * cc]), __float_as_uint(v[4 * cc + 1]), __float_as_uint(v[4 * cc + 2]),
                            __float_as_uint(v[4 * cc + 3])));
 }
-// 32 values as bf16 into a 32-row x 64-byte box (64-byte swizzle; the box is 512-byte aligned)
-__device__ __forceinline__ void box64_put_bf16x32(uint32_t sbox, int lane, const float* v) {
+// 32 values (times scale) as bf16 into a 32-row x 64-byte box (64-byte swizzle; the box is
+// 512-byte aligned)
+__device__ __forceinline__ void box64_put_bf16x32(uint32_t sbox, int lane, const float* v, float scale = 1.f) {
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
         const float* f = v + 8 * cc;
         st_shared_v4(sbox + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4),
-                     make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                                pack_bf16x2(f[6], f[7])));
+                     make_uint4(pack_bf16x2(scale * f[0], scale * f[1]), pack_bf16x2(scale * f[2], scale * f[3]),
+                                pack_bf16x2(scale * f[4], scale * f[5]), pack_bf16x2(scale * f[6], scale * f[7])));
     }
 }
 // hands the staged box to the async proxy and stores it at {c0 (column), c1 (row)}
@@ -108,6 +111,13 @@ __device__ __forceinline__ void box_store(const CUtensorMap* m, uint8_t* box, in
         tma_store_2d(m, box, c0, c1);
         bulk_commit();
     }
+}
+// stages 32 values in the warp's 2 KB box and stores them at {c0, c1}
+__device__ __forceinline__ void box64_emit(const CUtensorMap* m, uint8_t* box, int lane, const float* v, float scale,
+                                           int c0, int c1) {
+    box_acquire(lane);
+    box64_put_bf16x32(smem_u32(box), lane, v, scale);
+    box_store(m, box, lane, c0, c1);
 }
 
 struct GemmArgs {
@@ -213,10 +223,12 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // Epilogue of a 128 x 256 MXFP8 tile from registers: d holds columns [128 h, 128 h + 128) of
 // the thread's row.  For the gate/up product these are one [64 gate | 64 up] block of the
-// interleaved weight, i.e. g and u of I-columns [n0 + 64 h, n0 + 64 h + 64).
-template <int BN, int EPI>
-__device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& t, long long grow, int h,
-                                                 float* d) {
+// interleaved weight, i.e. g and u of I-columns [n0 + 64 h, n0 + 64 h + 64).  With TMA, the bf16
+// outputs go through the warp's 2 KB staging box (32 rows from brow, 32 columns at a time).
+template <int BN, int EPI, bool TMA>
+__device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& t, long long grow, int h, float* d,
+                                                 const CUtensorMap* tmC, const CUtensorMap* tmD, uint8_t* box,
+                                                 int lane, int brow) {
     if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
         __nv_bfloat16* gu = reinterpret_cast<__nv_bfloat16*>(a.out1);
 #pragma unroll
@@ -225,8 +237,13 @@ __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& 
             float* u = d + 64 + 32 * c;
             const int col = t.n0 + 64 * h + 32 * c;
             if (EPI == EPI_GU_ONLY || a.save_gu) {
-                store_bf16x32(gu + grow * (2LL * a.I) + col, g);
-                store_bf16x32(gu + grow * (2LL * a.I) + a.I + col, u);
+                if constexpr (TMA) {
+                    box64_emit(tmD, box, lane, g, 1.f, col, brow);
+                    box64_emit(tmD, box, lane, u, 1.f, a.I + col, brow);
+                } else {
+                    store_bf16x32(gu + grow * (2LL * a.I) + col, g);
+                    store_bf16x32(gu + grow * (2LL * a.I) + a.I + col, u);
+                }
             }
             if constexpr (EPI == EPI_SWIGLU) {
                 float hv[32];
@@ -244,10 +261,14 @@ __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& 
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out0) + grow * (long long)a.ld0 + t.n0 + 128 * h;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            float o[32];
+            if constexpr (TMA) {
+                box64_emit(tmC, box, lane, d + 32 * c, w, t.n0 + 128 * h + 32 * c, brow);
+            } else {
+                float o[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = w * d[32 * c + j];
-            store_bf16x32(out + 32 * c, o);
+                for (int j = 0; j < 32; ++j) o[j] = w * d[32 * c + j];
+                store_bf16x32(out + 32 * c, o);
+            }
         }
     } else if constexpr (EPI == EPI_WGRAD) {
         const long long off = (long long)t.e * a.out_e_stride + grow * a.ld0 + t.n0 + 128 * h;
@@ -304,7 +325,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     // columns, 128-byte swizzle) in shared memory and writes them with a TMA store (tmC; tmD for the
     // saved [g|u]), so that L2 receives whole lines rather than 16-byte halves of sectors
     constexpr bool kTmaOut = tma_out<EPI, MX, BN>();
-    constexpr int kOutBytes = kTmaOut ? kEpiWarps * out_box_bytes<EPI>() : 0;
+    constexpr int kOutBytes = kTmaOut ? kEpiWarps * out_box_bytes<EPI, kSingle>() : 0;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -615,7 +636,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty + acc);
-                if (t.valid) epilogue_drained<BN, EPI>(a, t, grow, half, d);
+                if (t.valid)
+                    epilogue_drained<BN, EPI, kTmaOut>(a, t, grow, half, d, &tmC, &tmD,
+                                                       sOut + (warp - 2) * out_box_bytes<EPI, kSingle>(), lane,
+                                                       t.m0 + 32 * quarter);
                 acc_phase ^= 1u;
                 continue;
             }
@@ -916,7 +940,9 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR, TWO>;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
-    const size_t out_bytes = tma_out<EPI, MX, BN>() ? (size_t)epi_warps<EPI, MX && BN == 256>() * out_box_bytes<EPI>() : 0;
+    const size_t out_bytes = tma_out<EPI, MX, BN>()
+                                 ? (size_t)epi_warps<EPI, MX && BN == 256>() * out_box_bytes<EPI, MX && BN == 256>()
+                                 : 0;
     const size_t fixed = 1024 + ring_stages<TWO>() * stage + out_bytes + 256;
     if (tma_out<EPI, MX, BN>() && !tc) return cudaErrorInvalidValue;
     const CUtensorMap& tcm = tc ? *tc : ta;   // kernels without a TMA-stored output never read it
@@ -1041,28 +1067,31 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
     const int64_t H = L.H, I = L.I, E = L.E, R = L.rows;
     auto u8 = [&](size_t off) { return reinterpret_cast<const uint8_t*>(b + off); };
     const int oes = a.out_f32 ? 4 : 2;   // weight-gradient output element size
-    CUtensorMap ta, tb, tc;
+    CUtensorMap ta, tb, tc, td;
     switch (kind) {
         case GemmKind::FwdGateUp:
         case GemmKind::FwdGateUpSaveOnly:
             // 256 weight rows = two [64 gate | 64 up] blocks = 128 I-columns per tile
-            if (!tmap_2d(&ta, b + M.x_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w13_r, 1, H, E * 2 * I, 256))
+            if (!tmap_2d(&ta, b + M.x_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w13_r, 1, H, E * 2 * I, 256) ||
+                !tmap_2d_sw64(&td, b + L.gu, 2, 2 * I, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 128); a.b_rows_e = (int)(2 * I);
             a.sfA = u8(M.x_r_sf); a.sfA_kt = (int)(H / 128);
             a.sfB = u8(M.w13_r_sf); a.sfB_kt = (int)(H / 128);
             a.out0 = b + L.hid; a.out1 = b + L.gu;
             a.q0 = reinterpret_cast<uint8_t*>(b + M.h_r); a.q0_sf = reinterpret_cast<uint8_t*>(b + M.h_r_sf);
-            return kind == GemmKind::FwdGateUp ? run<256, false, false, true, false, EPI_SWIGLU, true>(c, ta, tb, a)
-                                               : run<256, false, false, true, false, EPI_GU_ONLY, true>(c, ta, tb, a);
+            return kind == GemmKind::FwdGateUp
+                       ? run<256, false, false, true, false, EPI_SWIGLU, true>(c, ta, tb, a, &td, &td)
+                       : run<256, false, false, true, false, EPI_GU_ONLY, true>(c, ta, tb, a, &td, &td);
         case GemmKind::FwdDown:
-            if (!tmap_2d(&ta, b + M.h_r, 1, I, R, 128) || !tmap_2d(&tb, b + M.w2_r, 1, I, E * H, 256))
+            if (!tmap_2d(&ta, b + M.h_r, 1, I, R, 128) || !tmap_2d(&tb, b + M.w2_r, 1, I, E * H, 256) ||
+                !tmap_2d_sw64(&tc, b + L.ypart, 2, H, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 128); a.b_rows_e = (int)H;
             a.sfA = u8(M.h_r_sf); a.sfA_kt = (int)(I / 128);
             a.sfB = u8(M.w2_r_sf); a.sfB_kt = (int)(I / 128);
             a.out0 = b + L.ypart; a.ld0 = (int)H;
-            return run<256, false, false, false, false, EPI_WEIGHTED, true>(c, ta, tb, a);
+            return run<256, false, false, false, false, EPI_WEIGHTED, true>(c, ta, tb, a, &tc);
         case GemmKind::BwdDown:
             if (!tmap_2d(&ta, b + M.dy_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w2_c, 1, I, E * H, 128))
                 return cudaErrorInvalidValue;
@@ -1076,13 +1105,14 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.r_atoms = (int)(R / 128);
             return run<128, false, true, false, false, EPI_SWIGLU_BWD, true>(c, ta, tb, a);
         case GemmKind::BwdGateUp:
-            if (!tmap_2d(&ta, b + M.dg_r, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.w13_c, 1, H, E * 2 * I, 128))
+            if (!tmap_2d(&ta, b + M.dg_r, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.w13_c, 1, H, E * 2 * I, 128) ||
+                !tmap_2d_sw64(&tc, b + L.ypart, 2, H, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(2 * I / 128); a.b_rows_e = (int)(2 * I);
             a.sfA = u8(M.dg_r_sf); a.sfA_kt = (int)(2 * I / 128);
             a.sfB = u8(M.w13_c_sf); a.sfB_kt = (int)(E * 2 * I / 128);
             a.out0 = b + L.ypart; a.ld0 = (int)H;
-            return run<256, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a);
+            return run<256, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a, &tc);
         case GemmKind::WgradDown:
             // weight gradients keep 128 x 128 tiles with two accumulators: their contraction over an
             // expert's rows is short, so a drained single accumulator would stall the MMAs, and the

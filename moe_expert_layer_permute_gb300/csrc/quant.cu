@@ -57,26 +57,37 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
     __shared__ __align__(16) uint8_t qt[kQRows][kQCols + 16];
     __shared__ __align__(16) uint8_t s_sfr[512];
     __shared__ __align__(16) uint8_t s_sfc[512];
+    __shared__ long long s_src[128];   // source row of each tile row (-1: a zero padding row)
     const long long rt = (long long)blockIdx.y * 128;
     const long long R = tiles_dev ? (long long)(*tiles_dev) * kBM : R_max;
     if (rt >= R) return;
     const int c0 = blockIdx.x * kQCols;
     const int t = threadIdx.x;
-    for (int sub = 0; sub < 4; ++sub) {
-        const long long r0 = rt + 32 * sub;
-        // load 32 x 128 bf16 with 16-byte accesses (through the row map when dispatching)
+    if (row_slot) {
+        const int slot = __ldg(row_slot + rt + t);
+        s_src[t] = slot >= 0 ? slot / k : -1;
+    } else {
+        s_src[t] = rt + t;
+    }
+    __syncthreads();
+    // the 32 x 128 bf16 of pass `sub` with 16-byte accesses; thread t loads rows it*8 + t/16,
+    // columns 8 (t % 16) .. + 7 (through the row map when dispatching)
+    const int lr = t >> 4, lc = (t & 15) * 8;
+    auto load_pass = [&](int sub, uint4* w) {
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
-            const int rr = it * 8 + (t >> 4), cc = (t & 15) * 8;
-            long long sr = r0 + rr;
-            if (row_slot) {
-                const int slot = row_slot[sr];
-                sr = slot >= 0 ? slot / k : -1;
-            }
-            *reinterpret_cast<uint4*>(&tile[rr][cc]) =
-                sr >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + sr * C + c0 + cc)) : make_uint4(0, 0, 0, 0);
+            const long long sr = s_src[32 * sub + it * 8 + lr];
+            w[it] = sr >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + sr * C + c0 + lc)) : make_uint4(0, 0, 0, 0);
         }
+    };
+    uint4 nxt[4];
+    load_pass(0, nxt);
+    for (int sub = 0; sub < 4; ++sub) {
+        const long long r0 = rt + 32 * sub;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) *reinterpret_cast<uint4*>(&tile[it * 8 + lr][lc]) = nxt[it];
         __syncthreads();
+        if (sub < 3) load_pass(sub + 1, nxt);   // in flight while this pass is quantised
         if (q_row) {
             // thread -> (row t/4, block t%4): 32 consecutive values of one row
             const int rr = t >> 2, b = t & 3;
