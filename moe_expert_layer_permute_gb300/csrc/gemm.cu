@@ -775,10 +775,28 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
 #pragma unroll 1
                 for (int c = half; c < BN / 32; c += kHalves) {
                     float g[32], u[32];
-                    tmem_ld32(tacc + 32 * c, v);   // dA
                     const int col = t.n0 + 32 * c;
-                    load_bf16x32(gurow + col, g);
-                    load_bf16x32(gurow + a.I + col, u);
+                    // the saved g, u are requested first so that their latency overlaps the TMEM load
+                    uint4 graw[4], uraw[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        graw[q] = __ldg(reinterpret_cast<const uint4*>(gurow + col) + q);
+                        uraw[q] = __ldg(reinterpret_cast<const uint4*>(gurow + a.I + col) + q);
+                    }
+                    tmem_ld32(tacc + 32 * c, v);   // dA
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t gw[4] = {graw[q].x, graw[q].y, graw[q].z, graw[q].w};
+                        const uint32_t uw[4] = {uraw[q].x, uraw[q].y, uraw[q].z, uraw[q].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 gf = unpack_bf16x2(gw[i]), uf = unpack_bf16x2(uw[i]);
+                            g[8 * q + 2 * i] = gf.x;
+                            g[8 * q + 2 * i + 1] = gf.y;
+                            u[8 * q + 2 * i] = uf.x;
+                            u[8 * q + 2 * i + 1] = uf.y;
+                        }
+                    }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float s = sigmoidf_fast(g[j]);

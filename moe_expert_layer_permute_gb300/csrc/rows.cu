@@ -55,51 +55,59 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint4* _
     }
 }
 
-// One warp per token.  Each lane owns 8 consecutive columns of every 256-column chunk.
-__global__ void __launch_bounds__(kRowThreads) combine_rows_kernel(const uint4* __restrict__ part, uint4* __restrict__ out,
+// One warp per token.  Each lane owns 8 consecutive columns of every 256-column chunk and takes
+// two such chunks at a time, loading four routed rows of both before summing them (8 loads of 16
+// bytes in flight per lane, at 64 registers so that 64 warps stay resident: the kernel is bound
+// by memory latency).  Each output sums its k rows in the fixed order j = 0..k-1 in fp32.
+__device__ __forceinline__ void add_bf16x8(float* acc, uint4 w) {
+    const float2 a = unpack_bf16x2(w.x), b = unpack_bf16x2(w.y), c = unpack_bf16x2(w.z), d = unpack_bf16x2(w.w);
+    acc[0] += a.x; acc[1] += a.y; acc[2] += b.x; acc[3] += b.y;
+    acc[4] += c.x; acc[5] += c.y; acc[6] += d.x; acc[7] += d.y;
+}
+__device__ __forceinline__ uint4 pack_bf16x8(const float* acc) {
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    return o;
+}
+
+__global__ void __launch_bounds__(kRowThreads, 4) combine_rows_kernel(const uint4* __restrict__ part, uint4* __restrict__ out,
                                                                     const int* __restrict__ pos, int T, int k,
                                                                     int row_vecs, const float* __restrict__ dtw,
                                                                     int n_dtw, float* __restrict__ dtopk_w) {
+    constexpr int kBatch = 4;   // routed rows loaded per batch (for each of the two chunks)
     const int wpb = kRowThreads / 32;
     const int lane = threadIdx.x & 31;
     const int stride = gridDim.x * wpb;
     for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += stride) {
         const int* pt = pos + (size_t)t * k;
-        for (int v = lane; v < row_vecs; v += 32) {
-            float acc[8];
+        for (int v0 = lane; v0 < row_vecs; v0 += 64) {
+            const int v1 = v0 + 32;
+            const bool two = v1 < row_vecs;
+            float acc0[8], acc1[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-            int j = 0;
-            for (; j + 4 <= k; j += 4) {
-                uint4 w[4];
+            for (int q = 0; q < 8; ++q) acc0[q] = acc1[q] = 0.f;
+            for (int j0 = 0; j0 < k; j0 += kBatch) {
+                uint4 w0[kBatch], w1[kBatch];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int p = pt[j + u];
-                    w[u] = p >= 0 ? __ldg(part + (size_t)p * row_vecs + v) : make_uint4(0, 0, 0, 0);
+                for (int u = 0; u < kBatch; ++u) {
+                    const int p = j0 + u < k ? pt[j0 + u] : -1;
+                    const uint4* r = part + (size_t)(p >= 0 ? p : 0) * row_vecs;
+                    w0[u] = p >= 0 ? __ldg(r + v0) : make_uint4(0, 0, 0, 0);
+                    w1[u] = (p >= 0 && two) ? __ldg(r + v1) : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 a = unpack_bf16x2(w[u].x), b = unpack_bf16x2(w[u].y), c = unpack_bf16x2(w[u].z),
-                                 d = unpack_bf16x2(w[u].w);
-                    acc[0] += a.x; acc[1] += a.y; acc[2] += b.x; acc[3] += b.y;
-                    acc[4] += c.x; acc[5] += c.y; acc[6] += d.x; acc[7] += d.y;
+                for (int u = 0; u < kBatch; ++u) {
+                    if (j0 + u < k) {
+                        add_bf16x8(acc0, w0[u]);
+                        add_bf16x8(acc1, w1[u]);
+                    }
                 }
             }
-            for (; j < k; ++j) {
-                const int p = pt[j];
-                if (p < 0) continue;
-                const uint4 w = __ldg(part + (size_t)p * row_vecs + v);
-                const float2 a = unpack_bf16x2(w.x), b = unpack_bf16x2(w.y), c = unpack_bf16x2(w.z),
-                             d = unpack_bf16x2(w.w);
-                acc[0] += a.x; acc[1] += a.y; acc[2] += b.x; acc[3] += b.y;
-                acc[4] += c.x; acc[5] += c.y; acc[6] += d.x; acc[7] += d.y;
-            }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            out[(size_t)t * row_vecs + v] = o;
+            out[(size_t)t * row_vecs + v0] = pack_bf16x8(acc0);
+            if (two) out[(size_t)t * row_vecs + v1] = pack_bf16x8(acc1);
         }
         if (dtopk_w) {
             for (int j = lane; j < k; j += 32) {
