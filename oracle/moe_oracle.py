@@ -166,6 +166,14 @@ def _as64(a):
     return np.asarray(a, dtype=np.float64)
 
 
+def _stored_bf16(a):
+    """a as the layer stores it between its forward and its backward: an fp32 value rounded to
+    bf16 (to nearest, ties to even), read back exactly."""
+    u = np.asarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = ((u + ((u >> np.uint64(16)) & np.uint64(1)) + np.uint64(0x7FFF)) >> np.uint64(16)) << np.uint64(16)
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def forward(x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, keep: bool = False):
     """y[t] = sum_j w[t,j] * W2[e] (silu(W13[e,:I] x[t]) * (W13[e,I:] x[t])), e = topk_idx[t,j].
 
@@ -217,7 +225,9 @@ def backward(dy, x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, fp8_bwd: 
       dW2[e] += dy[t] (w h)^T               dW13[e,:I] += dg x[t]^T,  dW13[e,I:] += du x[t]^T
     In MXFP8 mode each GEMM operand is quantised along that GEMM's contraction axis first
     (for the weight gradients the contraction runs over the tokens of one expert group); with
-    fp8_bwd only the backward GEMMs' operands are, the forward (g, u, h) staying exact.
+    fp8_bwd only the backward GEMMs' operands are, the forward (g, u, h) staying exact.  With a
+    quantised backward, g and u enter it as the layer stores them, in bf16: the quantised codes of
+    [dg|du] and w h are decided from those values.
     """
     dy, x, W13, W2 = _as64(dy), _as64(x), _as64(W13), _as64(W2)
     T, H = x.shape
@@ -229,6 +239,11 @@ def backward(dy, x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, fp8_bwd: 
     r = fw["route"]
     off = r["off"]
     g, u, h, w_s = fw["g"], fw["u"], fw["h"], fw["w_sorted"]
+    if qb:
+        # the E4M3 codes of [dg|du] and w h are decided from the pre-activations as the layer
+        # keeps them for its backward, in bf16; both sides decide from the same stored values
+        g, u = _stored_bf16(g), _stored_bf16(u)
+        h = silu(g) * u
     X = fw["X_perm"]                         # already quantised along H in MXFP8 mode
     X_raw = permute_rows(x, r["perm"], k)
     dY = permute_rows(dy, r["perm"], k)
@@ -324,6 +339,8 @@ def backward_tokens(dy, x, topk_idx, topk_w, W13, W2, tokens, *, mxfp8: bool = F
             Wdb = mx_qdq(Wd, axis=0) if qb else Wd          # dgrad: contraction over H
             g = Wf[:I] @ xt
             u = Wf[I:] @ xt
+            if qb:
+                g, u = _stored_bf16(g), _stored_bf16(u)
             sg = sigmoid(g)
             dA = Wdb.T @ dyt
             dtw[n, j] = dA @ (silu(g) * u)
@@ -358,6 +375,8 @@ def wgrad_experts(dy, x, topk_idx, topk_w, W13, W2, experts, *, mxfp8: bool = Fa
             dYb, Wdb = mx_qdq(dY, axis=1), mx_qdq(Wd, axis=0)
         g = Xf @ Wf[:I].T
         u = Xf @ Wf[I:].T
+        if qb:
+            g, u = _stored_bf16(g), _stored_bf16(u)
         sg = sigmoid(g)
         h = g * sg * u
         dA = dYb @ Wdb

@@ -192,3 +192,58 @@ def test_fused_epilogue_copies(cuda_lib):
     assert rel_fro(decode_mx(q, sf, "col")[prow], oracle.mx_qdq_segments(ref["dG"], r["off"])) < TOL
     q, sf = _mxview(L, "hw_c", (R, I))
     assert rel_fro(decode_mx(q, sf, "col")[prow], oracle.mx_qdq_segments(ref["Hw"], r["off"])) < TOL
+
+
+# ---------------------------------------------------------------- edge cases in both block-scaled modes
+def _edge_inputs(case, precision):
+    import dataclasses
+    mk = lambda **kw: dataclasses.replace(gen.custom_config(**kw), precision=precision)   # noqa: E731
+    if case == "one_token":
+        return gen.make_inputs(mk(T=1, H=256, I=128, E=8, k=2, seed=31))
+    if case == "all_on_one_expert":
+        inp = gen.make_inputs(mk(T=300, H=256, I=128, E=8, k=1, seed=32))
+        inp.topk_idx = np.full((300, 1), 5, dtype=np.int32)
+        return inp
+    if case == "empty_experts":
+        inp = gen.make_inputs(mk(T=400, H=256, I=256, E=16, k=2, seed=33))
+        inp.topk_idx = np.ascontiguousarray(np.stack([np.arange(400) % 3, 7 + np.arange(400) % 2], 1).astype(np.int32))
+        return inp
+    if case == "single_expert_top1":
+        return gen.make_inputs(mk(T=200, H=256, I=128, E=1, k=1, seed=34))
+    return gen.make_inputs(mk(T=20, H=512, I=256, E=4, k=2, seed=35))     # fewer rows than a tile
+
+
+@pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
+@pytest.mark.parametrize("case", ["one_token", "all_on_one_expert", "empty_experts", "single_expert_top1",
+                                  "fewer_rows_than_a_tile"])
+def test_edge_cases_block_scaled(cuda_lib, case, precision):
+    inp = _edge_inputs(case, precision)
+    L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
+    L.fwd()
+    L.bwd()
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    mode = {"mxfp8": True} if precision == "mxfp8" else {"fp8_bwd": True}
+    y = oracle.forward(*_args(inp), mxfp8=precision == "mxfp8")
+    ref = oracle.backward(inp.f64("dy"), *_args(inp), **mode)
+    assert rel_fro(f64(L.y), y) < TOL
+    for got, n in ((L.dx, "dx"), (L.dW13, "dW13"), (L.dW2, "dW2"), (L.dtw, "dtopk_w")):
+        if np.linalg.norm(ref[n]) == 0:
+            assert torch.all(got == 0), n
+        else:
+            assert rel_fro(f64(got), ref[n]) < TOL, (n, rel_fro(f64(got), ref[n]))
+    if case == "empty_experts":
+        idle = sorted(set(range(16)) - set(np.unique(inp.topk_idx).tolist()))
+        assert torch.all(L.dW13[idle] == 0) and torch.all(L.dW2[idle] == 0)
+
+
+@pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
+def test_zero_tokens_block_scaled(cuda_lib, precision):
+    import dataclasses
+    inp = gen.make_inputs(dataclasses.replace(gen.custom_config(T=0, H=256, I=128, E=8, k=2, seed=36),
+                                              precision=precision))
+    L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
+    L.fwd()
+    L.bwd()
+    torch.cuda.synchronize()
+    assert torch.all(L.dW13 == 0) and torch.all(L.dW2 == 0)

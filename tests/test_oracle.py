@@ -314,6 +314,7 @@ def test_mxfp8_with_identity_quantiser_equals_bf16_path(monkeypatch):
     ref = oracle.backward(dy, x, idx, w, W13, W2)
     monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", lambda a, axis: np.asarray(a, dtype=np.float64))
     monkeypatch.setattr(oracle.moe_oracle, "mx_qdq_segments", lambda a, st: np.asarray(a, dtype=np.float64))
+    monkeypatch.setattr(oracle.moe_oracle, "_stored_bf16", lambda a: np.asarray(a, dtype=np.float64))
     got = oracle.backward(dy, x, idx, w, W13, W2, mxfp8=True)
     for k_ in ("dx", "dW13", "dW2", "dtopk_w"):
         np.testing.assert_allclose(got[k_], ref[k_], rtol=1e-13, atol=1e-13)
@@ -375,6 +376,7 @@ def test_fp8_bwd_with_identity_quantiser_equals_bf16_path(monkeypatch):
     ref = oracle.backward(dy, x, idx, w, W13, W2)
     monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", lambda a, axis: np.asarray(a, dtype=np.float64))
     monkeypatch.setattr(oracle.moe_oracle, "mx_qdq_segments", lambda a, st: np.asarray(a, dtype=np.float64))
+    monkeypatch.setattr(oracle.moe_oracle, "_stored_bf16", lambda a: np.asarray(a, dtype=np.float64))
     got = oracle.backward(dy, x, idx, w, W13, W2, fp8_bwd=True)
     for k_ in ("dx", "dW13", "dW2", "dtopk_w"):
         np.testing.assert_allclose(got[k_], ref[k_], rtol=1e-13, atol=1e-13)
@@ -463,3 +465,29 @@ def test_router_backward_matches_finite_differences_and_autograd():
     sel = torch.gather(lt, 1, torch.tensor(idx, dtype=torch.int64))
     (torch.softmax(sel, 1) * torch.tensor(dw)).sum().backward()
     np.testing.assert_allclose(dl, lt.grad.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_stored_bf16_rounds_to_nearest_even():
+    """The bf16 storage of the saved pre-activations against torch's own float32 -> bfloat16 cast,
+    on random values and on exact ties."""
+    import torch
+    rng = np.random.default_rng(34)
+    a = np.concatenate([rng.standard_normal(100000) * 10 ** rng.uniform(-3, 3, 100000),
+                        # exact ties between two bf16 neighbours, both parities
+                        (np.arange(1, 2001, dtype=np.float64) * 2 + 1) * 2.0 ** -8])
+    got = oracle.moe_oracle._stored_bf16(a)
+    ref = torch.tensor(a.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_quantised_backward_reads_bf16_stored_pre_activations(monkeypatch):
+    """With identity quantisers the only difference left between the fp8_bwd and the BF16 backward
+    is the bf16 storage of g and u: small, and gone when the storage is exact too."""
+    cfg = _small_cfg(T=48, H=32, I=32, E=4, k=2, seed=15)
+    x, idx, w, W13, W2, dy = _f64(gen.make_inputs(cfg))
+    ref = oracle.backward(dy, x, idx, w, W13, W2)
+    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", lambda a, axis: np.asarray(a, dtype=np.float64))
+    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq_segments", lambda a, st: np.asarray(a, dtype=np.float64))
+    got = oracle.backward(dy, x, idx, w, W13, W2, fp8_bwd=True)
+    for k_ in ("dx", "dW13", "dW2", "dtopk_w"):
+        assert 1e-6 < _rel(got[k_], ref[k_]) < 1e-2, k_
