@@ -37,7 +37,7 @@ import numpy as np
 
 __all__ = [
     "route", "permute_rows", "unpermute_sum", "sigmoid", "silu",
-    "e4m3_round", "mx_block_exponent", "mx_qdq", "mx_qdq_segments",
+    "e4m3_round", "e2m1_round", "mx_block_exponent", "mx_qdq", "mx_qdq_segments",
     "forward", "backward", "forward_tokens", "backward_tokens", "wgrad_experts",
     "router_forward", "router_backward",
 ]
@@ -115,33 +115,54 @@ def e4m3_round(v: np.ndarray) -> np.ndarray:
     return np.copysign(q, v)
 
 
-def mx_block_exponent(amax: np.ndarray) -> np.ndarray:
-    """Shared block exponent floor(log2(amax)) - 8, clamped to the E8M0 range; -127 for amax = 0."""
+# MXFP4 (the FP4 of the pages' FP8 x FP4 weights; OCP MX v1.0): E2M1 elements, values
+# {0, 0.5, 1, 1.5, 2, 3, 4, 6}, with the same E8M0 scale per 32 elements
+E2M1_MAX = 6.0
+E2M1_EMAX = 2          # exponent of the largest E2M1 value (6 = 1.5 * 2^2)
+E2M1_EMIN = 0          # exponent of the smallest normal (1.0); the subnormal is 0.5
+
+
+def e2m1_round(v: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 value (1 mantissa bit, ties to even), saturated to +-6."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)
+    e = np.maximum(ex - 1, E2M1_EMIN)
+    step = np.ldexp(1.0, e - 1)
+    q = np.minimum(np.round(a / step) * step, E2M1_MAX)
+    return np.copysign(q, v)
+
+
+def mx_block_exponent(amax: np.ndarray, emax: int = E4M3_EMAX) -> np.ndarray:
+    """Shared block exponent floor(log2(amax)) - emax (8 for E4M3, 2 for E2M1), clamped to the E8M0
+    range; -127 for amax = 0."""
     amax = np.asarray(amax, dtype=np.float64)
     _, ex = np.frexp(amax)
-    se = (ex - 1) - E4M3_EMAX
+    se = (ex - 1) - emax
     se = np.clip(se, -127, 127)
     return np.where(amax > 0, se, -127).astype(np.int64)
 
 
-def _qdq_last_axis(a: np.ndarray) -> np.ndarray:
+def _qdq_last_axis(a: np.ndarray, fmt: str = "e4m3") -> np.ndarray:
+    rnd, emax = (e4m3_round, E4M3_EMAX) if fmt == "e4m3" else (e2m1_round, E2M1_EMAX)
     n = a.shape[-1]
     nb = -(-n // MX_BLOCK)
     pad = nb * MX_BLOCK - n
     if pad:
         a = np.concatenate([a, np.zeros(a.shape[:-1] + (pad,))], axis=-1)
     b = a.reshape(a.shape[:-1] + (nb, MX_BLOCK))
-    se = mx_block_exponent(np.abs(b).max(axis=-1))[..., None]
+    se = mx_block_exponent(np.abs(b).max(axis=-1), emax)[..., None]
     scale = np.ldexp(1.0, se)
-    q = e4m3_round(b / scale) * scale
+    q = rnd(b / scale) * scale
     q = q.reshape(a.shape)
     return q[..., :n] if pad else q
 
 
-def mx_qdq(a: np.ndarray, axis: int) -> np.ndarray:
-    """Quantise to MXFP8 with 32-element blocks running along `axis`, then dequantise (fp64)."""
+def mx_qdq(a: np.ndarray, axis: int, fmt: str = "e4m3") -> np.ndarray:
+    """Quantise to MXFP8 (fmt "e4m3") or MXFP4 ("e2m1") with 32-element blocks running along
+    `axis`, then dequantise (fp64)."""
     a = np.moveaxis(np.asarray(a, dtype=np.float64), axis, -1)
-    return np.moveaxis(_qdq_last_axis(a), -1, axis)
+    return np.moveaxis(_qdq_last_axis(a, fmt), -1, axis)
 
 
 def mx_qdq_segments(a: np.ndarray, starts: np.ndarray) -> np.ndarray:
@@ -174,12 +195,17 @@ def _stored_bf16(a):
     return b.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
-def forward(x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, keep: bool = False):
+def forward(x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, fp8_fp4: bool = False, keep: bool = False):
     """y[t] = sum_j w[t,j] * W2[e] (silu(W13[e,:I] x[t]) * (W13[e,I:] x[t])), e = topk_idx[t,j].
 
     Evaluated per expert group in sorted (routed) order.  With keep=True also returns the
-    intermediates in sorted order: X_perm, g, u, h, o (and the routing dict).
+    intermediates in sorted order: X_perm, g, u, h, o (and the routing dict).  fp8_fp4: the FP8 x
+    FP4 forward the pages list for DeepGEMM's Mega MoE (wire.sakhanda.co, section "Как се
+    сравнява с други слети MoE опции?", comparison table), read as MXFP8 activations (X, h) times
+    MXFP4 weights (W13, W2), each blocked along its contraction.
     """
+    if fp8_fp4:
+        mxfp8 = True
     x, W13, W2 = _as64(x), _as64(W13), _as64(W2)
     T, H = x.shape
     E, I2, _ = W13.shape
@@ -198,8 +224,9 @@ def forward(x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, keep: bool = F
             continue
         Wg, Wu, Wd = W13[e, :I], W13[e, I:], W2[e]
         if mxfp8:
-            Wg, Wu = mx_qdq(Wg, axis=1), mx_qdq(Wu, axis=1)
-            Wd = mx_qdq(Wd, axis=1)          # W2[e] is [H, I]: blocks along I, the contraction
+            wf = "e2m1" if fp8_fp4 else "e4m3"
+            Wg, Wu = mx_qdq(Wg, axis=1, fmt=wf), mx_qdq(Wu, axis=1, fmt=wf)
+            Wd = mx_qdq(Wd, axis=1, fmt=wf)  # W2[e] is [H, I]: blocks along I, the contraction
         g[lo:hi] = X[lo:hi] @ Wg.T
         u[lo:hi] = X[lo:hi] @ Wu.T
         h[lo:hi] = silu(g[lo:hi]) * u[lo:hi]
@@ -290,9 +317,11 @@ def backward(dy, x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, fp8_bwd: 
 # ----------------------------------------------------------------------------------------------
 # sampled evaluation for full-size checks: a few tokens or a few experts at a time
 # ----------------------------------------------------------------------------------------------
-def forward_tokens(x, topk_idx, topk_w, W13, W2, tokens, *, mxfp8: bool = False):
-    """y[t] for the listed tokens only, one slot at a time (BF16 / MXFP8 as in `forward`)."""
+def forward_tokens(x, topk_idx, topk_w, W13, W2, tokens, *, mxfp8: bool = False, fp8_fp4: bool = False):
+    """y[t] for the listed tokens only, one slot at a time (BF16 / MXFP8 / FP8 x FP4 as in `forward`)."""
     I = W13.shape[1] // 2
+    wf = "e2m1" if fp8_fp4 else "e4m3"
+    mxfp8 = mxfp8 or fp8_fp4
     out = np.zeros((len(tokens), x.shape[1]))
     for n, t in enumerate(tokens):
         xt = _as64(x[t])
@@ -302,7 +331,7 @@ def forward_tokens(x, topk_idx, topk_w, W13, W2, tokens, *, mxfp8: bool = False)
             e = int(topk_idx[t, j])
             W = _as64(W13[e]); Wd = _as64(W2[e])
             if mxfp8:
-                W = mx_qdq(W, axis=1); Wd = mx_qdq(Wd, axis=1)
+                W = mx_qdq(W, axis=1, fmt=wf); Wd = mx_qdq(Wd, axis=1, fmt=wf)
             g = W[:I] @ xt
             u = W[I:] @ xt
             hh = silu(g) * u

@@ -281,7 +281,8 @@ def test_mxfp8_quantisation_points_follow_the_contraction_axes(monkeypatch):
     in_seg = []
     real, real_seg = oracle.moe_oracle.mx_qdq, oracle.moe_oracle.mx_qdq_segments
 
-    def rec(a, axis):
+    def rec(a, axis, fmt="e4m3"):
+        assert fmt == "e4m3"
         if not in_seg:
             calls.append(("ax", np.shape(a), axis))
         return real(a, axis)
@@ -312,7 +313,7 @@ def test_mxfp8_with_identity_quantiser_equals_bf16_path(monkeypatch):
     cfg = _small_cfg(T=48, H=32, I=32, E=4, k=2, seed=15)
     x, idx, w, W13, W2, dy = _f64(gen.make_inputs(cfg))
     ref = oracle.backward(dy, x, idx, w, W13, W2)
-    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", lambda a, axis: np.asarray(a, dtype=np.float64))
+    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", lambda a, axis, fmt="e4m3": np.asarray(a, dtype=np.float64))
     monkeypatch.setattr(oracle.moe_oracle, "mx_qdq_segments", lambda a, st: np.asarray(a, dtype=np.float64))
     monkeypatch.setattr(oracle.moe_oracle, "_stored_bf16", lambda a: np.asarray(a, dtype=np.float64))
     got = oracle.backward(dy, x, idx, w, W13, W2, mxfp8=True)
@@ -334,7 +335,8 @@ def _record_quantiser_calls(monkeypatch):
     calls, in_seg = [], []
     real, real_seg = oracle.moe_oracle.mx_qdq, oracle.moe_oracle.mx_qdq_segments
 
-    def rec(a, axis):
+    def rec(a, axis, fmt="e4m3"):
+        assert fmt == "e4m3"
         if not in_seg:
             calls.append(("ax", np.shape(a), axis))
         return real(a, axis)
@@ -374,7 +376,7 @@ def test_fp8_bwd_with_identity_quantiser_equals_bf16_path(monkeypatch):
     cfg = _small_cfg(T=48, H=32, I=32, E=4, k=2, seed=15)
     x, idx, w, W13, W2, dy = _f64(gen.make_inputs(cfg))
     ref = oracle.backward(dy, x, idx, w, W13, W2)
-    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", lambda a, axis: np.asarray(a, dtype=np.float64))
+    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", lambda a, axis, fmt="e4m3": np.asarray(a, dtype=np.float64))
     monkeypatch.setattr(oracle.moe_oracle, "mx_qdq_segments", lambda a, st: np.asarray(a, dtype=np.float64))
     monkeypatch.setattr(oracle.moe_oracle, "_stored_bf16", lambda a: np.asarray(a, dtype=np.float64))
     got = oracle.backward(dy, x, idx, w, W13, W2, fp8_bwd=True)
@@ -486,8 +488,63 @@ def test_quantised_backward_reads_bf16_stored_pre_activations(monkeypatch):
     cfg = _small_cfg(T=48, H=32, I=32, E=4, k=2, seed=15)
     x, idx, w, W13, W2, dy = _f64(gen.make_inputs(cfg))
     ref = oracle.backward(dy, x, idx, w, W13, W2)
-    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", lambda a, axis: np.asarray(a, dtype=np.float64))
+    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", lambda a, axis, fmt="e4m3": np.asarray(a, dtype=np.float64))
     monkeypatch.setattr(oracle.moe_oracle, "mx_qdq_segments", lambda a, st: np.asarray(a, dtype=np.float64))
     got = oracle.backward(dy, x, idx, w, W13, W2, fp8_bwd=True)
     for k_ in ("dx", "dW13", "dW2", "dtopk_w"):
         assert 1e-6 < _rel(got[k_], ref[k_]) < 1e-2, k_
+
+
+# ---------------------------------------------------------------- MXFP4 weights (FP8 x FP4 forward)
+def test_e2m1_grid_round_trips_ties_to_even_and_saturates():
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], dtype=np.float64)
+    for g in np.concatenate([grid, -grid]):
+        assert oracle.e2m1_round(np.array([g]))[0] == g
+    mids = {0.25: 0.0, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0, 5.0: 4.0}   # ties to the even code
+    for v, q in mids.items():
+        assert oracle.e2m1_round(np.array([v]))[0] == q, v
+        assert oracle.e2m1_round(np.array([-v]))[0] == -q, v
+    assert oracle.e2m1_round(np.array([5.9, 7.0, 1e9]))[0] == 6.0
+    assert np.all(oracle.e2m1_round(np.array([7.0, 1e9, -50.0])) == np.array([6.0, 6.0, -6.0]))
+
+
+def test_mxfp4_block_exponent_on_hand_built_blocks():
+    b = np.zeros((1, 32))
+    b[0, :3] = [6.0, 1.0, -0.75]              # amax 6: exponent floor(log2 6) - 2 = 0, scale 1
+    np.testing.assert_array_equal(oracle.mx_qdq(b, axis=1, fmt="e2m1")[0, :3], [6.0, 1.0, -1.0])
+    b[0, :3] = [1.0, 0.3, 0.2]                # amax 1: exponent -2, scale 1/4: 0.3 -> 1.2 -> 1.0 -> 0.25
+    np.testing.assert_allclose(oracle.mx_qdq(b, axis=1, fmt="e2m1")[0, :3], [1.0, 0.25, 0.25])
+    b[0, :3] = [7.5, 7.0, 0.0]                # amax 7.5: exponent 0, 7.5 and 7 saturate to 6
+    np.testing.assert_array_equal(oracle.mx_qdq(b, axis=1, fmt="e2m1")[0, :3], [6.0, 6.0, 0.0])
+
+
+def test_fp8_fp4_forward_quantises_weights_to_e2m1_and_activations_to_e4m3(monkeypatch):
+    cfg = _small_cfg(T=40, H=64, I=96, E=3, k=2, seed=14)
+    x, idx, w, W13, W2, dy = _f64(gen.make_inputs(cfg))
+    calls = []
+    real = oracle.moe_oracle.mx_qdq
+
+    def rec(a, axis, fmt="e4m3"):
+        calls.append((np.shape(a), axis, fmt))
+        return real(a, axis, fmt)
+    monkeypatch.setattr(oracle.moe_oracle, "mx_qdq", rec)
+    oracle.forward(x, idx, w, W13, W2, fp8_fp4=True)
+    H, I, S = 64, 96, 80
+    assert ((S, H), 1, "e4m3") in calls                       # X_perm along H
+    assert all(c[2] == "e2m1" for c in calls if c[0] in ((I, H), (H, I)))   # every weight block
+    assert ((I, H), 1, "e2m1") in calls and ((H, I), 1, "e2m1") in calls
+    assert any(c[0][1] == I and c[0][0] not in (H,) and c[2] == "e4m3" for c in calls)   # h along I
+
+
+def test_fp8_fp4_identity_quantiser_and_sampled_form():
+    cfg = _small_cfg(T=80, H=64, I=32, E=6, k=3, seed=12)
+    x, idx, w, W13, W2, dy = _f64(gen.make_inputs(cfg))
+    y = oracle.forward(x, idx, w, W13, W2, fp8_fp4=True)
+    toks = [0, 17, 79]
+    np.testing.assert_allclose(oracle.forward_tokens(x, idx, w, W13, W2, toks, fp8_fp4=True), y[toks],
+                               rtol=1e-11, atol=1e-12)
+    y_bf = oracle.forward(x, idx, w, W13, W2)
+    assert 5e-2 < _rel(y, y_bf) < 4e-1      # E2M1 weights (one mantissa bit) through two GEMMs
+    import unittest.mock as um
+    with um.patch.object(oracle.moe_oracle, "mx_qdq", lambda a, axis, fmt="e4m3": np.asarray(a, dtype=np.float64)):
+        np.testing.assert_allclose(oracle.forward(x, idx, w, W13, W2, fp8_fp4=True), y_bf, rtol=1e-13, atol=1e-13)
