@@ -51,7 +51,14 @@ extern "C" {
 /* MOE_FP8_BWD: the forward in BF16 and the backward in MXFP8 (the pages' fp8_bwd precision, a BF16
  * forward with an FP8 backward: MarkTechPost, "Prime Intellect Releases Prime Mega MoE", section
  * "How does the fused kernel work?"); y is bit-identical to MOE_BF16's. */
-typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_FP8_BWD = 2 } moe_precision;
+/* MOE_FP8_FP4: a forward-only layer whose GEMMs take MXFP8 activations (E4M3) times MXFP4 weights
+ * (E2M1 values, grid 0, 0.5, 1, 1.5, 2, 3, 4, 6, one E8M0 scale per 32 values with exponent
+ * floor(log2(amax)) - 2, ties to even, saturating at 6), each blocked along its GEMM's contraction
+ * (the FP8xFP4 data type the comparison table lists for DeepGEMM's Mega MoE: wire.sakhanda.co,
+ * "Prime Intellect пусна Prime Mega MoE", section "Как се сравнява с други слети MoE опции?", data
+ * types row; the English copy of that table drops the row).  Forward only, like DeepGEMM's kernel:
+ * moe_bwd returns MOE_ERR_UNSUPPORTED for it. */
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_FP8_BWD = 2, MOE_FP8_FP4 = 3 } moe_precision;
 typedef enum { MOE_DT_BF16 = 0, MOE_DT_F32 = 1, MOE_DT_I32 = 2 } moe_dtype;
 
 /* A view of a caller-owned buffer: `data` is a device pointer for the layer calls. */
@@ -125,7 +132,8 @@ int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* t
             moe_scratch* scratch, void* stream);
 
 /* Backward of <dy, y>: dx, dW13, dW2 and dtopk_w (all overwritten).  Without
- * MOE_FLAG_REUSE_FWD it recomputes the routing and the first GEMM itself. */
+ * MOE_FLAG_REUSE_FWD it recomputes the routing and the first GEMM itself.  MOE_FP8_FP4 scratch:
+ * MOE_ERR_UNSUPPORTED (forward only). */
 int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_idx,
             const moe_tensor* topk_w, const moe_tensor* W13, const moe_tensor* W2,
             moe_tensor* dx, moe_tensor* dW13, moe_tensor* dW2, moe_tensor* dtopk_w,
@@ -200,13 +208,16 @@ enum {
     MOE_VIEW_XPERM, MOE_VIEW_HID, MOE_VIEW_GU, MOE_VIEW_YPART, MOE_VIEW_DG, MOE_VIEW_HW,
     MOE_VIEW_DYPERM, MOE_VIEW_COUNT_
 };
-/* MXFP8 operand copies (MOE_MXFP8; MOE_FP8_BWD has only the backward's: X_C, DY_R, DY_C, DG_R, DG_C,
- * HW_C, W13_C, W2_C, the others are 0 bytes): for each operand a uint8 E4M3 value array in
+/* MX operand copies (MOE_MXFP8; MOE_FP8_BWD has only the backward's: X_C, DY_R, DY_C, DG_R, DG_C,
+ * HW_C, W13_C, W2_C; MOE_FP8_FP4 only the forward's: X_R, H_R, W13_R, W2_R; absent ones are 0
+ * bytes): for each operand a uint8 E4M3 value array in
  * the source's layout, then its E8M0 scales (one byte per 32 values) in tensor-core atoms of 128
  * MN-rows x 4 K-blocks (512 bytes: MN-row m, K-block b at byte 16*(m%32) + 4*((m/32)%4) + b%4;
  * atom (m/128, b/4) at ((m/128) * (K/128) + b/4) * 512).  "_R" copies are blocked along the row
  * (MN = rows, K = columns), "_C" copies along the column (MN = columns, K = rows).
- * W13_R stores each expert's rows in 128-row blocks of [64 gate rows | 64 up rows]. */
+ * W13_R stores each expert's rows in 128-row blocks of [64 gate rows | 64 up rows].  Under
+ * MOE_FP8_FP4, W13_R and W2_R hold packed E2M1 values, two per byte (the even column in the low
+ * nibble), half the bytes of a row; their scale arrays keep the layout above. */
 enum {
     MOE_VIEW_MX_X_R = 32, MOE_VIEW_MX_X_R_SF, MOE_VIEW_MX_X_C, MOE_VIEW_MX_X_C_SF,
     MOE_VIEW_MX_H_R, MOE_VIEW_MX_H_R_SF,

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -328,12 +329,15 @@ __device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t sbo) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
+// B-operand format field of the kind::mxf8f6f4 instruction descriptor for E2M1 (bits 10-12 = 5).
+constexpr uint32_t kFmtE2M1B = 5u << 10;
+
 // Instruction descriptor of kind::mxf8f6f4 with E4M3 A/B, fp32 D and E8M0 block scales;
 // sfa_id / sfb_id select the byte (K-block) of the 32-bit scale column each MMA reads.
 __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, bool a_mn_major, bool b_mn_major, uint32_t sfa_id,
                                                   uint32_t sfb_id) {
     return ((sfb_id & 3u) << 4)                        // B scale-factor id
-           | (0u << 7) | (0u << 10)                    // A, B: E4M3
+           | (0u << 7) | (0u << 10)                    // A, B: E4M3 (B: kFmtE2M1B OR-ed in)
            | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | (1u << 23)     // scales are UE8M0
            | ((uint32_t)(M >> 4) << 24) | ((sfa_id & 3u) << 29);
@@ -420,6 +424,19 @@ __device__ __forceinline__ void mx_scale_bits(uint32_t amax_bits, uint8_t* sf, f
     const int b = max((int)(amax_bits >> 23) - 8, 0);
     *sf = (uint8_t)b;
     *inv = __uint_as_float((uint32_t)(254 - b) << 23);
+}
+
+// MXFP4 (E2M1 values) block scale: floor(log2(amax)) - 2 (2 = the largest E2M1 exponent), by the
+// same field arithmetic as mx_scale_bits.
+__device__ __forceinline__ void mx_scale_bits_e2m1(uint32_t amax_bits, uint8_t* sf, float* inv) {
+    const int b = max((int)(amax_bits >> 23) - 2, 0);
+    *sf = (uint8_t)b;
+    *inv = __uint_as_float((uint32_t)(254 - b) << 23);
+}
+
+// Two values to E2M1 (round to nearest even, saturated to +-6), a in the low nibble.
+__device__ __forceinline__ uint32_t to_e2m1x2(float a, float b) {
+    return (uint32_t)__nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest);
 }
 
 // Two values to E4M3 (round to nearest even, saturated to +-448), packed low byte first.

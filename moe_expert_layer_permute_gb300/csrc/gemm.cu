@@ -151,6 +151,8 @@ struct GemmArgs {
     uint8_t* q2;
     uint8_t* q2_sf;
     int r_atoms;               // padded row capacity / 128 (K atoms of the row-blocked scales)
+    uint32_t b_fmt;            // B-format bits OR-ed into the block-scaled instruction descriptor
+                               // (kFmtE2M1B: MXFP4 weights, unpacked to 16-byte rows by the TMA)
 };
 
 struct Tile {
@@ -552,8 +554,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                                                      : sdesc_sw128(sa + ks * kKStep, 16, 1024);
                             const uint64_t bd = B_MN ? sdesc_sw128(sb + ks * kMnStep, kMnLbo, 1024)
                                                      : sdesc_sw128(sb + ks * kKStep, 16, 1024);
-                            mma_mxf8(d_tmem, ad, bd, idesc_mxf8(kBM, BN, A_MN, B_MN, ks, ks), sf_cols, sf_cols + 4,
-                                     (kb | ks) != 0);
+                            mma_mxf8(d_tmem, ad, bd, idesc_mxf8(kBM, BN, A_MN, B_MN, ks, ks) | a.b_fmt, sf_cols,
+                                     sf_cols + 4, (kb | ks) != 0);
                         }
                     } else {
 #pragma unroll
@@ -923,6 +925,22 @@ static bool tmap_2d(CUtensorMap* m, const void* ptr, int esize, uint64_t inner, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D tensor map of packed E2M1 values [outer, inner] (inner / 2 bytes a row), box {128 values,
+// box_rows}: the TMA unpacks each 8 bytes (16 values) into a 16-byte shared-memory chunk, so a box
+// row lands as 128 bytes with the same 128-byte swizzle as an E4M3 row of 128 values.  The global
+// rows must start on 32-byte boundaries and inner must be a multiple of 128.
+static bool tmap_2d_fp4(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc || inner % 128 != 0 || reinterpret_cast<uintptr_t>(ptr) % 32 != 0) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner / 2};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D tensor map with box {64 bytes, box_rows} and 64-byte swizzle (staged SwiGLU-backward outputs)
 static bool tmap_2d_sw64(CUtensorMap* m, const void* ptr, int esize, uint64_t inner, uint64_t outer,
                          uint32_t box_rows) {
@@ -1090,9 +1108,12 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
         case GemmKind::FwdGateUp:
         case GemmKind::FwdGateUpSaveOnly:
             // 256 weight rows = two [64 gate | 64 up] blocks = 128 I-columns per tile
-            if (!tmap_2d(&ta, b + M.x_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w13_r, 1, H, E * 2 * I, 256) ||
+            if (!tmap_2d(&ta, b + M.x_r, 1, H, R, 128) ||
+                !(L.fp4w ? tmap_2d_fp4(&tb, b + M.w13_r, H, E * 2 * I, 256)
+                         : tmap_2d(&tb, b + M.w13_r, 1, H, E * 2 * I, 256)) ||
                 !tmap_2d_sw64(&td, b + L.gu, 2, 2 * I, R, 32))
                 return cudaErrorInvalidValue;
+            a.b_fmt = L.fp4w ? kFmtE2M1B : 0u;
             a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 128); a.b_rows_e = (int)(2 * I);
             a.sfA = u8(M.x_r_sf); a.sfA_kt = (int)(H / 128);
             a.sfB = u8(M.w13_r_sf); a.sfB_kt = (int)(H / 128);
@@ -1102,9 +1123,11 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
                        ? run<256, false, false, true, false, EPI_SWIGLU, true>(c, ta, tb, a, &td, &td)
                        : run<256, false, false, true, false, EPI_GU_ONLY, true>(c, ta, tb, a, &td, &td);
         case GemmKind::FwdDown:
-            if (!tmap_2d(&ta, b + M.h_r, 1, I, R, 128) || !tmap_2d(&tb, b + M.w2_r, 1, I, E * H, 256) ||
+            if (!tmap_2d(&ta, b + M.h_r, 1, I, R, 128) ||
+                !(L.fp4w ? tmap_2d_fp4(&tb, b + M.w2_r, I, E * H, 256) : tmap_2d(&tb, b + M.w2_r, 1, I, E * H, 256)) ||
                 !tmap_2d_sw64(&tc, b + L.ypart, 2, H, R, 32))
                 return cudaErrorInvalidValue;
+            a.b_fmt = L.fp4w ? kFmtE2M1B : 0u;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 128); a.b_rows_e = (int)H;
             a.sfA = u8(M.h_r_sf); a.sfA_kt = (int)(I / 128);
             a.sfB = u8(M.w2_r_sf); a.sfB_kt = (int)(I / 128);

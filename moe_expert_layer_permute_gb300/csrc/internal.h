@@ -15,8 +15,9 @@ constexpr int kBK = 64;           // bf16 elements of K per pipeline stage (one 
 constexpr int kRouteChunk = 2048; // slots per block of the routing kernels
 constexpr int kMaxExperts = 1024;
 
-// MXFP8 operand copies (E4M3 values + E8M0 scale atoms, see quant.cu): "_r" blocked along the
-// row (K-major use), "_c" blocked along the column (MN-major use).
+// MX operand copies (E4M3 values + E8M0 scale atoms, see quant.cu): "_r" blocked along the
+// row (K-major use), "_c" blocked along the column (MN-major use).  In the FP8 x FP4 forward the
+// weights' _r copies hold packed E2M1 values instead.
 struct MxLayout {
     size_t x_r, x_r_sf, x_c, x_c_sf;      // dispatched x rows [rows, H]
     size_t h_r, h_r_sf;                   // h [rows, I]
@@ -35,7 +36,9 @@ struct Layout {
     size_t ctrl, hist, cnt, off, pad_off, mtile, order, base, perm, inv, pos, row_slot;
     size_t xperm, hid, gu, ypart, dyperm, dg, hw, dtw;
     bool mx_fwd, mx_bwd, mx_on;   // forward / backward GEMMs in MXFP8; either (MXFP8 regions exist)
+    bool fp4w;                    // FP8 x FP4 forward: w13_r / w2_r hold MXFP4 (packed E2M1)
     MxLayout mx;
+    size_t mx_bytes[24];          // byte size of each MxLayout region, in field order (0: absent)
     size_t total;
 };
 
@@ -82,8 +85,10 @@ int bwd_down_bn(int64_t I);
 // the first tiles_dev[0] * 128 rows.  Any of the outputs may be null.  gate_up_I > 0 stores the
 // row-blocked copy of a [E*2I, H] gate/up weight in [64 gate | 64 up] row blocks.
 // With row_slot (padded rows only) source row r is row_slot[r] / k, zero where row_slot[r] < 0.
+// fp4: the row-blocked copy holds MXFP4 (packed E2M1, C / 2 bytes a row) and q_col must be null.
 cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int C, const int* tiles_dev, void* q_row,
-                            void* sf_row, void* q_col, void* sf_col, int gate_up_I, const int* row_slot = nullptr);
+                            void* sf_row, void* q_col, void* sf_col, int gate_up_I, const int* row_slot = nullptr,
+                            bool fp4 = false);
 
 // tracing ids: one per kernel kind; the GEMM kinds follow kTraceGemm (BF16) and kTraceGemmMx
 enum TraceId : int {

@@ -21,6 +21,7 @@
 namespace moe {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+static_assert(sizeof(MxLayout) == 24 * sizeof(size_t), "MxLayout: 12 operands of (values, scales) offsets");
 
 bool make_layout(const moe_desc* d, Layout* L) {
     if (!d) return false;
@@ -31,7 +32,8 @@ bool make_layout(const moe_desc* d, Layout* L) {
     if (rows >= (int64_t)INT32_MAX / 2) return false;
     L->T = d->T; L->H = d->H; L->I = d->I; L->E = d->E; L->k = d->k; L->S = S; L->rows = rows;
     L->nb_route = (S + kRouteChunk - 1) / kRouteChunk;
-    L->mx_fwd = d->precision == MOE_MXFP8;
+    L->fp4w = d->precision == MOE_FP8_FP4;
+    L->mx_fwd = d->precision == MOE_MXFP8 || L->fp4w;
     L->mx_bwd = d->precision == MOE_MXFP8 || d->precision == MOE_FP8_BWD;
     L->mx_on = L->mx_fwd || L->mx_bwd;
     L->n_dtw = 2 * (d->I / (L->mx_bwd ? 128 : bwd_down_bn(d->I)));  // two column halves per n-tile
@@ -59,23 +61,33 @@ bool make_layout(const moe_desc* d, Layout* L) {
     L->hw = take((size_t)rows * d->I * 2);
     L->dtw = take((size_t)rows * L->n_dtw * 4);
     L->mx = MxLayout{};
+    for (size_t& v : L->mx_bytes) v = 0;
     if (L->mx_on) {
         MxLayout& M = L->mx;
         const size_t H = d->H, I = d->I, E = d->E, R = rows;
-        auto q = [&](size_t elems, size_t* data, size_t* sf) { *data = take(elems); *sf = take(elems / 32); };
-        const size_t F = L->mx_fwd ? 1 : 0;   // the forward-only copies are empty without an MXFP8 forward
-        q(F * R * H, &M.x_r, &M.x_r_sf);
-        q(R * H, &M.x_c, &M.x_c_sf);
-        q(F * R * I, &M.h_r, &M.h_r_sf);
-        q(R * H, &M.dy_r, &M.dy_r_sf);
-        q(R * H, &M.dy_c, &M.dy_c_sf);
-        q(R * 2 * I, &M.dg_r, &M.dg_r_sf);
-        q(R * 2 * I, &M.dg_c, &M.dg_c_sf);
-        q(R * I, &M.hw_c, &M.hw_c_sf);
-        q(F * E * 2 * I * H, &M.w13_r, &M.w13_r_sf);
-        q(E * 2 * I * H, &M.w13_c, &M.w13_c_sf);
-        q(F * E * H * I, &M.w2_r, &M.w2_r_sf);
-        q(E * H * I, &M.w2_c, &M.w2_c_sf);
+        // regions in MxLayout field order: the values (vbits bits each), then one scale byte per 32
+        int n = 0;
+        auto q = [&](size_t elems, int vbits, size_t* data, size_t* sf) {
+            L->mx_bytes[n++] = elems * vbits / 8;
+            L->mx_bytes[n++] = elems / 32;
+            *data = take(elems * vbits / 8);
+            *sf = take(elems / 32);
+        };
+        const size_t F = L->mx_fwd ? 1 : 0;   // forward-only copies: empty without an MX forward
+        const size_t B = L->mx_bwd ? 1 : 0;   // backward copies: empty without an MXFP8 backward
+        const int wb = L->fp4w ? 4 : 8;       // bits of the forward weights' values
+        q(F * R * H, 8, &M.x_r, &M.x_r_sf);
+        q(B * R * H, 8, &M.x_c, &M.x_c_sf);
+        q(F * R * I, 8, &M.h_r, &M.h_r_sf);
+        q(B * R * H, 8, &M.dy_r, &M.dy_r_sf);
+        q(B * R * H, 8, &M.dy_c, &M.dy_c_sf);
+        q(B * R * 2 * I, 8, &M.dg_r, &M.dg_r_sf);
+        q(B * R * 2 * I, 8, &M.dg_c, &M.dg_c_sf);
+        q(B * R * I, 8, &M.hw_c, &M.hw_c_sf);
+        q(F * E * 2 * I * H, wb, &M.w13_r, &M.w13_r_sf);
+        q(B * E * 2 * I * H, 8, &M.w13_c, &M.w13_c_sf);
+        q(F * E * H * I, wb, &M.w2_r, &M.w2_r_sf);
+        q(B * E * H * I, 8, &M.w2_c, &M.w2_c_sf);
     }
     L->total = o;
     return true;
@@ -173,7 +185,9 @@ static int check_weight_grad(const moe_tensor* t, int ndim, int64_t a, int64_t b
 static int check_desc_scratch(moe_scratch* s, Layout* L) {
     if (!s) return MOE_ERR_NULL;
     const moe_desc* d = &s->desc;
-    if (d->precision != MOE_BF16 && d->precision != MOE_MXFP8 && d->precision != MOE_FP8_BWD) return MOE_ERR_UNSUPPORTED;
+    if (d->precision != MOE_BF16 && d->precision != MOE_MXFP8 && d->precision != MOE_FP8_BWD &&
+        d->precision != MOE_FP8_FP4)
+        return MOE_ERR_UNSUPPORTED;
     if (!make_layout(d, L)) return MOE_ERR_SHAPE;
     if (!s->data) return MOE_ERR_SCRATCH;
     if (reinterpret_cast<uintptr_t>(s->data) % 256 != 0) return MOE_ERR_SCRATCH;
@@ -203,8 +217,9 @@ static uint64_t weights_tag(const moe_desc* d, const void* w13, const void* w2) 
     return h | 1ull;
 }
 
-// MXFP8 copies of the weights: for an MXFP8 forward W13 blocked along H (gate/up row blocks) and
-// W2 along I; for an MXFP8 backward W13 blocked along 2I and W2 along H.  Skipped when the caller
+// MX copies of the weights: for an MX forward W13 blocked along H (gate/up row blocks) and W2
+// along I, in E4M3 or, for the FP8 x FP4 forward, in E2M1; for an MXFP8 backward W13 blocked
+// along 2I and W2 along H.  Skipped when the caller
 // states the weights are unchanged since the call that made these copies on this scratch
 // (MOE_FLAG_REUSE_WEIGHTS).
 static int mx_weights(const Ctx& c, moe_scratch* s, const void* W13, const void* W2) {
@@ -215,11 +230,12 @@ static int mx_weights(const Ctx& c, moe_scratch* s, const void* W13, const void*
     if (d->flags & MOE_FLAG_REUSE_WEIGHTS) return s->state[1] == tag ? MOE_OK : MOE_ERR_STATE;
     char* b = c.base;
     auto fw = [&](size_t off) { return L.mx_fwd ? b + off : nullptr; };
-    if (launch_mx_quant(c, W13, L.E * 2 * L.I, (int)L.H, nullptr, fw(M.w13_r), fw(M.w13_r_sf), b + M.w13_c,
-                        b + M.w13_c_sf, (int)L.I) != cudaSuccess)
+    auto bw = [&](size_t off) { return L.mx_bwd ? b + off : nullptr; };
+    if (launch_mx_quant(c, W13, L.E * 2 * L.I, (int)L.H, nullptr, fw(M.w13_r), fw(M.w13_r_sf), bw(M.w13_c),
+                        bw(M.w13_c_sf), (int)L.I, nullptr, L.fp4w) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (launch_mx_quant(c, W2, L.E * L.H, (int)L.I, nullptr, fw(M.w2_r), fw(M.w2_r_sf), b + M.w2_c, b + M.w2_c_sf,
-                        0) != cudaSuccess)
+    if (launch_mx_quant(c, W2, L.E * L.H, (int)L.I, nullptr, fw(M.w2_r), fw(M.w2_r_sf), bw(M.w2_c), bw(M.w2_c_sf), 0,
+                        nullptr, L.fp4w) != cudaSuccess)
         return MOE_ERR_CUDA;
     s->state[1] = tag;
     return MOE_OK;
@@ -283,7 +299,8 @@ int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* t
         // token-blocked copy the weight gradient of W13 reads
         const MxLayout& M = L.mx;
         if ((rc = mx_weights(c, scratch, W13->data, W2->data))) return rc;
-        MOE_TRY_CUDA(mx_rows(c, x->data, true, (int)H, M.x_r, M.x_r_sf, save ? M.x_c : 0, save ? M.x_c_sf : 0));
+        const bool xc = save && L.mx_bwd;
+        MOE_TRY_CUDA(mx_rows(c, x->data, true, (int)H, M.x_r, M.x_r_sf, xc ? M.x_c : 0, xc ? M.x_c_sf : 0));
     } else {
         MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, nullptr, nullptr));
     }
@@ -305,6 +322,7 @@ int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_id
     Layout L;
     int rc = check_desc_scratch(scratch, &L);
     if (rc) return rc;
+    if (L.fp4w) return MOE_ERR_UNSUPPORTED;   // the FP8 x FP4 layer is forward only
     const moe_desc* d = &scratch->desc;
     const int64_t T = d->T, H = d->H, I = d->I, E = d->E, k = d->k;
     bool f32_13 = false, f32_2 = false;
@@ -450,11 +468,8 @@ int moe_scratch_view(const moe_desc* desc, int view, uint64_t* offset, uint64_t*
             if (!L.mx_on || view < MOE_VIEW_MX_X_R || view >= MOE_VIEW_MX_END_) return MOE_ERR_SHAPE;
             // MxLayout lists the regions in view order: value array then scales, per operand
             const int i = view - MOE_VIEW_MX_X_R;
-            const uint64_t F = L.mx_fwd ? 1 : 0;   // x_r, h_r, w13_r, w2_r: MXFP8 forward only
-            const uint64_t elems[12] = {F * R * H, R * H,     F * R * I,     R * H,         R * H,     R * 2 * I,
-                                        R * 2 * I, R * I, F * E * 2 * I * H, E * 2 * I * H, F * E * H * I, E * H * I};
             *offset = reinterpret_cast<const size_t*>(&L.mx)[i];
-            *bytes = (i % 2 == 0) ? elems[i / 2] : elems[i / 2] / 32;
+            *bytes = L.mx_bytes[i];
         }
     }
     return MOE_OK;

@@ -1,4 +1,4 @@
-// quant.cu - MXFP8 quantiser: bf16 [R, C] -> E4M3 values with one E8M0 scale per 32 elements.
+// quant.cu - MX quantiser: bf16 [R, C] -> E4M3 (or E2M1) values with one E8M0 scale per 32 elements.
 //
 // MXFP8 operands (Blackwell only, per ic.work analysis, section "算子下沉时代的硬件死锁暗礁") follow
 // the OCP Microscaling v1.0 rule: a block of 32 values shares the exponent
@@ -16,6 +16,9 @@
 // 16*(m % 32) + 4*((m / 32) % 4) + (b % 4); atom (mn / 128, kb / 4) at
 // ((mn / 128) * (K / 128) + kb / 4) * 512.  For row blocks MN = rows, K = C; for col blocks
 // MN = columns, K = R.
+// FP4 (row blocks only, weights of the FP8 x FP4 forward): E2M1 values with the block exponent
+// floor(log2(amax)) - 2, rounded to nearest even and saturated to +-6, two per byte (the even
+// column in the low nibble), rows of C / 2 bytes; the scales are laid out as above.
 // Optionally the row-blocked output permutes rows within each expert's [2I, H] gate/up matrix so
 // that every 128-row block holds 64 gate rows followed by the 64 up rows of the same I columns.
 // With a row map (row_slot, k) the quantiser is also the dispatch: output row r takes source row
@@ -44,10 +47,21 @@ __device__ __forceinline__ uint2 e4m3x8(uint4 w, float inv) {
     return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
+// 8 bf16 (one uint4) scaled by inv into 8 E2M1 nibbles (one 32-bit word, element 0 lowest)
+__device__ __forceinline__ uint32_t e2m1x8(uint4 w, float inv) {
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t p = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        p |= to_e2m1x2(__uint_as_float(in[i] << 16) * inv, __uint_as_float(in[i] & 0xFFFF0000u) * inv) << (8 * i);
+    return p;
+}
+
 // grid: (C / 128, R_max / 128); one block quantises a 128 x 128 tile in four passes of 32 rows.
 // Its row-blocked scales (128 rows x 4 column blocks) and column-blocked scales (128 columns x 4
 // row blocks) are each exactly one 512-byte atom: staged in shared memory and written with 16-byte
 // stores.  tiles_dev (optional): device count of valid 128-row tiles.
+template <bool FP4>
 __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16* __restrict__ src, long long R_max,
                                                              int C, const int* __restrict__ tiles_dev,
                                                              uint8_t* __restrict__ q_row, uint8_t* __restrict__ sf_row,
@@ -101,7 +115,8 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
             }
             uint8_t sf;
             float inv;
-            mx_scale_bits(absmax_to_f32_bits(m2), &sf, &inv);
+            if constexpr (FP4) mx_scale_bits_e2m1(absmax_to_f32_bits(m2), &sf, &inv);
+            else mx_scale_bits(absmax_to_f32_bits(m2), &sf, &inv);
             long long r = r0 + rr;
             if (gate_up_I > 0) {  // 128-row blocks of [64 gate rows | 64 up rows] per expert
                 const long long e = r / (2 * gate_up_I), j = r % (2 * gate_up_I);
@@ -111,14 +126,21 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
             } else {
                 s_sfr[16 * rr + 4 * sub + b] = sf;                  // row 32 sub + rr of the atom
             }
-            uint2 o[4];
+            if constexpr (FP4) {
+                uint32_t o[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) o[q] = e4m3x8(w[q], inv);
-            uint4* dst = reinterpret_cast<uint4*>(q_row + r * C + c0 + 32 * b);
-            dst[0] = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
-            dst[1] = make_uint4(o[2].x, o[2].y, o[3].x, o[3].y);
+                for (int q = 0; q < 4; ++q) o[q] = e2m1x8(w[q], inv);
+                *reinterpret_cast<uint4*>(q_row + r * (C / 2) + (c0 + 32 * b) / 2) = make_uint4(o[0], o[1], o[2], o[3]);
+            } else {
+                uint2 o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) o[q] = e4m3x8(w[q], inv);
+                uint4* dst = reinterpret_cast<uint4*>(q_row + r * C + c0 + 32 * b);
+                dst[0] = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
+                dst[1] = make_uint4(o[2].x, o[2].y, o[3].x, o[3].y);
+            }
         }
-        if (q_col) {
+        if (!FP4 && q_col) {
             // thread -> column t: 32 rows of one column
             uint32_t m = 0;
             uint32_t v[32];
@@ -149,17 +171,19 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
     // the tile's two scale atoms, 16 bytes per thread
     if (q_row && gate_up_I <= 0 && t < 32)
         reinterpret_cast<uint4*>(sf_row + sf_index(rt, c0 >> 5, C / 128))[t] = reinterpret_cast<const uint4*>(s_sfr)[t];
-    if (q_col && t >= 32 && t < 64)
+    if (!FP4 && q_col && t >= 32 && t < 64)
         reinterpret_cast<uint4*>(sf_col + sf_index(c0, rt >> 5, R_max / 128))[t - 32] =
             reinterpret_cast<const uint4*>(s_sfc)[t - 32];
 }
 
 cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int C, const int* tiles_dev, void* q_row,
-                            void* sf_row, void* q_col, void* sf_col, int gate_up_I, const int* row_slot) {
+                            void* sf_row, void* q_col, void* sf_col, int gate_up_I, const int* row_slot, bool fp4) {
     if (R_max <= 0) return cudaSuccess;
+    if (fp4 && (q_col || !q_row)) return cudaErrorInvalidValue;   // MXFP4 copies are row-blocked only
     dim3 grid(C / kQCols, (unsigned)(R_max / 128));
+    auto kern = fp4 ? mx_quant_kernel<true> : mx_quant_kernel<false>;
     trace_begin(c.st, kTraceQuant);
-    mx_quant_kernel<<<grid, kQThreads, 0, c.st>>>(
+    kern<<<grid, kQThreads, 0, c.st>>>(
         reinterpret_cast<const __nv_bfloat16*>(src), R_max, C, tiles_dev, reinterpret_cast<uint8_t*>(q_row),
         reinterpret_cast<uint8_t*>(sf_row), reinterpret_cast<uint8_t*>(q_col), reinterpret_cast<uint8_t*>(sf_col),
         gate_up_I, row_slot, (int)c.L->k);

@@ -38,7 +38,8 @@ class LayerConfig:
     I: int
     E: int
     k: int
-    precision: str = "bf16"          # "bf16", "mxfp8" or "fp8_bwd" (BF16 forward, MXFP8 backward)
+    precision: str = "bf16"          # "bf16", "mxfp8", "fp8_bwd" (BF16 forward, MXFP8 backward) or
+                                     # "fp8_fp4" (forward only: MXFP8 activations x MXFP4 weights)
     routing: str = "uniform"         # "uniform" or "zipf"
     seed: int = 1000
     zipf_s: float = 1.2
@@ -62,6 +63,8 @@ CONFIGS = {
                                        precision="mxfp8", seed=1001),
     "qwen3_30b_a3b_fp8_bwd": LayerConfig("qwen3_30b_a3b_fp8_bwd", T=16384, H=2048, I=768, E=128, k=8,
                                          precision="fp8_bwd", seed=1001),
+    "qwen3_30b_a3b_fp8_fp4": LayerConfig("qwen3_30b_a3b_fp8_fp4", T=16384, H=2048, I=768, E=128, k=8,
+                                         precision="fp8_fp4", seed=1001),
     "qwen3_235b_a22b": LayerConfig("qwen3_235b_a22b", T=16384, H=4096, I=1536, E=128, k=8, seed=1003),
     "qwen3_235b_a22b_mxfp8": LayerConfig("qwen3_235b_a22b_mxfp8", T=16384, H=4096, I=1536, E=128, k=8,
                                          precision="mxfp8", seed=1003),

@@ -200,8 +200,8 @@ def forward(x, topk_idx, topk_w, W13, W2, *, mxfp8: bool = False, fp8_fp4: bool 
 
     Evaluated per expert group in sorted (routed) order.  With keep=True also returns the
     intermediates in sorted order: X_perm, g, u, h, o (and the routing dict).  fp8_fp4: the FP8 x
-    FP4 forward the pages list for DeepGEMM's Mega MoE (wire.sakhanda.co, section "Как се
-    сравнява с други слети MoE опции?", comparison table), read as MXFP8 activations (X, h) times
+    FP4 forward the pages list for DeepGEMM's Mega MoE (wire.sakhanda.co, "Prime Intellect пусна
+    Prime Mega MoE", section "Как се сравнява с други слети MoE опции?", data types row), read as MXFP8 activations (X, h) times
     MXFP4 weights (W13, W2), each blocked along its contraction.
     """
     if fp8_fp4:

@@ -41,7 +41,8 @@ class DeviceLayer:
         self.dW13 = torch.full((E, 2 * I, H), float("nan"), dtype=wgrad_dtype, device=dev)
         self.dW2 = torch.full((E, H, I), float("nan"), dtype=wgrad_dtype, device=dev)
         self.dtw = torch.full((T, k), float("nan"), dtype=torch.float32, device=dev)
-        prec = {"bf16": bd.MOE_BF16, "mxfp8": bd.MOE_MXFP8, "fp8_bwd": bd.MOE_FP8_BWD}[cfg.precision]
+        prec = {"bf16": bd.MOE_BF16, "mxfp8": bd.MOE_MXFP8, "fp8_bwd": bd.MOE_FP8_BWD,
+                "fp8_fp4": bd.MOE_FP8_FP4}[cfg.precision]
         self.scratch = bd.Scratch(T, H, I, E, k, precision=prec, device=dev)
 
     def fwd(self, flags=0):
@@ -90,3 +91,26 @@ def decode_mx(q: np.ndarray, sf: np.ndarray, along: str) -> np.ndarray:
     else:
         idx = sf_index(c, r // 32, R // 128)
     return vals * np.ldexp(1.0, sf[idx].astype(np.int64) - 127)
+
+
+# ---- MXFP4 decoding (E2M1 code table from its bit fields: 1 sign, 2 exponent (bias 1), 1 mantissa)
+def e2m1_table() -> np.ndarray:
+    tab = np.zeros(16)
+    for code in range(16):
+        sg, ex, m = code >> 3, (code >> 1) & 3, code & 1
+        v = m * 0.5 if ex == 0 else (1 + m / 2.0) * 2.0 ** (ex - 1)
+        tab[code] = -v if sg else v
+    return tab
+
+
+def decode_mxfp4_rows(q: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    """Dequantise packed E2M1 [R, C/2] (the even column in the low nibble) with row-blocked scale
+    atoms (blocks of 32 columns) into fp64 [R, C]."""
+    R, half = q.shape
+    C = 2 * half
+    codes = np.empty((R, C), dtype=np.int64)
+    codes[:, 0::2] = q & 0xF
+    codes[:, 1::2] = q >> 4
+    r = np.arange(R)[:, None]
+    c = np.arange(C)[None, :]
+    return e2m1_table()[codes] * np.ldexp(1.0, sf[sf_index(r, c // 32, C // 128)].astype(np.int64) - 127)

@@ -182,6 +182,39 @@ def test_fp8_bwd_layout_has_only_the_backward_mxfp8_copies(bd):
     assert bd.moe_scratch_bytes(b) < bd.moe_scratch_bytes(d) < bd.moe_scratch_bytes(m)
 
 
+def test_fp8_fp4_layout_has_only_the_forward_copies_with_packed_weights(bd):
+    """FP8 x FP4 (forward only): no backward copies; the weights' values take half the bytes of
+    their E4M3 copies (two E2M1 values a byte), their scales the same bytes."""
+    d = bd.make_desc(2048, 512, 256, 16, 4, bd.MOE_FP8_FP4)
+    m = bd.make_desc(2048, 512, 256, 16, 4, bd.MOE_MXFP8)
+    for name in ("x_c", "dy_r", "dy_c", "dg_r", "dg_c", "hw_c", "w13_c", "w2_c"):
+        assert bd.view_span(d, bd.MX_VIEWS[name])[1] == 0, name
+        assert bd.view_span(d, bd.MX_VIEWS[name + "_sf"])[1] == 0, name
+    for name in ("x_r", "h_r"):
+        assert bd.view_span(d, bd.MX_VIEWS[name])[1] == bd.view_span(m, bd.MX_VIEWS[name])[1] > 0, name
+    for name in ("w13_r", "w2_r"):
+        assert 2 * bd.view_span(d, bd.MX_VIEWS[name])[1] == bd.view_span(m, bd.MX_VIEWS[name])[1] > 0, name
+        assert bd.view_span(d, bd.MX_VIEWS[name + "_sf"])[1] == bd.view_span(m, bd.MX_VIEWS[name + "_sf"])[1]
+        off, n = bd.view_span(d, bd.MX_VIEWS[name])
+        assert off % 32 == 0 and n > 0      # packed rows are read by 32-byte aligned tensor maps
+    assert bd.moe_scratch_bytes(d) < bd.moe_scratch_bytes(m)
+
+
+def test_fp8_fp4_backward_is_refused_before_any_launch(bd):
+    f = _Fake(bd)
+    T, H, I, E, k = 256, 256, 128, 8, 2
+    B16, I32, F32 = bd.MOE_DT_BF16, bd.MOE_DT_I32, bd.MOE_DT_F32
+    args = [f.t((T, H), B16), f.t((T, H), B16), f.t((T, k), I32), f.t((T, k), F32), f.t((E, 2 * I, H), B16),
+            f.t((E, H, I), B16), f.t((T, H), B16), f.t((E, 2 * I, H), F32), f.t((E, H, I), F32), f.t((T, k), F32)]
+    s = bd.MoeScratch()
+    s.desc = bd.make_desc(T, H, I, E, k, bd.MOE_FP8_FP4)
+    s.bytes = bd.moe_scratch_bytes(s.desc)
+    s.data = 1 << 40
+    assert bd.LIB.moe_bwd(*[ctypes.byref(a) for a in args], ctypes.byref(s), None) == bd.ERR["MOE_ERR_UNSUPPORTED"]
+    s.desc = bd.make_desc(T, H, I, E, k, 4)     # no such precision
+    assert bd.LIB.moe_bwd(*[ctypes.byref(a) for a in args], ctypes.byref(s), None) == bd.ERR["MOE_ERR_UNSUPPORTED"]
+
+
 def test_router_argument_checks(bd):
     """Every bad argument of the router entry points is refused before any launch (no GPU)."""
     f = _Fake(bd)

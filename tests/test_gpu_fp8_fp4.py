@@ -1,0 +1,165 @@
+"""FP8 x FP4 forward (MXFP8 activations times MXFP4 weights, the data types the pages list for
+DeepGEMM's Mega MoE) against the fp64 oracle in the same mode.
+
+Bar: the MXFP4 weight copies decode exactly to the oracle's E2M1 quantise-dequantise of the same
+bf16 weights, and the E4M3 activation copy to its E4M3 one; y within a relative Frobenius error
+of 3e-2 of the oracle (the h quantisation decides in fp32 on the device and in fp64 in the
+oracle), and closer to the FP8 x FP4 oracle than to the MXFP8 one.  The backward is not offered:
+moe_bwd answers MOE_ERR_UNSUPPORTED."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_expert_layer_permute_gb300 import inputs as gen
+
+from _layer import DeviceLayer, decode_mx, decode_mxfp4_rows, f64, rel_fro
+
+pytestmark = pytest.mark.gpu
+TOL = 3e-2
+
+
+def fp4(cfg):
+    return dataclasses.replace(cfg, precision="fp8_fp4", name=cfg.name + "_fp4")
+
+
+SMALL = {
+    "tiny": fp4(gen.CONFIGS["tiny"]),
+    "medium": fp4(gen.custom_config("medium", T=2048, H=512, I=256, E=16, k=4, seed=21)),
+    "medium_I384": fp4(gen.custom_config("medium_I384", T=1500, H=768, I=384, E=12, k=3, seed=22)),
+    "skew_small": fp4(gen.custom_config("skew_small", T=1024, H=256, I=128, E=32, k=8, routing="zipf", seed=23)),
+}
+
+
+def _args(inp):
+    return inp.f64("x"), inp.topk_idx, inp.f64("topk_w"), inp.f64("W13"), inp.f64("W2")
+
+
+def test_quantiser_matches_oracle_bit_exact(cuda_lib):
+    bd = cuda_lib
+    inp = gen.make_inputs(SMALL["medium"])
+    cfg = inp.cfg
+    L = DeviceLayer(bd, inp)
+    L.fwd()
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    H, I, E = cfg.H, cfg.I, cfg.E
+    sfv = lambda n: L.view(bd.MX_VIEWS[n], torch.uint8, (-1,)).cpu().numpy()   # noqa: E731
+    # W13: E2M1 along H, stored in 128-row blocks of [64 gate | 64 up]
+    q = L.view(bd.MX_VIEWS["w13_r"], torch.uint8, (E * 2 * I, H // 2)).cpu().numpy()
+    dq = decode_mxfp4_rows(q, sfv("w13_r_sf")).reshape(E, 2 * I // 128, 2, 64, H)
+    ref = oracle.mx_qdq(inp.f64("W13"), axis=2, fmt="e2m1")
+    np.testing.assert_array_equal(dq[:, :, 0].reshape(E, I, H), ref[:, :I])
+    np.testing.assert_array_equal(dq[:, :, 1].reshape(E, I, H), ref[:, I:])
+    # W2: E2M1 along I
+    q = L.view(bd.MX_VIEWS["w2_r"], torch.uint8, (E * H, I // 2)).cpu().numpy()
+    np.testing.assert_array_equal(decode_mxfp4_rows(q, sfv("w2_r_sf")).reshape(E, H, I),
+                                  oracle.mx_qdq(inp.f64("W2"), axis=2, fmt="e2m1"))
+    # the dispatched activations stay E4M3 along H
+    r = oracle.route(inp.topk_idx, E)
+    pad = L.view(bd.MOE_VIEW_PAD_OFFSETS, torch.int32, (E + 1,)).cpu().numpy()
+    prow = np.concatenate([pad[e] + np.arange(r["off"][e + 1] - r["off"][e]) for e in range(E)])
+    q = L.view(bd.MX_VIEWS["x_r"], torch.uint8, (L.rows(), H)).cpu().numpy()
+    X = inp.f64("x")[r["perm"] // cfg.k]
+    np.testing.assert_array_equal(decode_mx(q, sfv("x_r_sf"), "row")[prow], oracle.mx_qdq(X, axis=1))
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward(cuda_lib, name):
+    inp = gen.make_inputs(SMALL[name])
+    L = DeviceLayer(cuda_lib, inp)
+    L.fwd()
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    y_ref = oracle.forward(*_args(inp), fp8_fp4=True)
+    err = rel_fro(f64(L.y), y_ref)
+    assert err < TOL, err
+    # FP4 weights really were used: far closer to this oracle than to the MXFP8 one
+    assert err < 0.5 * rel_fro(f64(L.y), oracle.forward(*_args(inp), mxfp8=True))
+
+
+def test_backward_is_unsupported(cuda_lib):
+    inp = gen.make_inputs(SMALL["tiny"])
+    L = DeviceLayer(cuda_lib, inp)
+    L.fwd(flags=cuda_lib.MOE_FLAG_SAVE_GU)
+    with pytest.raises(cuda_lib.MoeError) as ei:
+        L.bwd(flags=cuda_lib.MOE_FLAG_REUSE_FWD)
+    assert ei.value.code == cuda_lib.ERR["MOE_ERR_UNSUPPORTED"]
+    torch.cuda.synchronize()
+    assert L.status() == 0
+
+
+def test_weight_reuse_is_exact_and_checked(cuda_lib):
+    bd = cuda_lib
+    inp = gen.make_inputs(SMALL["medium"])
+    L = DeviceLayer(bd, inp)
+    L.fwd()
+    y0 = L.y.clone()
+    L.fwd(flags=bd.MOE_FLAG_REUSE_WEIGHTS)
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    assert torch.equal(L.y, y0)
+    W13b = L.W13.clone()
+    L.W13 = W13b   # other weights: the saved copies no longer match
+    with pytest.raises(bd.MoeError):
+        L.fwd(flags=bd.MOE_FLAG_REUSE_WEIGHTS)
+
+
+def _edge_inputs(case):
+    mk = lambda **kw: fp4(gen.custom_config(**kw))   # noqa: E731
+    if case == "one_token":
+        return gen.make_inputs(mk(T=1, H=256, I=128, E=8, k=2, seed=31))
+    if case == "all_on_one_expert":
+        inp = gen.make_inputs(mk(T=300, H=256, I=128, E=8, k=1, seed=32))
+        inp.topk_idx = np.full((300, 1), 5, dtype=np.int32)
+        return inp
+    if case == "empty_experts":
+        inp = gen.make_inputs(mk(T=400, H=256, I=256, E=16, k=2, seed=33))
+        inp.topk_idx = np.ascontiguousarray(np.stack([np.arange(400) % 3, 7 + np.arange(400) % 2], 1).astype(np.int32))
+        return inp
+    if case == "single_expert_top1":
+        return gen.make_inputs(mk(T=200, H=256, I=128, E=1, k=1, seed=34))
+    if case == "zero_weight_block":
+        inp = gen.make_inputs(mk(T=200, H=256, I=128, E=4, k=2, seed=37))
+        inp.W13[1, :, 32:64] = 0          # whole blocks of 32 along H are zero: scale byte 0
+        inp.W2[2, :, :32] = 0
+        return inp
+    return gen.make_inputs(mk(T=20, H=512, I=256, E=4, k=2, seed=35))     # fewer rows than a tile
+
+
+@pytest.mark.parametrize("case", ["one_token", "all_on_one_expert", "empty_experts", "single_expert_top1",
+                                  "zero_weight_block", "fewer_rows_than_a_tile"])
+def test_edge_cases(cuda_lib, case):
+    inp = _edge_inputs(case)
+    L = DeviceLayer(cuda_lib, inp)
+    L.fwd()
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    assert rel_fro(f64(L.y), oracle.forward(*_args(inp), fp8_fp4=True)) < TOL
+
+
+def test_zero_tokens(cuda_lib):
+    inp = gen.make_inputs(fp4(gen.custom_config(T=0, H=256, I=128, E=8, k=2, seed=36)))
+    L = DeviceLayer(cuda_lib, inp)
+    L.fwd()
+    torch.cuda.synchronize()
+    assert L.status() == 0 and L.y.numel() == 0
+
+
+def test_full_size_sampled(cuda_lib):
+    cfg = gen.CONFIGS["qwen3_30b_a3b_fp8_fp4"]
+    inp = gen.make_inputs(cfg)
+    L = DeviceLayer(cuda_lib, inp)
+    L.fwd()
+    L.fwd(flags=cuda_lib.MOE_FLAG_REUSE_WEIGHTS)
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    rng = np.random.default_rng(3)
+    toks = np.sort(rng.choice(cfg.T, 8, replace=False))
+    ti = torch.from_numpy(toks).cuda()
+    y_s = oracle.forward_tokens(inp.f32("x"), inp.topk_idx, inp.topk_w, inp.f32("W13"), inp.f32("W2"), toks,
+                                fp8_fp4=True)
+    assert rel_fro(f64(L.y[ti]), y_s) < TOL
+    assert torch.isfinite(L.y).all()
