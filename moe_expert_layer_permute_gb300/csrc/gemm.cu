@@ -393,6 +393,9 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool ok = true;
+            // bytes one stage's copies complete: a packed-E2M1 B tile counts the bytes it reads
+            // (half a byte a value) although it lands in shared memory as a byte a value
+            const uint32_t stage_tx = kStageBytes - (a.b_fmt ? kBTileBytes / 2 : 0);
             for (int L = unit0; L < num_tiles && ok; L += unit_stride) {
                 const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
                 // first B row of the tile (K-major B); MXFP8 gate/up weights are stored with
@@ -428,7 +431,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         if (++stage == kStages) { stage = 0; phase ^= 1u; }
                         continue;
                     }
-                    mbar_arrive_expect_tx(full + stage, kStageBytes);
+                    mbar_arrive_expect_tx(full + stage, stage_tx);
                     if (!A_MN) {
                         tma_load_2d(dA, &tmA, full + stage, k0, t.m0);
                     } else {
