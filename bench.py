@@ -327,6 +327,81 @@ def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
     return out
 
 
+def fwd_measure(bd, gen, cfg, steps, warmup, ws, local, peak, peak_src):
+    """The forward alone in a forward-only precision (FP8 x FP4): per call with the weights
+    quantised in the call, and with the copies made once (MOE_FLAG_REUSE_WEIGHTS, fixed weights as
+    when serving); per-kernel times of the latter and the roofline of its dominant GEMM."""
+    import numpy as np
+    import torch
+
+    dev = torch.device("cuda", local)
+    inp = gen.make_inputs(cfg)
+
+    def host(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a))
+
+    d = {n: host(getattr(inp, n)).to(dev) for n in ("x", "topk_idx", "topk_w", "W13", "W2")}
+    del inp
+    d["y"] = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    prec = {"fp8_fp4": bd.MOE_FP8_FP4, "mxfp8": bd.MOE_MXFP8}[cfg.precision]
+    sc = bd.Scratch(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, precision=prec, device=dev)
+    stream = torch.cuda.current_stream()
+    RW = bd.MOE_FLAG_REUSE_WEIGHTS
+
+    def fwd(flags=0):
+        bd.moe_fwd(d["x"], d["topk_idx"], d["topk_w"], d["W13"], d["W2"], d["y"], sc, flags=flags)
+
+    def timed(fn, n):
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        return allreduce_max(e0.elapsed_time(e1), ws)
+
+    fwd()
+    for _ in range(max(3, warmup)):
+        fwd(RW)
+    torch.cuda.synchronize()
+    if bd.moe_read_device_status(sc) != 0:
+        raise RuntimeError("device status word set during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    q_ms = timed(fwd, steps) / steps
+    r_ms = timed(lambda: fwd(RW), steps) / steps
+    bd.moe_trace_reset()
+    bd.moe_trace_enable(True)
+    traced = max(3, min(steps, 50))
+    timed(lambda: fwd(RW), traced)
+    bd.moe_trace_enable(False)
+    kern = bd.moe_trace_read()
+    clk = clocks.stop()
+    status = bd.moe_read_device_status(sc)
+    del d, sc
+    torch.cuda.empty_cache()
+    fl = cfg.fwd_flops()
+    shf = float(cfg.S) * cfg.H * cfg.I
+    total = sum(v[1] for v in kern.values())
+    rows = {n: {"launches": c, "avg_ms": ms / c, "share": ms / total if total else None} for n, (c, ms) in kern.items()}
+    gemms = {n: v for n, v in rows.items() if n.replace("gemm_mx_", "gemm_") in GEMM_FLOPS}
+    top = max(gemms, key=lambda n: gemms[n]["avg_ms"] * gemms[n]["launches"])
+    ach = GEMM_FLOPS[top.replace("gemm_mx_", "gemm_")] * shf / (gemms[top]["avg_ms"] * 1e-3) / 1e12
+    return {"workload": cfg.name, "fwd_ms": q_ms, "fwd_ms_reuse_weights": r_ms,
+            "fwd_tflops": fl / (q_ms * 1e-3) / 1e12, "fwd_tflops_reuse_weights": fl / (r_ms * 1e-3) / 1e12,
+            "frac_of_peak_reuse_weights": fl / (r_ms * 1e-3) / 1e12 / peak,
+            "peak_tflops": {"value": peak, "source": peak_src},
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                         "traffic": None, "kernel": top, "peak_source": peak_src},
+            "gpu_launches_per_fwd": int(sum(v[0] for v in kern.values()) // traced),
+            "kernels": rows, "clocks": clk, "device_status": status}
+
+
 def router_measure(bd, gen, cfg, reps, hbm_peak):
     """The router before the layer (top-k + softmax over the selected, and its backward) on the
     workload's T x E logits.  One timed iteration is a CUDA graph of NB launches over NB distinct
@@ -470,6 +545,17 @@ def run_ours(args, rank, ws, local):
         fs["workload"] = fcfg.name
         fs["peak_tflops"] = {"value": blend_peak, "source": fsrc}
         line["fp8_bwd"] = fs
+    if not args.no_mx and cfg.precision == "bf16" and args.config + "_fp8_fp4" in gen.CONFIGS:
+        # the forward-only FP8 x FP4 layer (E4M3 activations x E2M1 weights run at the FP8 rate),
+        # beside the MXFP8 forward with its weight copies made once too
+        psrc = f"{src} bf16_tflops_sustained x 2 (nominal FP8:BF16 ratio; kind::mxf8f6f4 runs E2M1 at it)"
+        f4 = fwd_measure(bd, gen, gen.CONFIGS[args.config + "_fp8_fp4"], args.steps, args.warmup, ws, local,
+                         mx_peak, psrc)
+        if args.config + "_mxfp8" in gen.CONFIGS:
+            f8 = fwd_measure(bd, gen, gen.CONFIGS[args.config + "_mxfp8"], args.steps, args.warmup, ws, local,
+                             mx_peak, psrc)
+            f4["mxfp8_fwd_ms_reuse_weights"] = f8["fwd_ms_reuse_weights"]
+        line["fp8_fp4_fwd"] = f4
     # the router that precedes the layer (outside the layer step, as in the pages' benchmark)
     line["router"] = router_measure(bd, gen, cfg, 20, peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
