@@ -63,18 +63,11 @@ constexpr bool tma_out() {
 // boxes would not fit beside the ring
 template <int EPI, bool SINGLE>
 constexpr int out_box_bytes() { return (EPI == EPI_SWIGLU_BWD || SINGLE) ? 2048 : 4096; }
-// staging boxes per epilogue warp, used in rotation: the MXFP8 weight gradients (128 x 128 tiles,
-// fp32 rows: four boxes a tile) get four, so that a tile's stores stream out back to back
-// instead of each waiting for the previous box to be read out; the others keep one
-template <int EPI, bool MX, int BN>
-constexpr int out_boxes() { return (MX && BN == 128 && EPI == EPI_WGRAD) ? 4 : 1; }
 
 // ---- staged TMA stores: one 32-row x 128-byte box per epilogue warp, row = lane ----------------
-// waits until the warp's box stored PENDING stores ago (with a ring of PENDING + 1 boxes: the
-// box about to be rewritten) has been read out by its TMA store
-template <int PENDING = 0>
+// waits until the warp's previous box has been read out by its TMA store
 __device__ __forceinline__ void box_acquire(int lane) {
-    if (lane == 0) bulk_wait_read<PENDING>();
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
 }
 // 16-byte chunk `chunk` of the lane's row, 128-byte swizzle (the box is 1024-byte aligned)
@@ -334,8 +327,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     // columns, 128-byte swizzle) in shared memory and writes them with a TMA store (tmC; tmD for the
     // saved [g|u]), so that L2 receives whole lines rather than 16-byte halves of sectors
     constexpr bool kTmaOut = tma_out<EPI, MX, BN>();
-    constexpr int kOutBoxes = out_boxes<EPI, MX, BN>();
-    constexpr int kOutBytes = kTmaOut ? kEpiWarps * kOutBoxes * out_box_bytes<EPI, kSingle>() : 0;
+    constexpr int kOutBytes = kTmaOut ? kEpiWarps * out_box_bytes<EPI, kSingle>() : 0;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -630,7 +622,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         int acc = 0;
         uint32_t acc_phase = 0;
-        int ring = 0;   // next box of the warp's staging ring (the box stored kOutBoxes stores ago)
         for (int L = unit0; L < num_tiles; L += unit_stride) {
             const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
             if (!mbar_wait(tfull + acc, acc_phase, abort_flag, a.status)) break;
@@ -660,7 +651,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             if (!t.valid) {
                 // duplicate tile of a CTA pair: nothing to store
             } else if constexpr (kTmaOut && EPI != EPI_SWIGLU_BWD) {
-                uint8_t* box = sOut + (warp - 2) * kOutBoxes * 4096;
+                uint8_t* box = sOut + (warp - 2) * 4096;
                 const uint32_t sbox = smem_u32(box);
                 const int brow = t.m0 + 32 * quarter;   // first row of the warp's boxes
                 if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
@@ -697,29 +688,23 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 } else if constexpr (EPI == EPI_WGRAD) {
                     // rows of this expert's block of the weight gradient [E * M, N]
                     const int orow = t.e * a.m_tiles * kBM + brow;
-                    // each box is the next of the warp's ring: the one rewritten was stored
-                    // kOutBoxes stores ago, and at most kOutBoxes - 1 later stores may still read
                     if (a.out_f32) {
 #pragma unroll 1
                         for (int b = 0; b < BN / 32; ++b) {
-                            const int rb = ring;
-                            ring = ring + 1 == kOutBoxes ? 0 : ring + 1;
-                            box_acquire<kOutBoxes - 1>(lane);
+                            box_acquire(lane);
                             if (t.kb > 0) {
                                 tmem_ld32(tacc + 32 * b, v);
                             } else {
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) v[j] = 0.f;
                             }
-                            box_put_f32x32(sbox + rb * 4096, lane, v);
-                            box_store(&tmC, box + rb * 4096, lane, t.n0 + 32 * b, orow);
+                            box_put_f32x32(sbox, lane, v);
+                            box_store(&tmC, box, lane, t.n0 + 32 * b, orow);
                         }
                     } else {
 #pragma unroll 1
                         for (int b = 0; b < BN / 64; ++b) {
-                            const int rb = ring;
-                            ring = ring + 1 == kOutBoxes ? 0 : ring + 1;
-                            box_acquire<kOutBoxes - 1>(lane);
+                            box_acquire(lane);
 #pragma unroll 1
                             for (int h = 0; h < 2; ++h) {
                                 if (t.kb > 0) {
@@ -728,9 +713,9 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
 #pragma unroll
                                     for (int j = 0; j < 32; ++j) v[j] = 0.f;
                                 }
-                                box_put_bf16x32(sbox + rb * 4096, lane, h, v, 1.f);
+                                box_put_bf16x32(sbox, lane, h, v, 1.f);
                             }
-                            box_store(&tmC, box + rb * 4096, lane, t.n0 + 64 * b, orow);
+                            box_store(&tmC, box, lane, t.n0 + 64 * b, orow);
                         }
                     }
                 } else {   // EPI_WEIGHTED, EPI_PLAIN: one bf16 row block
@@ -994,10 +979,9 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR, TWO>;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
-    const size_t out_bytes = tma_out<EPI, MX, BN>() ? (size_t)epi_warps<EPI, MX && BN == 256>() *
-                                                          out_boxes<EPI, MX, BN>() *
-                                                          out_box_bytes<EPI, MX && BN == 256>()
-                                                    : 0;
+    const size_t out_bytes = tma_out<EPI, MX, BN>()
+                                 ? (size_t)epi_warps<EPI, MX && BN == 256>() * out_box_bytes<EPI, MX && BN == 256>()
+                                 : 0;
     const size_t fixed = 1024 + ring_stages<TWO>() * stage + out_bytes + 256;
     if (tma_out<EPI, MX, BN>() && !tc) return cudaErrorInvalidValue;
     const CUtensorMap& tcm = tc ? *tc : ta;   // kernels without a TMA-stored output never read it
