@@ -1159,32 +1159,27 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.sfB = u8(M.w13_c_sf); a.sfB_kt = (int)(E * 2 * I / 128);
             a.out0 = b + L.ypart; a.ld0 = (int)H;
             return run<256, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a, &tc);
-        case GemmKind::WgradDown: {
-            // weight gradients in 128 x 256 tiles where N allows (one accumulator, drained to
-            // registers; a 128 x 128 MXFP8 MMA reads its operands from shared memory about as
-            // fast as the SM can deliver them), else 128 x 128 with two; a pair shares B
-            const int bn = (I % 256 == 0) ? 256 : 128;
-            // B box: a whole 128-row K slice per MN chunk when each CTA of the pair loads one of
-            // two chunks (BN = 256), half of it when the pair splits one chunk's K rows
-            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, bn == 256 ? 128 : 64) ||
+        case GemmKind::WgradDown:
+            // weight gradients keep 128 x 128 tiles with two accumulators: their contraction over an
+            // expert's rows is short, so a drained single accumulator would stall the MMAs, and the
+            // fp32 output stores need the epilogue to overlap the next tile; a pair splits B's K rows
+            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 64) ||
                 !tmap_2d(&tc, out, oes, I, E * H, 32))
                 return cudaErrorInvalidValue;
-            a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / bn);
+            a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / 128);
             a.sfA = u8(M.dy_c_sf); a.sfA_kt = (int)(R / 128);
             a.sfB = u8(M.hw_c_sf); a.sfB_kt = (int)(R / 128);
             a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
-            return bn == 256 ? run<256, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc)
-                             : run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
-        }
+            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
         case GemmKind::WgradGateUp:
-            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 128) ||
+            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 64) ||
                 !tmap_2d(&tc, out, oes, H, E * 2 * I, 32))
                 return cudaErrorInvalidValue;
-            a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 256);
+            a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 128);
             a.sfA = u8(M.dg_c_sf); a.sfA_kt = (int)(R / 128);
             a.sfB = u8(M.x_c_sf); a.sfB_kt = (int)(R / 128);
             a.out0 = out; a.ld0 = (int)H; a.out_e_stride = 2 * I * H;
-            return run<256, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
+            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
     }
     return cudaErrorInvalidValue;
 }
