@@ -49,33 +49,25 @@ template <int EPI, bool SINGLE>
 constexpr int epi_warps() { return (EPI == EPI_SWIGLU_BWD || SINGLE) ? 8 : 4; }
 template <int EPI, bool SINGLE>
 constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI, SINGLE>(); }
-// Epilogues that write bf16 / fp32 row blocks from the accumulator stage them in shared memory
-// and store them by TMA
+// Epilogues of four warps that write bf16 / fp32 row blocks from the accumulator: they stage
+// them in shared memory and store them by TMA (the drained MXFP8 128 x 256 tiles keep direct stores)
 template <int EPI, bool MX, int BN>
 constexpr bool tma_out() {
     return (!(MX && BN == 256) && epi_warps<EPI, MX && BN == 256>() == 4 &&
             (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WGRAD)) ||
            (!MX && EPI == EPI_SWIGLU_BWD) ||
-           (MX && BN == 256 &&
-            (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WGRAD));
+           (MX && BN == 256 && (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY));
 }
 // bytes of one warp's staging box: 32 rows x 128 bytes, or 32 x 64 (64-byte swizzle) for the
 // eight-warp epilogues (the SwiGLU backward, the drained MXFP8 128 x 256 tiles), whose 4 KB
-// boxes would not fit beside the ring; the drained MXFP8 weight gradients (two-SM, four stages)
-// keep 4 KB boxes for their fp32 rows
+// boxes would not fit beside the ring
 template <int EPI, bool SINGLE>
-constexpr int out_box_bytes() { return (EPI == EPI_SWIGLU_BWD || (SINGLE && EPI != EPI_WGRAD)) ? 2048 : 4096; }
-// staging boxes per epilogue warp, used in turn: two for the drained MXFP8 weight gradients (each
-// warp stores 32 rows x 128 fp32 columns a tile), one otherwise
-template <int EPI, bool SINGLE>
-constexpr int out_boxes() { return (SINGLE && EPI == EPI_WGRAD) ? 2 : 1; }
+constexpr int out_box_bytes() { return (EPI == EPI_SWIGLU_BWD || SINGLE) ? 2048 : 4096; }
 
 // ---- staged TMA stores: one 32-row x 128-byte box per epilogue warp, row = lane ----------------
-// waits until the warp's box stored PENDING + 1 stores ago has been read out by its TMA store
-// (PENDING = 0: the previous one; with a ring of PENDING + 1 boxes, the box about to be rewritten)
-template <int PENDING = 0>
+// waits until the warp's previous box has been read out by its TMA store
 __device__ __forceinline__ void box_acquire(int lane) {
-    if (lane == 0) bulk_wait_read<PENDING>();
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
 }
 // 16-byte chunk `chunk` of the lane's row, 128-byte swizzle (the box is 1024-byte aligned)
@@ -281,47 +273,16 @@ __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& 
             }
         }
     } else if constexpr (EPI == EPI_WGRAD) {
-        if constexpr (TMA) {
-            // rows of this expert's block of the gradient [E * M, N], through the warp's two 4 KB
-            // boxes in turn (a tile stores an even number of boxes, so each starts at box 0)
-            const int orow = t.e * a.m_tiles * kBM + brow;
-            const uint32_t sbox = smem_u32(box);
-            if (a.out_f32) {
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    float o[32];
+        const long long off = (long long)t.e * a.out_e_stride + grow * a.ld0 + t.n0 + 128 * h;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] = t.kb > 0 ? d[32 * c + j] : 0.f;
-                    box_acquire<1>(lane);
-                    box_put_f32x32(sbox + (c & 1) * 4096, lane, o);
-                    box_store(tmC, box + (c & 1) * 4096, lane, t.n0 + 128 * h + 32 * c, orow);
-                }
-            } else {
-#pragma unroll 1
-                for (int b = 0; b < 2; ++b) {
-                    box_acquire<1>(lane);
+        for (int c = 0; c < 4; ++c) {
+            float o[32];
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float o[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = t.kb > 0 ? d[64 * b + 32 * hh + j] : 0.f;
-                        box_put_bf16x32(sbox + (b & 1) * 4096, lane, hh, o, 1.f);
-                    }
-                    box_store(tmC, box + (b & 1) * 4096, lane, t.n0 + 128 * h + 64 * b, orow);
-                }
-            }
-        } else {
-            const long long off = (long long)t.e * a.out_e_stride + grow * a.ld0 + t.n0 + 128 * h;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float o[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = t.kb > 0 ? d[32 * c + j] : 0.f;
-                if (a.out_f32)
-                    store_f32x32(reinterpret_cast<float*>(a.out0) + off + 32 * c, o);
-                else
-                    store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.out0) + off + 32 * c, o);
-            }
+            for (int j = 0; j < 32; ++j) o[j] = t.kb > 0 ? d[32 * c + j] : 0.f;
+            if (a.out_f32)
+                store_f32x32(reinterpret_cast<float*>(a.out0) + off + 32 * c, o);
+            else
+                store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.out0) + off + 32 * c, o);
         }
     }
 }
@@ -329,9 +290,9 @@ __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& 
 // Stages of the smem ring: a CTA pair driving one MMA (TWO) holds only half of each B tile per
 // CTA, which leaves room for six.
 // pipeline stages: six for the two-SM BF16 tiles and the 128 x 128 MXFP8 tiles (33 KB a stage),
-// four otherwise (the two-SM MXFP8 weight gradients: 33.5 KB a stage beside 64 KB of boxes)
+// four otherwise
 template <bool TWO, bool MX, int BN>
-constexpr int ring_stages() { return ((TWO && !MX) || (MX && BN == 128)) ? 6 : kStages; }
+constexpr int ring_stages() { return (TWO || (MX && BN == 128)) ? 6 : kStages; }
 
 // PAIR: clusters of two CTAs on two m-tiles of one expert and the same n-tile.  Without TWO each
 // CTA runs its own MMAs and the pair only shares B by TMA multicast; with TWO the leader CTA
@@ -341,10 +302,8 @@ template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX
 __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
-                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const GemmArgs a) {
-    // tmSA / tmSB (two-SM MXFP8 only): the scale arrays as [atoms * 4, 128] bytes, one atom a box
-    static_assert(!TWO || (PAIR && (!MX || (BN == 256 && WGRAD))), "two-SM MMAs run in CTA pairs");
+    static_assert(!TWO || (PAIR && !MX), "two-SM MMAs run in CTA pairs, BF16 only");
     constexpr int kStages = ring_stages<TWO, MX, BN>();
     constexpr int kElems = MX ? 128 : 64;                // K elements per stage
     constexpr int kMmaK = MX ? 32 : 16;                  // K elements per MMA
@@ -370,8 +329,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     // columns, 128-byte swizzle) in shared memory and writes them with a TMA store (tmC; tmD for the
     // saved [g|u]), so that L2 receives whole lines rather than 16-byte halves of sectors
     constexpr bool kTmaOut = tma_out<EPI, MX, BN>();
-    constexpr int kOutBoxes = out_boxes<EPI, kSingle>();
-    constexpr int kOutBytes = kTmaOut ? kEpiWarps * kOutBoxes * out_box_bytes<EPI, kSingle>() : 0;
+    constexpr int kOutBytes = kTmaOut ? kEpiWarps * out_box_bytes<EPI, kSingle>() : 0;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -470,17 +428,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
 #pragma unroll
                             for (int c = 0; c < nch / 2; ++c)
                                 tma_load_2d_pair(dB + c * kMnLbo, &tmB, lbar, t.n0 + kMnChunk * (rank * nch / 2 + c), krow);
-                        }
-                        if constexpr (MX) {
-                            // this CTA's A atom and all of B's atoms (each SM reads its scales from
-                            // its own tensor memory), counted on the leader's barrier
-                            uint8_t* dS = sSF + stage * kSfBytes;
-                            const int kt = t.row0 / 128 + kb;
-                            tma_load_2d_pair(dS, &tmSA, lbar, 0, 4 * ((t.m0 / 128) * a.sfA_kt + kt));
-#pragma unroll
-                            for (int c = 0; c < kSfBAtoms; ++c)
-                                tma_load_2d_pair(dS + kSfAtom * (1 + c), &tmSB, lbar, 0,
-                                                 4 * ((t.n0 / 128 + c) * a.sfB_kt + kt));
                         }
                         ++issued;
                         if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -604,19 +551,16 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         const uint32_t sf_cols = tmem_base + kAccStages * BN + stage * kSfCols;
                         const uint32_t ss = sf_base + stage * kSfBytes;
 #pragma unroll
-                        for (int c = 0; c <= kSfBAtoms; ++c) {
-                            if constexpr (TWO) tmem_cp_sf_atom_pair(sf_cols + 4 * c, sdesc_plain(ss + kSfAtom * c, 128));
-                            else tmem_cp_sf_atom(sf_cols + 4 * c, sdesc_plain(ss + kSfAtom * c, 128));
-                        }
+                        for (int c = 0; c <= kSfBAtoms; ++c)
+                            tmem_cp_sf_atom(sf_cols + 4 * c, sdesc_plain(ss + kSfAtom * c, 128));
 #pragma unroll
                         for (int ks = 0; ks < kElems / kMmaK; ++ks) {
                             const uint64_t ad = A_MN ? sdesc_sw128(sa + ks * kMnStep, kMnLbo, 1024)
                                                      : sdesc_sw128(sa + ks * kKStep, 16, 1024);
                             const uint64_t bd = B_MN ? sdesc_sw128(sb + ks * kMnStep, kMnLbo, 1024)
                                                      : sdesc_sw128(sb + ks * kKStep, 16, 1024);
-                            const uint32_t id = idesc_mxf8(TWO ? 2 * kBM : kBM, BN, A_MN, B_MN, ks, ks) | a.b_fmt;
-                            if constexpr (TWO) mma_mxf8_pair(d_tmem, ad, bd, id, sf_cols, sf_cols + 4, (kb | ks) != 0);
-                            else mma_mxf8(d_tmem, ad, bd, id, sf_cols, sf_cols + 4, (kb | ks) != 0);
+                            mma_mxf8(d_tmem, ad, bd, idesc_mxf8(kBM, BN, A_MN, B_MN, ks, ks) | a.b_fmt, sf_cols,
+                                     sf_cols + 4, (kb | ks) != 0);
                         }
                     } else {
 #pragma unroll
@@ -698,14 +642,11 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 tmem_ld32(tcol + 96, d + 96);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    if (TWO && rank == 1) mbar_arrive_cluster(tempty + acc, 0);   // the leader's MMAs reuse it
-                    else mbar_arrive(tempty + acc);
-                }
+                if (lane == 0) mbar_arrive(tempty + acc);
                 if (t.valid)
                     epilogue_drained<BN, EPI, kTmaOut>(a, t, grow, half, d, &tmC, &tmD,
-                                                       sOut + (warp - 2) * kOutBoxes * out_box_bytes<EPI, kSingle>(),
-                                                       lane, t.m0 + 32 * quarter);
+                                                       sOut + (warp - 2) * out_box_bytes<EPI, kSingle>(), lane,
+                                                       t.m0 + 32 * quarter);
                 acc_phase ^= 1u;
                 continue;
             }
@@ -1005,20 +946,6 @@ static bool tmap_2d_fp4(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D tensor map over an array of 512-byte scale atoms viewed as [bytes / 128, 128] bytes, box
-// {128, 4}: one atom a copy, unswizzled
-static bool tmap_sf(CUtensorMap* m, const void* ptr, uint64_t bytes) {
-    EncodeTiledFn enc = get_encode();
-    if (!enc || bytes < 512 || bytes % 512 != 0) return false;
-    const cuuint64_t dims[2] = {128, bytes / 128};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {128, 4};
-    const cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // 2-D tensor map with box {64 bytes, box_rows} and 64-byte swizzle (staged SwiGLU-backward outputs)
 static bool tmap_2d_sw64(CUtensorMap* m, const void* ptr, int esize, uint64_t inner, uint64_t outer,
                          uint32_t box_rows) {
@@ -1043,33 +970,24 @@ constexpr bool use_pairs() { return WGRAD; }
 // gradients and the backward gate/up product, where they measured 6-10% faster on GB300; the
 // forward products and the SwiGLU backward keep one CTA per 128 x 256 tile (a grouped-M pair
 // needs two m-tiles of one expert, and the duplicated odd tiles cancel the gain there).
-// The MXFP8 weight gradients run two-SM too (256 x 256 per pair, 128 x 256 per CTA with one
-// accumulator): a one-SM 128 x 128 block-scaled MMA needs about 225 bytes a clock of shared-memory
-// traffic (operand reads plus the TMA fills) against the SM's 128, and was measured at 0.42-0.52
-// of the MXFP8 peak; a pair holding half of B each needs about half that.
 template <int BN, bool MX, bool WGRAD, int EPI>
-constexpr bool use_two() { return BN == 256 && (MX ? WGRAD : (WGRAD || EPI == EPI_PLAIN)); }
+constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN); }
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                       const CUtensorMap* tc = nullptr, const CUtensorMap* td = nullptr,
-                       const CUtensorMap* tsa = nullptr, const CUtensorMap* tsb = nullptr) {
+                       const CUtensorMap* tc = nullptr, const CUtensorMap* td = nullptr) {
     constexpr bool TWO = use_two<BN, MX, WGRAD, EPI>();
     constexpr bool PAIR = TWO || use_pairs<WGRAD>();
     auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR, TWO>;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
-    const size_t out_bytes = tma_out<EPI, MX, BN>() ? (size_t)epi_warps<EPI, MX && BN == 256>() *
-                                                          out_boxes<EPI, MX && BN == 256>() *
-                                                          out_box_bytes<EPI, MX && BN == 256>()
-                                                    : 0;
+    const size_t out_bytes = tma_out<EPI, MX, BN>()
+                                 ? (size_t)epi_warps<EPI, MX && BN == 256>() * out_box_bytes<EPI, MX && BN == 256>()
+                                 : 0;
     const size_t fixed = 1024 + ring_stages<TWO, MX, BN>() * stage + out_bytes + 256;
     if (tma_out<EPI, MX, BN>() && !tc) return cudaErrorInvalidValue;
     const CUtensorMap& tcm = tc ? *tc : ta;   // kernels without a TMA-stored output never read it
     const CUtensorMap& tdm = td ? *td : tcm;
-    if (TWO && MX && (!tsa || !tsb)) return cudaErrorInvalidValue;
-    const CUtensorMap& tsam = tsa ? *tsa : ta;   // scale maps: read by the two-SM MXFP8 products only
-    const CUtensorMap& tsbm = tsb ? *tsb : ta;
     const size_t smem = fixed + (size_t)2 * (a.E + 1) * 4;
     const size_t smem_max = fixed + (size_t)2 * (kMaxExperts + 1) * 4;
     static std::once_flag once;
@@ -1098,7 +1016,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (!PAIR) {
-        kern<<<c.num_sms, kThreads, smem, c.st>>>(ta, tb, tcm, tdm, tsam, tsbm, a);
+        kern<<<c.num_sms, kThreads, smem, c.st>>>(ta, tb, tcm, tdm, a);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -1113,7 +1031,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     cfg.stream = c.st;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tcm, tdm, tsam, tsbm, a);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tcm, tdm, a);
 }
 
 int bwd_down_bn(int64_t I) { return (I % 256 == 0) ? 256 : 128; }
@@ -1242,28 +1160,26 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.out0 = b + L.ypart; a.ld0 = (int)H;
             return run<256, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a, &tc);
         case GemmKind::WgradDown:
-        case GemmKind::WgradGateUp: {
-            // dW2[e] = dY^T (w h): M = H, N = I;  dW13[e] = [dg|du]^T X: M = 2I, N = H; both
-            // operands token-blocked (MN-major).  Where N allows, two-SM 256 x 256 tiles (each CTA
-            // 128 x 256 with one accumulator drained to registers, half of B, its A atom and all of
-            // B's scale atoms); else 128 x 128 tiles with two accumulators, a pair sharing B.
-            const bool down = kind == GemmKind::WgradDown;
-            const int64_t Mw = down ? H : 2 * I, Nw = down ? I : H;
-            const size_t qa = down ? M.dy_c : M.dg_c, qb = down ? M.hw_c : M.x_c;
-            const size_t sa = down ? M.dy_c_sf : M.dg_c_sf, sb = down ? M.hw_c_sf : M.x_c_sf;
-            const bool two = Nw % 256 == 0;
-            CUtensorMap tsa, tsb;
-            if (!tmap_2d(&ta, b + qa, 1, Mw, R, 128) || !tmap_2d(&tb, b + qb, 1, Nw, R, two ? 128 : 64) ||
-                !tmap_2d(&tc, out, oes, Nw, E * Mw, 32) || !tmap_sf(&tsa, b + sa, (uint64_t)R * Mw / 32) ||
-                !tmap_sf(&tsb, b + sb, (uint64_t)R * Nw / 32))
+            // weight gradients keep 128 x 128 tiles with two accumulators: their contraction over an
+            // expert's rows is short, so a drained single accumulator would stall the MMAs, and the
+            // fp32 output stores need the epilogue to overlap the next tile; a pair splits B's K rows
+            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 64) ||
+                !tmap_2d(&tc, out, oes, I, E * H, 32))
                 return cudaErrorInvalidValue;
-            a.m_tiles = (int)(Mw / 128); a.n_tiles = (int)(Nw / (two ? 256 : 128));
-            a.sfA = u8(sa); a.sfA_kt = (int)(R / 128);
-            a.sfB = u8(sb); a.sfB_kt = (int)(R / 128);
-            a.out0 = out; a.ld0 = (int)Nw; a.out_e_stride = Mw * Nw;
-            return two ? run<256, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc, nullptr, &tsa, &tsb)
-                       : run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
-        }
+            a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / 128);
+            a.sfA = u8(M.dy_c_sf); a.sfA_kt = (int)(R / 128);
+            a.sfB = u8(M.hw_c_sf); a.sfB_kt = (int)(R / 128);
+            a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
+            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
+        case GemmKind::WgradGateUp:
+            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 64) ||
+                !tmap_2d(&tc, out, oes, H, E * 2 * I, 32))
+                return cudaErrorInvalidValue;
+            a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 128);
+            a.sfA = u8(M.dg_c_sf); a.sfA_kt = (int)(R / 128);
+            a.sfB = u8(M.x_c_sf); a.sfB_kt = (int)(R / 128);
+            a.out0 = out; a.ld0 = (int)H; a.out_e_stride = 2 * I * H;
+            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
     }
     return cudaErrorInvalidValue;
 }
