@@ -502,6 +502,22 @@ def run_ours(args, rank, ws, local):
     # fp8_bwd: the checkpointed layer is two BF16 forwards (2F) and one MXFP8 backward (2F), so its
     # peak is the harmonic blend 4F / (2F / P_bf16 + 2F / P_mx)
     blend_peak = 2.0 * bf16_peak * mx_peak / (bf16_peak + mx_peak)
+    if cfg.precision == "fp8_fp4":
+        # a forward-only layer: the line is its forward with the weight copies made once
+        psrc = f"{src} bf16_tflops_sustained x 2 (nominal FP8:BF16 ratio; kind::mxf8f6f4 runs E2M1 at it)"
+        f4 = fwd_measure(bd, gen, cfg, args.steps, args.warmup, ws, local, mx_peak, psrc)
+        return {
+            "metric": METRIC, "value": f4["fwd_tflops_reuse_weights"] * ws, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": f4["fwd_ms_reuse_weights"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8-e4m3 x mxfp4-e2m1",
+            "data": "synthetic: seeded N(0,1) x, N(0,1/sqrt(fan_in)) weights, uniform top-8 routing, softmax weights",
+            "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} k={cfg.k} fp8_fp4 "
+                                   f"{cfg.routing} routing",
+                       "step": "fwd (forward only; weight copies made once)",
+                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "roofline": f4["roofline"], "gpu_launches": f4["gpu_launches_per_fwd"] * args.steps,
+            "clocks": f4["clocks"], "device_status": f4["device_status"], "fp8_fp4_fwd": f4, "cpu_baseline": None,
+        }
     is_mx = cfg.precision == "mxfp8"
     peak = {"bf16": bf16_peak, "mxfp8": mx_peak, "fp8_bwd": blend_peak}[cfg.precision]
     peak_src = (f"{src} bf16_tflops_sustained" + {"bf16": "", "mxfp8": " x 2 (nominal MXFP8:BF16 ratio)",

@@ -80,6 +80,8 @@ CONFIGS = {
     "profile_30b_e32": LayerConfig("profile_30b_e32", T=4096, H=2048, I=768, E=32, k=8, seed=1001),
     "profile_30b_e32_mxfp8": LayerConfig("profile_30b_e32_mxfp8", T=4096, H=2048, I=768, E=32, k=8,
                                          precision="mxfp8", seed=1001),
+    "profile_30b_e32_fp8_fp4": LayerConfig("profile_30b_e32_fp8_fp4", T=4096, H=2048, I=768, E=32, k=8,
+                                           precision="fp8_fp4", seed=1001),
 }
 
 
