@@ -473,24 +473,26 @@ __device__ __forceinline__ void quant_row32(const float* v, uint8_t* dst, uint8_
 
 // Column blocks: the 32 lanes of a warp hold 32 consecutive rows (lane = row), each the same 32
 // columns; column j's scale is shared by the 32 rows.  The column maxima come from one warp
-// max-reduction each on the |value| bit patterns (non-negative floats order like integers), whose
-// result every lane receives, so every lane derives all 32 scales itself (a few integer
-// operations each, in place of a broadcast).  Lane j writes the scale byte of column col0 + j;
-// every lane writes its own row's 32 bytes.
+// max-reduction each on the |value| bit patterns (non-negative floats order like integers); lane
+// j keeps column j's maximum, derives its scale and 2^-exp, and the factors are broadcast back.
+// Lane j writes the scale byte of column col0 + j; every lane writes its own row's 32 bytes.
 __device__ __forceinline__ void quant_col32_warp(const float* v, uint8_t* dst_row, uint8_t* sf_base,
                                                  long long col0, long long kblock, long long k_atoms) {
     const int lane = threadIdx.x & 31;
-    float inv[32];
-    uint8_t my_sf = 0;
+    uint32_t mine = 0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j])));
-        uint8_t sf;
-        mx_scale_bits(m, &sf, &inv[j]);
-        if (j == lane) my_sf = sf;
+        if (j == lane) mine = m;
     }
+    uint8_t sf;
+    float my_inv;
+    mx_scale_bits(mine, &sf, &my_inv);
+    float inv[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) inv[j] = __shfl_sync(0xffffffffu, my_inv, j);
     store_e4m3x32(dst_row, v, inv);
-    sf_base[sf_index(col0 + lane, kblock, k_atoms)] = my_sf;
+    sf_base[sf_index(col0 + lane, kblock, k_atoms)] = sf;
 }
 
 }  // namespace moe
