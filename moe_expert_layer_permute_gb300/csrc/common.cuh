@@ -73,11 +73,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-// Requests the 128-byte line holding `p` into L2 (no register result).
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
-}
-
 // ------------------------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion counted on an mbarrier)
 // ------------------------------------------------------------------------------------------

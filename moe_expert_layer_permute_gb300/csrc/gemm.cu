@@ -626,16 +626,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
         uint32_t acc_phase = 0;
         for (int L = unit0; L < num_tiles; L += unit_stride) {
             const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
-            if constexpr (EPI == EPI_SWIGLU_BWD) {
-                // the row's saved g, u for this warp's column chunks are requested into L2 while the
-                // tile's MMAs run (64 bytes each, inside one 128-byte line)
-                const __nv_bfloat16* gurow = a.gu + ((long long)t.m0 + r) * (2LL * a.I);
-#pragma unroll 1
-                for (int c = half; c < BN / 32; c += kHalves) {
-                    prefetch_l2(gurow + t.n0 + 32 * c);
-                    prefetch_l2(gurow + a.I + t.n0 + 32 * c);
-                }
-            }
             if (!mbar_wait(tfull + acc, acc_phase, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + lane_addr + (uint32_t)(acc * BN);
