@@ -149,11 +149,25 @@ GEMM_FLOPS = {  # algorithmic FLOPs per launch of each grouped GEMM (BF16 or MXF
 }
 
 
+def oracle_step(cfg, a, dy):
+    """One step of the workload by the oracle in the workload's precision (quantise-dequantise at
+    the same points as the layer): 2 x forward + backward, or the forward alone for the
+    forward-only FP8 x FP4 layer.  Returns the step's algorithmic FLOPs per token-sample FLOP unit."""
+    import oracle
+    fwd_kw = {"mxfp8": {"mxfp8": True}, "fp8_fp4": {"fp8_fp4": True}}.get(cfg.precision, {})
+    bwd_kw = {"mxfp8": {"mxfp8": True}, "fp8_bwd": {"fp8_bwd": True}}.get(cfg.precision, {})
+    oracle.forward(*a, **fwd_kw)
+    if cfg.precision == "fp8_fp4":
+        return 1
+    oracle.forward(*a, **fwd_kw)
+    oracle.backward(dy, *a, **bwd_kw)
+    return 4
+
+
 def cpu_baseline(cfg, budget_s: float, seed_tokens: int = 256):
     """The oracle as it stands, on a token sample of the workload (all E experts, same k)."""
     import numpy as np
 
-    import oracle
     from moe_expert_layer_permute_gb300 import inputs as gen
     cores = len(os.sched_getaffinity(0))
     Ts = seed_tokens
@@ -166,18 +180,17 @@ def cpu_baseline(cfg, budget_s: float, seed_tokens: int = 256):
     t_end = time.time() + budget_s
     while True:
         t0 = time.perf_counter()
-        oracle.forward(*args)
-        oracle.forward(*args)
-        oracle.backward(dy, *args)
+        units = oracle_step(cfg, args, dy)
         runs.append(time.perf_counter() - t0)
         if time.time() > t_end or len(runs) >= 3:
             break
     sec = statistics.median(runs)
-    flops = 4 * sub.fwd_flops()
+    flops = units * sub.fwd_flops()
     del np
+    what = "forward" if units == 1 else "checkpointed layer 2xfwd+bwd"
     return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{Ts} tokens of {cfg.name} (all {cfg.E} experts, top-{cfg.k}), fp64 numpy, "
-                      f"checkpointed layer 2xfwd+bwd, median of {len(runs)} runs ({sec:.2f} s each)",
+            "sample": f"{Ts} tokens of {cfg.name} (all {cfg.E} experts, top-{cfg.k}), fp64 numpy {cfg.precision}, "
+                      f"{what}, median of {len(runs)} runs ({sec:.2f} s each)",
             "seconds_per_layer_sample": sec}
 
 
@@ -585,7 +598,6 @@ def run_reference(args, rank, ws):
     """The fp64 oracle timed on the host cores, each step a bounded token sample of the workload."""
     import numpy as np
 
-    import oracle
     from moe_expert_layer_permute_gb300 import inputs as gen
     cfg = gen.CONFIGS[args.config]
     cores = len(os.sched_getaffinity(0))
@@ -595,29 +607,27 @@ def run_reference(args, rank, ws):
     inp = gen.make_inputs(sub)
     a = (inp.f64("x"), inp.topk_idx, inp.f64("topk_w"), inp.f64("W13"), inp.f64("W2"))
     dy = inp.f64("dy")
+    fwd_only = cfg.precision == "fp8_fp4"
 
-    def step():
-        oracle.forward(*a)
-        oracle.forward(*a)
-        oracle.backward(dy, *a)
-
+    units = 1 if fwd_only else 4
     for _ in range(args.warmup):
-        step()
+        oracle_step(cfg, a, dy)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        oracle_step(cfg, a, dy)
     sec = (time.perf_counter() - t0) / args.steps
-    val = 4 * sub.fwd_flops() / sec / 1e12
+    val = units * sub.fwd_flops() / sec / 1e12
     del np
     return {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (same recipe as ours)",
             "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} k={cfg.k} "
                                    f"{cfg.precision} {cfg.routing} routing",
-                       "step": "fwd + fwd + bwd (oracle)", "parallelism": "single process"},
+                       "step": "fwd (oracle)" if fwd_only else "fwd + fwd + bwd (oracle)",
+                       "parallelism": "single process"},
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": f"{Ts} tokens of {cfg.name} per step (all {cfg.E} experts, top-{cfg.k}), "
-                                       f"fp64 numpy checkpointed layer"},
+                                       f"fp64 numpy {'forward' if fwd_only else 'checkpointed layer'}"},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
