@@ -971,7 +971,10 @@ constexpr bool use_pairs() { return WGRAD; }
 // forward products and the SwiGLU backward keep one CTA per 128 x 256 tile (a grouped-M pair
 // needs two m-tiles of one expert, and the duplicated odd tiles cancel the gain there).
 template <int BN, bool MX, bool WGRAD, int EPI>
-constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN); }
+constexpr bool use_two() {
+    return !MX && BN == 256 &&
+           (WGRAD || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WEIGHTED);
+}
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
