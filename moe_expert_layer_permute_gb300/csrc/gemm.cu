@@ -1057,7 +1057,9 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
                        ? run<256, false, false, true, false, EPI_SWIGLU, false>(c, ta, tb, a, &tc, &td)
                        : run<256, false, false, true, false, EPI_GU_ONLY, false>(c, ta, tb, a, &tc, &td);
         case GemmKind::FwdDown:
-            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 256) ||
+            // B box: the pair's CTAs each load half of the 256 weight rows
+            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) ||
+                !tmap_2d(&tb, W, 2, I, E * H, use_two<256, false, false, EPI_WEIGHTED>() ? 128 : 256) ||
                 !tmap_2d(&tc, b + L.ypart, 2, H, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 64); a.b_rows_e = (int)H;
