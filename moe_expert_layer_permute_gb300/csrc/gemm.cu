@@ -971,10 +971,7 @@ constexpr bool use_pairs() { return WGRAD; }
 // forward products and the SwiGLU backward keep one CTA per 128 x 256 tile (a grouped-M pair
 // needs two m-tiles of one expert, and the duplicated odd tiles cancel the gain there).
 template <int BN, bool MX, bool WGRAD, int EPI>
-constexpr bool use_two() {
-    return !MX && BN == 256 &&
-           (WGRAD || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WEIGHTED);
-}
+constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN); }
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
@@ -1057,9 +1054,7 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
                        ? run<256, false, false, true, false, EPI_SWIGLU, false>(c, ta, tb, a, &tc, &td)
                        : run<256, false, false, true, false, EPI_GU_ONLY, false>(c, ta, tb, a, &tc, &td);
         case GemmKind::FwdDown:
-            // B box: the pair's CTAs each load half of the 256 weight rows
-            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) ||
-                !tmap_2d(&tb, W, 2, I, E * H, use_two<256, false, false, EPI_WEIGHTED>() ? 128 : 256) ||
+            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 256) ||
                 !tmap_2d(&tc, b + L.ypart, 2, H, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 64); a.b_rows_e = (int)H;
