@@ -175,21 +175,14 @@ __device__ __forceinline__ int find_expert(const int* s_mtile, int E, int gm) {
 // expert (rank 0 the even, rank 1 the odd one) and the same n-tile, so they need the same B tile.
 // Grouped-M units enumerate the pairs of each expert (s_pair: prefix of ceil(m-tiles / 2)); an
 // expert with an odd m-tile count gives rank 1 a duplicate of rank 0's last tile, not stored.
-// NPAIR (grouped-M products in clusters of two single-SM CTAs): unit L is one m-tile and a pair
-// of adjacent n-tiles; rank r takes n-tile 2q + r, and the pair shares the A tile.
-template <int BN, bool WGRAD, bool SPLIT, int kElems, bool PAIR, bool NPAIR = false>
+template <int BN, bool WGRAD, bool SPLIT, int kElems, bool PAIR>
 __device__ __forceinline__ Tile decode_tile(int L, const GemmArgs& a, const int* s_mtile, const int* s_pair,
                                             int rank) {
     Tile t;
     t.valid = true;
     if (!WGRAD) {
         int gm;
-        if (NPAIR) {
-            const int hn = a.n_tiles / 2;
-            gm = L / hn;
-            t.nt = 2 * (L - gm * hn) + rank;
-            t.e = find_expert(s_mtile, a.E, gm);
-        } else if (PAIR) {
+        if (PAIR) {
             const int P = L / a.n_tiles;
             t.nt = L - P * a.n_tiles;
             t.e = find_expert(s_pair, a.E, P);
@@ -312,10 +305,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         const GemmArgs a) {
     static_assert(!TWO || (PAIR && !MX), "two-SM MMAs run in CTA pairs, BF16 only");
     constexpr int kStages = ring_stages<TWO, MX, BN>();
-    // clusters of two single-SM CTAs on one m-tile and adjacent n-tiles: each loads half of the
-    // shared A tile and multicasts it, and its own B (grouped-M products without TWO)
-    constexpr bool kNPair = PAIR && !WGRAD && !TWO;
-    static_assert(!kNPair || !A_MN, "a shared A tile is K-major");
     constexpr int kElems = MX ? 128 : 64;                // K elements per stage
     constexpr int kMmaK = MX ? 32 : 16;                  // K elements per MMA
     constexpr int kMnChunk = MX ? 128 : 64;              // MN elements per 128-byte row (MN-major)
@@ -396,9 +385,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem_base = *tslot;
-    const int num_tiles = WGRAD    ? a.E * (PAIR ? a.m_tiles / 2 : a.m_tiles) * a.n_tiles
-                          : kNPair ? s_mtile[a.E] * (a.n_tiles / 2)
-                                   : (PAIR ? s_pair[a.E] : s_mtile[a.E]) * a.n_tiles;
+    const int num_tiles = WGRAD ? a.E * (PAIR ? a.m_tiles / 2 : a.m_tiles) * a.n_tiles
+                                : (PAIR ? s_pair[a.E] : s_mtile[a.E]) * a.n_tiles;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -411,7 +399,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             // (half a byte a value) although it lands in shared memory as a byte a value
             const uint32_t stage_tx = kStageBytes - (a.b_fmt ? kBTileBytes / 2 : 0);
             for (int L = unit0; L < num_tiles && ok; L += unit_stride) {
-                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR, kNPair>(L, a, s_mtile, s_pair, rank);
+                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
                 // first B row of the tile (K-major B); MXFP8 gate/up weights are stored with
                 // 128-row blocks of [64 gate | 64 up] rows, so the split tile is one block
                 const int b_row0 = t.e * a.b_rows_e + ((SPLIT && MX) ? t.nt * BN : t.n0);
@@ -446,18 +434,14 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         continue;
                     }
                     mbar_arrive_expect_tx(full + stage, stage_tx);
-                    if (kNPair) {
-                        // this CTA's half of the shared A rows, to both CTAs (64-row box)
-                        tma_load_2d_mc(dA + rank * (kBM / 2) * kRowBytes, &tmA, full + stage, k0,
-                                       t.m0 + rank * (kBM / 2), kPeers);
-                    } else if (!A_MN) {
+                    if (!A_MN) {
                         tma_load_2d(dA, &tmA, full + stage, k0, t.m0);
                     } else {
 #pragma unroll
                         for (int c = 0; c < kBM / kMnChunk; ++c)
                             tma_load_2d(dA + c * kMnLbo, &tmA, full + stage, t.m0 + kMnChunk * c, t.row0 + k0);
                     }
-                    if (PAIR && !kNPair) {
+                    if (PAIR) {
                         // each CTA loads half of the B tile and multicasts it to both
                         if (!B_MN) {
                             const int brow = (SPLIT && !MX) ? t.e * a.b_rows_e + rank * a.b_up + t.n0
@@ -509,7 +493,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                                 mn_tile = t.n0 / 128 + c;
                                 kt = t.row0 / 128 + kb;
                             }
-                            if (!PAIR || kNPair)   // n-pairs: each CTA's own n-tile
+                            if (!PAIR)
                                 bulk_load(dS + kSfAtom * (1 + c), a.sfB + (mn_tile * a.sfB_kt + kt) * kSfAtom, kSfAtom,
                                           full + stage);
                             else if (rank == 0)   // B's scales go to both CTAs
@@ -538,7 +522,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             // issues the MMAs; before exiting, wait for the leader's releases of its last stages
             long long consumed = 0;
             for (int L = unit0; L < num_tiles; L += unit_stride)
-                consumed += decode_tile<BN, WGRAD, SPLIT, kElems, PAIR, kNPair>(L, a, s_mtile, s_pair, rank).kb;
+                consumed += decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank).kb;
             for (int s = 0; s < kStages; ++s) {
                 if (consumed > s) {
                     const long long n = (consumed - s + kStages - 1) / kStages;
@@ -554,7 +538,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB), sf_base = smem_u32(sSF);
             long long consumed = 0;
             for (int L = unit0; L < num_tiles && ok; L += unit_stride) {
-                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR, kNPair>(L, a, s_mtile, s_pair, rank);
+                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
                 if (!(TWO ? mbar_wait_cluster(tempty + acc, acc_phase ^ 1u, abort_flag, a.status)
                           : mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag, a.status))) { ok = false; break; }
                 tc_fence_after();
@@ -641,7 +625,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int L = unit0; L < num_tiles; L += unit_stride) {
-            const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR, kNPair>(L, a, s_mtile, s_pair, rank);
+            const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
             if (!mbar_wait(tfull + acc, acc_phase, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + lane_addr + (uint32_t)(acc * BN);
@@ -989,14 +973,11 @@ constexpr bool use_pairs() { return WGRAD; }
 template <int BN, bool MX, bool WGRAD, int EPI>
 constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN); }
 
-// NP: a grouped-M product in clusters of two single-SM CTAs sharing the A tile (n-tile pairs;
-// the caller checks that n_tiles is even and gives A a 64-row box)
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool NP = false>
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
                        const CUtensorMap* tc = nullptr, const CUtensorMap* td = nullptr) {
     constexpr bool TWO = use_two<BN, MX, WGRAD, EPI>();
-    static_assert(!NP || (!TWO && !WGRAD), "n-tile pairs are single-SM grouped-M products");
-    constexpr bool PAIR = TWO || use_pairs<WGRAD>() || NP;
+    constexpr bool PAIR = TWO || use_pairs<WGRAD>();
     auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR, TWO>;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
@@ -1063,30 +1044,22 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
     CUtensorMap ta, tb, tc, td;
     switch (kind) {
         case GemmKind::FwdGateUp:
-        case GemmKind::FwdGateUpSaveOnly: {
-            // n-tile pairs sharing the dispatched rows where the n-tile count is even
-            const bool np = (I / 128) % 2 == 0;
-            if (!tmap_2d(&ta, b + L.xperm, 2, H, R, np ? 64 : 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 128) ||
+        case GemmKind::FwdGateUpSaveOnly:
+            if (!tmap_2d(&ta, b + L.xperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 128) ||
                 !tmap_2d(&tc, b + L.hid, 2, I, R, 32) || !tmap_2d(&td, b + L.gu, 2, 2 * I, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 64); a.b_rows_e = (int)(2 * I); a.b_up = (int)I;
             a.out0 = b + L.hid; a.out1 = b + L.gu;
-            if (kind == GemmKind::FwdGateUp)
-                return np ? run<256, false, false, true, false, EPI_SWIGLU, false, true>(c, ta, tb, a, &tc, &td)
-                          : run<256, false, false, true, false, EPI_SWIGLU, false>(c, ta, tb, a, &tc, &td);
-            return np ? run<256, false, false, true, false, EPI_GU_ONLY, false, true>(c, ta, tb, a, &tc, &td)
-                      : run<256, false, false, true, false, EPI_GU_ONLY, false>(c, ta, tb, a, &tc, &td);
-        }
-        case GemmKind::FwdDown: {
-            const bool np = (H / 256) % 2 == 0;
-            if (!tmap_2d(&ta, b + L.hid, 2, I, R, np ? 64 : 128) || !tmap_2d(&tb, W, 2, I, E * H, 256) ||
+            return kind == GemmKind::FwdGateUp
+                       ? run<256, false, false, true, false, EPI_SWIGLU, false>(c, ta, tb, a, &tc, &td)
+                       : run<256, false, false, true, false, EPI_GU_ONLY, false>(c, ta, tb, a, &tc, &td);
+        case GemmKind::FwdDown:
+            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 256) ||
                 !tmap_2d(&tc, b + L.ypart, 2, H, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 64); a.b_rows_e = (int)H;
             a.out0 = b + L.ypart; a.ld0 = (int)H;
-            return np ? run<256, false, false, false, false, EPI_WEIGHTED, false, true>(c, ta, tb, a, &tc)
-                      : run<256, false, false, false, false, EPI_WEIGHTED, false>(c, ta, tb, a, &tc);
-        }
+            return run<256, false, false, false, false, EPI_WEIGHTED, false>(c, ta, tb, a, &tc);
         case GemmKind::BwdDown: {
             const int bn = bwd_down_bn(I);
             if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 64) ||
