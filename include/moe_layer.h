@@ -85,9 +85,10 @@ typedef struct {
  * that had MOE_FLAG_SAVE_GU and the same x, topk_idx, topk_w, W13, W2 pointers and desc; returns
  * MOE_ERR_STATE if the scratch handle does not record such a forward. */
 #define MOE_FLAG_REUSE_FWD   0x2u
-/* MXFP8 only: W13 and W2 hold the same values as when an earlier call on this scratch (same
- * pointers) quantised them, so their E4M3 copies in scratch are reused instead of being made
- * again (a training step quantises its weights once: forward, recompute and backward share them).
+/* Block-scaled precisions only (MOE_MXFP8, MOE_FP8_BWD, MOE_FP8_FP4): W13 and W2 hold the same
+ * values as when an earlier call on this scratch (same pointers) quantised them, so their E4M3 /
+ * E2M1 copies in scratch are reused instead of being made again (a training step quantises its
+ * weights once: forward, recompute and backward share them; a forward-only layer keeps them).
  * Returns MOE_ERR_STATE if the scratch handle records no quantisation of these pointers. */
 #define MOE_FLAG_REUSE_WEIGHTS 0x4u
 

@@ -1099,8 +1099,9 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
 }
 
 // MXFP8: 128 x 256 tiles (one accumulator) for the forward and data-gradient products except the
-// SwiGLU backward; 128 x 128 tiles (two accumulators) for it and the weight gradients; operands are the E4M3 copies made by the quantiser and
-// the epilogues (quant.cu, the fused epilogues above).
+// SwiGLU backward; 128 x 128 tiles (two accumulators) for it and the weight gradients.  Operands
+// are the E4M3 copies made by the quantiser and the epilogues (quant.cu, the fused epilogues
+// above); in the FP8 x FP4 forward the weights are the quantiser's packed E2M1 copies.
 static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmArgs& a) {
     const Layout& L = *c.L;
     const MxLayout& M = L.mx;

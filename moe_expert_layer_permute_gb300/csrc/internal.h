@@ -81,7 +81,7 @@ cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, b
 // N tile of the backward down-projection product (and so the number of <dA, h> partials per row)
 int bwd_down_bn(int64_t I);
 
-// MXFP8 quantiser over a bf16 [R_max, C] array (R_max % 32 == 0, C % 128 == 0); with tiles_dev only
+// MX quantiser over a bf16 [R_max, C] array (R_max % 32 == 0, C % 128 == 0); with tiles_dev only
 // the first tiles_dev[0] * 128 rows.  Any of the outputs may be null.  gate_up_I > 0 stores the
 // row-blocked copy of a [E*2I, H] gate/up weight in [64 gate | 64 up] row blocks.
 // With row_slot (padded rows only) source row r is row_slot[r] / k, zero where row_slot[r] < 0.
