@@ -194,20 +194,38 @@ def cpu_baseline(cfg, budget_s: float, seed_tokens: int = 256):
             "seconds_per_layer_sample": sec}
 
 
+def host_tensor(a):
+    """A numpy input array as a CPU torch tensor (bf16 bit patterns reinterpreted)."""
+    import numpy as np
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a))
+
+
+def timed(fn, n, ws, stream):
+    """Milliseconds of n calls of fn between CUDA events on `stream`, with a barrier and a device
+    synchronisation on both sides; the maximum over ranks."""
+    import torch
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    return allreduce_max(e0.elapsed_time(e1), ws)
+
+
 def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
     """Times fwd, bwd and the checkpointed layer for one workload; returns a dict of results."""
-    import numpy as np
     import torch
 
     dev = torch.device("cuda", local)
     inp = gen.make_inputs(cfg)
-
-    def host(a):
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
-        return torch.from_numpy(np.ascontiguousarray(a))
-
-    h_in = {n: host(getattr(inp, n)).pin_memory() for n in ("x", "topk_idx", "topk_w", "W13", "W2", "dy")}
+    h_in = {n: host_tensor(getattr(inp, n)).pin_memory() for n in ("x", "topk_idx", "topk_w", "W13", "W2", "dy")}
     del inp
     d = {n: t.to(dev) for n, t in h_in.items()}
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
@@ -240,18 +258,6 @@ def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
         fwd(bd.MOE_FLAG_SAVE_GU | RW)
         bwd(bd.MOE_FLAG_REUSE_FWD | RW)
 
-    def timed(fn, n):
-        barrier(ws)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier(ws)
-        return allreduce_max(e0.elapsed_time(e1), ws)
-
     for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize()
@@ -262,16 +268,16 @@ def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
     clocks.start()
     # forward alone (each call makes its own MXFP8 weight copies) and backward alone (reusing a
     # saved forward, as in the layer)
-    fwd_ms = timed(fwd, steps) / steps
+    fwd_ms = timed(fwd, steps, ws, stream) / steps
     fwd(bd.MOE_FLAG_SAVE_GU)
-    bwd_ms = timed(lambda: bwd(bd.MOE_FLAG_REUSE_FWD | RW), steps) / steps
+    bwd_ms = timed(lambda: bwd(bd.MOE_FLAG_REUSE_FWD | RW), steps, ws, stream) / steps
     # the checkpointed layer; then the same steps again with per-kernel CUDA events recorded on
     # the launch stream (the events between launches cost time, so they are not in full_ms)
-    full_total = timed(step, steps)
+    full_total = timed(step, steps, ws, stream)
     bd.moe_trace_reset()
     bd.moe_trace_enable(True)
     traced_steps = max(3, min(steps, 50))
-    timed(step, traced_steps)
+    timed(step, traced_steps, ws, stream)
     bd.moe_trace_enable(False)
     kern = bd.moe_trace_read()
     clk = clocks.stop()
@@ -330,7 +336,7 @@ def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
 
         e2e_steps = max(3, min(steps, 20))
         e2e_run(2)
-        out["e2e_ms"] = timed(lambda: e2e_run(e2e_steps), 1) / e2e_steps
+        out["e2e_ms"] = timed(lambda: e2e_run(e2e_steps), 1, ws, stream) / e2e_steps
         out["h2d"], out["d2h"] = h2d, d2h
         out["e2e_copies"] = ("per step: x, dy, topk_idx, topk_w host->device and y, dx, dtopk_w device->host "
                              "(pinned host memory; W13, W2 resident and dW13, dW2 kept on the device as in "
@@ -344,18 +350,11 @@ def fwd_measure(bd, gen, cfg, steps, warmup, ws, local, peak, peak_src):
     """The forward alone in a forward-only precision (FP8 x FP4): per call with the weights
     quantised in the call, and with the copies made once (MOE_FLAG_REUSE_WEIGHTS, fixed weights as
     when serving); per-kernel times of the latter and the roofline of its dominant GEMM."""
-    import numpy as np
     import torch
 
     dev = torch.device("cuda", local)
     inp = gen.make_inputs(cfg)
-
-    def host(a):
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
-        return torch.from_numpy(np.ascontiguousarray(a))
-
-    d = {n: host(getattr(inp, n)).to(dev) for n in ("x", "topk_idx", "topk_w", "W13", "W2")}
+    d = {n: host_tensor(getattr(inp, n)).to(dev) for n in ("x", "topk_idx", "topk_w", "W13", "W2")}
     del inp
     d["y"] = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
     prec = {"fp8_fp4": bd.MOE_FP8_FP4, "mxfp8": bd.MOE_MXFP8}[cfg.precision]
@@ -366,18 +365,6 @@ def fwd_measure(bd, gen, cfg, steps, warmup, ws, local, peak, peak_src):
     def fwd(flags=0):
         bd.moe_fwd(d["x"], d["topk_idx"], d["topk_w"], d["W13"], d["W2"], d["y"], sc, flags=flags)
 
-    def timed(fn, n):
-        barrier(ws)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier(ws)
-        return allreduce_max(e0.elapsed_time(e1), ws)
-
     fwd()
     for _ in range(max(3, warmup)):
         fwd(RW)
@@ -386,12 +373,12 @@ def fwd_measure(bd, gen, cfg, steps, warmup, ws, local, peak, peak_src):
         raise RuntimeError("device status word set during warm-up")
     clocks = ClockSampler(local)
     clocks.start()
-    q_ms = timed(fwd, steps) / steps
-    r_ms = timed(lambda: fwd(RW), steps) / steps
+    q_ms = timed(fwd, steps, ws, stream) / steps
+    r_ms = timed(lambda: fwd(RW), steps, ws, stream) / steps
     bd.moe_trace_reset()
     bd.moe_trace_enable(True)
     traced = max(3, min(steps, 50))
-    timed(lambda: fwd(RW), traced)
+    timed(lambda: fwd(RW), traced, ws, stream)
     bd.moe_trace_enable(False)
     kern = bd.moe_trace_read()
     clk = clocks.stop()
