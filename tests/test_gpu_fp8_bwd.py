@@ -68,8 +68,9 @@ def test_backward(cuda_lib, name, reuse):
     assert rel_fro(f64(L.dx), ref["dx"]) < rel_fro(f64(L.dx), bf["dx"])
 
 
-def test_full_size_sampled(cuda_lib):
-    cfg = gen.CONFIGS["qwen3_30b_a3b_fp8_bwd"]
+@pytest.mark.parametrize("name", ["qwen3_30b_a3b", "qwen3_235b_a22b"])
+def test_full_size_sampled(cuda_lib, name):
+    cfg = fp8b(gen.CONFIGS[name])
     inp = gen.make_inputs(cfg)
     L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
     L.fwd()

@@ -148,8 +148,9 @@ def test_zero_tokens(cuda_lib):
     assert L.status() == 0 and L.y.numel() == 0
 
 
-def test_full_size_sampled(cuda_lib):
-    cfg = gen.CONFIGS["qwen3_30b_a3b_fp8_fp4"]
+@pytest.mark.parametrize("name", ["qwen3_30b_a3b", "qwen3_235b_a22b"])
+def test_full_size_sampled(cuda_lib, name):
+    cfg = fp4(gen.CONFIGS[name])
     inp = gen.make_inputs(cfg)
     L = DeviceLayer(cuda_lib, inp)
     L.fwd()
