@@ -141,7 +141,7 @@ class ClockSampler:
 # named workload: profiles/gemm_fwd_gate_up_bf16_profile_30b_e32.md (profile_30b_e32, the forward
 # that saves [g|u]: 343.6 MB read + 124.6 MB written; every size scales with E at equal per-expert
 # work, so x4 for the 128-expert layer).  Kernels not captured since their last change are absent.
-PROFILED_TRAFFIC = {("qwen3_30b_a3b", "gemm_fwd_gate_up_swiglu"): 4 * (343.563e6 + 124.586e6)}
+PROFILED_TRAFFIC = {("qwen3_30b_a3b", "gemm_fwd_gate_up_swiglu"): 4 * (343.474e6 + 124.403e6)}
 
 GEMM_FLOPS = {  # algorithmic FLOPs per launch of each grouped GEMM (BF16 or MXFP8), in units of S*H*I
     "gemm_fwd_gate_up_swiglu": 4, "gemm_fwd_gate_up_save": 4, "gemm_fwd_down_weighted": 2,
