@@ -548,3 +548,22 @@ def test_fp8_fp4_identity_quantiser_and_sampled_form():
     import unittest.mock as um
     with um.patch.object(oracle.moe_oracle, "mx_qdq", lambda a, axis, fmt="e4m3": np.asarray(a, dtype=np.float64)):
         np.testing.assert_allclose(oracle.forward(x, idx, w, W13, W2, fp8_fp4=True), y_bf, rtol=1e-13, atol=1e-13)
+
+
+def test_e2m1_round_matches_brute_force_nearest_even():
+    """e2m1_round against a brute force written from the format: the nearest of the eight
+    magnitudes, a tie going to the code whose mantissa bit is 0, saturation at 6."""
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])      # codes 0..7, mantissa = code & 1
+    rng = np.random.default_rng(11)
+    mids = (mags[1:] + mags[:-1]) / 2
+    v = np.concatenate([rng.uniform(0, 8, 200_000), mids, np.nextafter(mids, 0), np.nextafter(mids, 9),
+                        mags, [6.5, 7.0, 100.0, 1e-30]])
+    v = np.concatenate([v, -v])
+    a = np.minimum(np.abs(v), 6.0)
+    d = np.abs(a[:, None] - mags[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    odd = (np.arange(8) & 1).astype(bool)
+    pick = np.where(cand.sum(axis=1) > 1, np.argmax(cand & ~odd[None, :], axis=1), np.argmax(cand, axis=1))
+    expect = np.copysign(mags[pick], v)
+    np.testing.assert_array_equal(oracle.e2m1_round(v), expect)
