@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
     __shared__ __align__(16) uint8_t qt[kQRows][kQCols + 16];
     __shared__ __align__(16) uint8_t s_sfr[512];
     __shared__ __align__(16) uint8_t s_sfc[512];
+    __shared__ uint32_t s_cmax[2][64];  // column-pair maxima of the two row halves (column blocks)
     __shared__ long long s_src[128];   // source row of each tile row (-1: a zero padding row)
     const long long rt = (long long)blockIdx.y * 128;
     const long long R = tiles_dev ? (long long)(*tiles_dev) * kBM : R_max;
@@ -141,24 +142,34 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
             }
         }
         if (!FP4 && q_col) {
-            // thread -> column t: 32 rows of one column
-            uint32_t m = 0;
-            uint32_t v[32];
+            // thread -> columns 2 cp, 2 cp + 1 (cp = 32 (warp & 1) + lane) over rows 16 rh .. + 15
+            // (rh = warp >> 1): one 32-bit shared load holds both columns of a row, one packed
+            // unsigned max tracks both columns' |value| maxima, and the two row halves' maxima
+            // meet in shared memory; each row's two codes leave as one 2-byte store
+            const int cp = 32 * ((t >> 5) & 1) + (t & 31), rh = t >> 6;
+            uint32_t w[16];
+            uint32_t m2 = 0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                v[j] = reinterpret_cast<const uint16_t*>(&tile[j][0])[t];
-                m = max(m, v[j] & 0x7FFFu);
+            for (int j = 0; j < 16; ++j) {
+                w[j] = reinterpret_cast<const uint32_t*>(&tile[16 * rh + j][0])[cp];
+                m2 = absmax_bf16x2(m2, w[j]);
             }
-            uint8_t sf;
-            float inv;
-            mx_scale_bits(m << 16, &sf, &inv);
+            s_cmax[rh][cp] = m2;
+            __syncthreads();
+            m2 = __vmaxu2(m2, s_cmax[rh ^ 1][cp]);
+            uint8_t sf0, sf1;
+            float inv0, inv1;
+            mx_scale_bits((m2 & 0xFFFFu) << 16, &sf0, &inv0);      // column 2 cp
+            mx_scale_bits(m2 & 0xFFFF0000u, &sf1, &inv1);          // column 2 cp + 1
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                const uint16_t p = to_e4m3x2(__uint_as_float(v[j] << 16) * inv, __uint_as_float(v[j + 1] << 16) * inv);
-                qt[j][t] = (uint8_t)(p & 0xFF);
-                qt[j + 1][t] = (uint8_t)(p >> 8);
+            for (int j = 0; j < 16; ++j)
+                *reinterpret_cast<uint16_t*>(&qt[16 * rh + j][2 * cp]) =
+                    to_e4m3x2(__uint_as_float(w[j] << 16) * inv0, __uint_as_float(w[j] & 0xFFFF0000u) * inv1);
+            if (rh == 0) {   // columns 2 cp, 2 cp + 1, row block sub
+                const int c0 = 2 * cp, c1 = 2 * cp + 1;
+                s_sfc[16 * (c0 & 31) + 4 * (c0 >> 5) + sub] = sf0;
+                s_sfc[16 * (c1 & 31) + 4 * (c1 >> 5) + sub] = sf1;
             }
-            s_sfc[16 * (t & 31) + 4 * (t >> 5) + sub] = sf;           // column t, row block sub
             __syncthreads();
             const int rr = t >> 2, q = t & 3;
             const uint4* s4 = reinterpret_cast<const uint4*>(&qt[rr][32 * q]);
