@@ -123,10 +123,8 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
                 const long long e = r / (2 * gate_up_I), j = r % (2 * gate_up_I);
                 const long long jj = j < gate_up_I ? j : j - gate_up_I;
                 r = e * 2 * gate_up_I + 128 * (jj / 64) + (j < gate_up_I ? 0 : 64) + jj % 64;
-                sf_row[sf_index(r, (c0 >> 5) + b, C / 128)] = sf;   // rows scatter across atoms
-            } else {
-                s_sfr[16 * rr + 4 * sub + b] = sf;                  // row 32 sub + rr of the atom
             }
+            s_sfr[16 * rr + 4 * sub + b] = sf;                      // tile row 32 sub + rr
             if constexpr (FP4) {
                 uint32_t o[4];
 #pragma unroll
@@ -182,6 +180,19 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
     // the tile's two scale atoms, 16 bytes per thread
     if (q_row && gate_up_I <= 0 && t < 32)
         reinterpret_cast<uint4*>(sf_row + sf_index(rt, c0 >> 5, C / 128))[t] = reinterpret_cast<const uint4*>(s_sfr)[t];
+    if (q_row && gate_up_I > 0 && t < 64) {
+        // gate/up order: the tile (128 rows, all gate or all up, as 128 divides I) fills one half of
+        // two destination atoms, its rows [0, 64) the half at `off` of block jb / 64 and rows
+        // [64, 128) that of the next block; atom row p's four bytes sit at 16 (p % 32) + 4 ((p / 32) % 4),
+        // so each 32-row slice of a half is 8 contiguous bytes per p % 32
+        const long long e = rt / (2 * gate_up_I), j = rt % (2 * gate_up_I);
+        const bool up = j >= gate_up_I;
+        const long long jb = up ? j - gate_up_I : j;                  // a multiple of 128
+        const int half = t >> 5, m = t & 31;
+        const long long blk = e * 2 * gate_up_I + 128 * (jb / 64 + half);   // destination block's first row
+        uint8_t* dst = sf_row + sf_index(blk, c0 >> 5, C / 128) + 16 * m + (up ? 8 : 0);
+        *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(s_sfr + 16 * m + 8 * half);
+    }
     if (!FP4 && q_col && t >= 32 && t < 64)
         reinterpret_cast<uint4*>(sf_col + sf_index(c0, rt >> 5, R_max / 128))[t - 32] =
             reinterpret_cast<const uint4*>(s_sfc)[t - 32];
