@@ -85,8 +85,81 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
         s_src[t] = rt + t;
     }
     __syncthreads();
-    // the 32 x 128 bf16 of pass `sub` with 16-byte accesses; thread t loads rows it*8 + t/16,
-    // columns 8 (t % 16) .. + 7 (through the row map when dispatching)
+    // row blocks: thread -> (row 32 sub + t/4 of the tile, block t%4), the row's 32 values in w
+    const int rr = t >> 2, b = t & 3;
+    auto emit_row = [&](const uint4* w, int sub) {
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, w[q].x), w[q].y), w[q].z), w[q].w);
+        uint8_t sf;
+        float inv;
+        if constexpr (FP4) mx_scale_bits_e2m1(absmax_to_f32_bits(m2), &sf, &inv);
+        else mx_scale_bits(absmax_to_f32_bits(m2), &sf, &inv);
+        long long r = rt + 32 * sub + rr;
+        if (gate_up_I > 0) {  // 128-row blocks of [64 gate rows | 64 up rows] per expert
+            const long long e = r / (2 * gate_up_I), j = r % (2 * gate_up_I);
+            const long long jj = j < gate_up_I ? j : j - gate_up_I;
+            r = e * 2 * gate_up_I + 128 * (jj / 64) + (j < gate_up_I ? 0 : 64) + jj % 64;
+        }
+        s_sfr[16 * rr + 4 * sub + b] = sf;                      // tile row 32 sub + rr
+        if constexpr (FP4) {
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[q] = e2m1x8(w[q], inv);
+            *reinterpret_cast<uint4*>(q_row + r * (C / 2) + (c0 + 32 * b) / 2) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            uint2 o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[q] = e4m3x8(w[q], inv);
+            uint4* dst = reinterpret_cast<uint4*>(q_row + r * C + c0 + 32 * b);
+            dst[0] = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
+            dst[1] = make_uint4(o[2].x, o[2].y, o[3].x, o[3].y);
+        }
+    };
+    // the gate/up copy's scales (threads 0..63, after the passes): the tile (128 rows, all gate or
+    // all up, as 128 divides I) fills one half of two destination atoms, its rows [0, 64) the half
+    // at row 64 * up of block jb / 64 and rows [64, 128) that of the next block; atom row p's four
+    // bytes sit at 16 (p % 32) + 4 ((p / 32) % 4), so each half is 8 contiguous bytes per p % 32
+    auto store_gate_up_scales = [&]() {
+        if (t >= 64) return;
+        const long long e = rt / (2 * gate_up_I), j = rt % (2 * gate_up_I);
+        const bool up = j >= gate_up_I;
+        const long long jb = up ? j - gate_up_I : j;                         // a multiple of 128
+        const int half = t >> 5, m = t & 31;
+        const long long blk = e * 2 * gate_up_I + 128 * (jb / 64 + half);   // destination block's first row
+        uint8_t* dst = sf_row + sf_index(blk, c0 >> 5, C / 128) + 16 * m + (up ? 8 : 0);
+        *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(s_sfr + 16 * m + 8 * half);
+    };
+    if (!q_col) {
+        if (!q_row) return;
+        // row blocks only: each thread reads its 64 bytes of the row straight from global memory
+        // (no staging, no barriers), the next pass's loads in flight while this one is quantised
+        auto load_row = [&](int sub, uint4* w) {
+            const long long sr = s_src[32 * sub + rr];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                w[q] = sr >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + sr * C + c0 + 32 * b) + q)
+                               : make_uint4(0, 0, 0, 0);
+        };
+        uint4 cur[4], nx[4];
+        load_row(0, cur);
+#pragma unroll 1
+        for (int sub = 0; sub < 4; ++sub) {
+            if (sub < 3) load_row(sub + 1, nx);
+            emit_row(cur, sub);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) cur[q] = nx[q];
+        }
+        __syncthreads();
+        if (gate_up_I <= 0 && t < 32)
+            reinterpret_cast<uint4*>(sf_row + sf_index(rt, c0 >> 5, C / 128))[t] = reinterpret_cast<const uint4*>(s_sfr)[t];
+        if (gate_up_I > 0) store_gate_up_scales();
+        return;
+    }
+    // with a column-blocked copy: the 32 x 128 bf16 of pass `sub` staged in shared memory with
+    // 16-byte accesses; thread t loads rows it*8 + t/16, columns 8 (t % 16) .. + 7 (through the
+    // row map when dispatching)
     const int lr = t >> 4, lc = (t & 15) * 8;
     auto load_pass = [&](int sub, uint4* w) {
 #pragma unroll
@@ -104,40 +177,11 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
         __syncthreads();
         if (sub < 3) load_pass(sub + 1, nxt);   // in flight while this pass is quantised
         if (q_row) {
-            // thread -> (row t/4, block t%4): 32 consecutive values of one row
-            const int rr = t >> 2, b = t & 3;
-            const uint4* src4 = reinterpret_cast<const uint4*>(&tile[rr][32 * b]);
             uint4 w[4];
-            uint32_t m2 = 0;
+            const uint4* src4 = reinterpret_cast<const uint4*>(&tile[rr][32 * b]);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                w[q] = src4[q];
-                m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(m2, w[q].x), w[q].y), w[q].z), w[q].w);
-            }
-            uint8_t sf;
-            float inv;
-            if constexpr (FP4) mx_scale_bits_e2m1(absmax_to_f32_bits(m2), &sf, &inv);
-            else mx_scale_bits(absmax_to_f32_bits(m2), &sf, &inv);
-            long long r = r0 + rr;
-            if (gate_up_I > 0) {  // 128-row blocks of [64 gate rows | 64 up rows] per expert
-                const long long e = r / (2 * gate_up_I), j = r % (2 * gate_up_I);
-                const long long jj = j < gate_up_I ? j : j - gate_up_I;
-                r = e * 2 * gate_up_I + 128 * (jj / 64) + (j < gate_up_I ? 0 : 64) + jj % 64;
-            }
-            s_sfr[16 * rr + 4 * sub + b] = sf;                      // tile row 32 sub + rr
-            if constexpr (FP4) {
-                uint32_t o[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) o[q] = e2m1x8(w[q], inv);
-                *reinterpret_cast<uint4*>(q_row + r * (C / 2) + (c0 + 32 * b) / 2) = make_uint4(o[0], o[1], o[2], o[3]);
-            } else {
-                uint2 o[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) o[q] = e4m3x8(w[q], inv);
-                uint4* dst = reinterpret_cast<uint4*>(q_row + r * C + c0 + 32 * b);
-                dst[0] = make_uint4(o[0].x, o[0].y, o[1].x, o[1].y);
-                dst[1] = make_uint4(o[2].x, o[2].y, o[3].x, o[3].y);
-            }
+            for (int q = 0; q < 4; ++q) w[q] = src4[q];
+            emit_row(w, sub);
         }
         if (!FP4 && q_col) {
             // thread -> columns 2 cp, 2 cp + 1 (cp = 32 (warp & 1) + lane) over rows 16 rh .. + 15
@@ -164,14 +208,14 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
                 *reinterpret_cast<uint16_t*>(&qt[16 * rh + j][2 * cp]) =
                     to_e4m3x2(__uint_as_float(w[j] << 16) * inv0, __uint_as_float(w[j] & 0xFFFF0000u) * inv1);
             if (rh == 0) {   // columns 2 cp, 2 cp + 1, row block sub
-                const int c0 = 2 * cp, c1 = 2 * cp + 1;
-                s_sfc[16 * (c0 & 31) + 4 * (c0 >> 5) + sub] = sf0;
-                s_sfc[16 * (c1 & 31) + 4 * (c1 >> 5) + sub] = sf1;
+                const int ca = 2 * cp, cb = 2 * cp + 1;
+                s_sfc[16 * (ca & 31) + 4 * (ca >> 5) + sub] = sf0;
+                s_sfc[16 * (cb & 31) + 4 * (cb >> 5) + sub] = sf1;
             }
             __syncthreads();
-            const int rr = t >> 2, q = t & 3;
-            const uint4* s4 = reinterpret_cast<const uint4*>(&qt[rr][32 * q]);
-            uint4* dst = reinterpret_cast<uint4*>(q_col + (r0 + rr) * C + c0 + 32 * q);
+            // the 32 x 128 codes out, thread -> (row t/4, 32 columns at 32 (t%4))
+            const uint4* s4 = reinterpret_cast<const uint4*>(&qt[rr][32 * b]);
+            uint4* dst = reinterpret_cast<uint4*>(q_col + (r0 + rr) * C + c0 + 32 * b);
             dst[0] = s4[0];
             dst[1] = s4[1];
         }
@@ -180,19 +224,7 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
     // the tile's two scale atoms, 16 bytes per thread
     if (q_row && gate_up_I <= 0 && t < 32)
         reinterpret_cast<uint4*>(sf_row + sf_index(rt, c0 >> 5, C / 128))[t] = reinterpret_cast<const uint4*>(s_sfr)[t];
-    if (q_row && gate_up_I > 0 && t < 64) {
-        // gate/up order: the tile (128 rows, all gate or all up, as 128 divides I) fills one half of
-        // two destination atoms, its rows [0, 64) the half at `off` of block jb / 64 and rows
-        // [64, 128) that of the next block; atom row p's four bytes sit at 16 (p % 32) + 4 ((p / 32) % 4),
-        // so each 32-row slice of a half is 8 contiguous bytes per p % 32
-        const long long e = rt / (2 * gate_up_I), j = rt % (2 * gate_up_I);
-        const bool up = j >= gate_up_I;
-        const long long jb = up ? j - gate_up_I : j;                  // a multiple of 128
-        const int half = t >> 5, m = t & 31;
-        const long long blk = e * 2 * gate_up_I + 128 * (jb / 64 + half);   // destination block's first row
-        uint8_t* dst = sf_row + sf_index(blk, c0 >> 5, C / 128) + 16 * m + (up ? 8 : 0);
-        *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(s_sfr + 16 * m + 8 * half);
-    }
+    if (q_row && gate_up_I > 0) store_gate_up_scales();
     if (!FP4 && q_col && t >= 32 && t < 64)
         reinterpret_cast<uint4*>(sf_col + sf_index(c0, rt >> 5, R_max / 128))[t - 32] =
             reinterpret_cast<const uint4*>(s_sfc)[t - 32];
