@@ -289,10 +289,11 @@ __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& 
 
 // Stages of the smem ring: a CTA pair driving one MMA (TWO) holds only half of each B tile per
 // CTA, which leaves room for six.
-// pipeline stages: six for the two-SM BF16 tiles and the 128 x 128 MXFP8 tiles (33 KB a stage),
-// four otherwise
-template <bool TWO, bool MX, int BN>
-constexpr int ring_stages() { return (TWO || (MX && BN == 128)) ? 6 : kStages; }
+// pipeline stages: six for the two-SM BF16 tiles and the 128 x 128 MXFP8 weight-gradient tiles
+// (33 KB a stage), four otherwise (the MXFP8 SwiGLU backward, bound by its epilogue, measured
+// 578 µs with four against 592-596 µs with six)
+template <bool TWO, bool MX, int BN, bool WGRAD>
+constexpr int ring_stages() { return (TWO || (MX && BN == 128 && WGRAD)) ? 6 : kStages; }
 
 // PAIR: clusters of two CTAs on two m-tiles of one expert and the same n-tile.  Without TWO each
 // CTA runs its own MMAs and the pair only shares B by TMA multicast; with TWO the leader CTA
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const GemmArgs a) {
     static_assert(!TWO || (PAIR && !MX), "two-SM MMAs run in CTA pairs, BF16 only");
-    constexpr int kStages = ring_stages<TWO, MX, BN>();
+    constexpr int kStages = ring_stages<TWO, MX, BN, WGRAD>();
     constexpr int kElems = MX ? 128 : 64;                // K elements per stage
     constexpr int kMmaK = MX ? 32 : 16;                  // K elements per MMA
     constexpr int kMnChunk = MX ? 128 : 64;              // MN elements per 128-byte row (MN-major)
@@ -984,7 +985,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     const size_t out_bytes = tma_out<EPI, MX, BN>()
                                  ? (size_t)epi_warps<EPI, MX && BN == 256>() * out_box_bytes<EPI, MX && BN == 256>()
                                  : 0;
-    const size_t fixed = 1024 + ring_stages<TWO, MX, BN>() * stage + out_bytes + 256;
+    const size_t fixed = 1024 + ring_stages<TWO, MX, BN, WGRAD>() * stage + out_bytes + 256;
     if (tma_out<EPI, MX, BN>() && !tc) return cudaErrorInvalidValue;
     const CUtensorMap& tcm = tc ? *tc : ta;   // kernels without a TMA-stored output never read it
     const CUtensorMap& tdm = td ? *td : tcm;
