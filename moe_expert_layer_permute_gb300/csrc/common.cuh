@@ -391,7 +391,14 @@ __device__ __forceinline__ void store_f32x32(float* dst, const float* v) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
-__device__ __forceinline__ float sigmoidf_fast(float z) { return __frcp_rn(1.0f + __expf(-z)); }
+// 1/x by the hardware's approximate reciprocal (rcp.approx, about 1 ulp; subnormals flushed).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+// sigmoid(z) = 1 / (1 + e^-z); 1 + e^-z is at least 1, and e^-z = inf gives 0
+__device__ __forceinline__ float sigmoidf_fast(float z) { return rcp_approx(1.0f + __expf(-z)); }
 
 // ------------------------------------------------------------------------------------------
 // MXFP8 (OCP Microscaling v1.0): E4M3 values, one E8M0 scale per 32 values
