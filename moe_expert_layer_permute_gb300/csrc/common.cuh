@@ -409,20 +409,6 @@ __host__ __device__ __forceinline__ long long sf_index(long long mn, long long k
     return ((mn >> 7) * k_atoms + (kblock >> 2)) * 512 + 16 * (mn & 31) + 4 * ((mn >> 5) & 3) + (kblock & 3);
 }
 
-// Shared exponent floor(log2(amax)) - 8 (8 = the largest E4M3 exponent), clamped to the E8M0
-// range and stored biased by 127, and the exact factor 2^-exp; an all-zero block gets byte 0.
-__device__ __forceinline__ void mx_scale(float amax, uint8_t* sf, float* inv) {
-    if (!(amax > 0.f)) {
-        *sf = 0;
-        *inv = 0.f;
-        return;
-    }
-    int se = ilogbf(amax) - 8;
-    se = max(-127, min(127, se));
-    *sf = (uint8_t)(se + 127);
-    *inv = scalbnf(1.0f, -se);
-}
-
 // The same scale from the bits of a non-negative finite amax.  For a normal amax the biased
 // exponent field is floor(log2(amax)) + 127, so the scale byte floor(log2(amax)) - 8 + 127 is the
 // field - 8; fields below 9 (amax < 2^-118, subnormals and zero) all clamp to byte 0.  2^-exp
