@@ -409,10 +409,11 @@ __host__ __device__ __forceinline__ long long sf_index(long long mn, long long k
     return ((mn >> 7) * k_atoms + (kblock >> 2)) * 512 + 16 * (mn & 31) + 4 * ((mn >> 5) & 3) + (kblock & 3);
 }
 
-// The same scale from the bits of a non-negative finite amax.  For a normal amax the biased
-// exponent field is floor(log2(amax)) + 127, so the scale byte floor(log2(amax)) - 8 + 127 is the
-// field - 8; fields below 9 (amax < 2^-118, subnormals and zero) all clamp to byte 0.  2^-exp
-// then has the biased exponent 254 - byte, always a normal float.
+// MXFP8 block scale from the bits of a non-negative finite amax: the shared exponent
+// floor(log2(amax)) - 8 (8 = the largest E4M3 exponent), stored biased by 127 in one byte, and the
+// exact factor 2^-exp.  For a normal amax the biased exponent field is floor(log2(amax)) + 127, so
+// the byte is the field - 8; fields below 9 (amax < 2^-118, subnormals and zero) all clamp to
+// byte 0.  2^-exp then has the biased exponent 254 - byte, always a normal float.
 __device__ __forceinline__ void mx_scale_bits(uint32_t amax_bits, uint8_t* sf, float* inv) {
     const int b = max((int)(amax_bits >> 23) - 8, 0);
     *sf = (uint8_t)b;
