@@ -41,6 +41,7 @@ def parse_args():
     p.add_argument("--config", default="qwen3_30b_a3b")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-mx", action="store_true", help="skip the MXFP8 measurement of the same layer")
+    p.add_argument("--no-extra", action="store_true", help="skip the 235B-shaped and Zipf-routed workloads")
     return p.parse_args()
 
 
@@ -137,11 +138,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------ ours
-# DRAM bytes (read + write) per launch from one ncu capture of the current build, scaled to the
-# named workload: profiles/gemm_fwd_gate_up_bf16_profile_30b_e32.md (profile_30b_e32, the forward
-# that saves [g|u]: 343.6 MB read + 124.6 MB written; every size scales with E at equal per-expert
-# work, so x4 for the 128-expert layer).  Kernels not captured since their last change are absent.
-PROFILED_TRAFFIC = {("qwen3_30b_a3b", "gemm_fwd_gate_up_swiglu"): 4 * (343.474e6 + 124.403e6)}
+# DRAM bytes (read + write) per launch of a kernel, from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum) of the current build on the profile_30b_e32 workload (4096 tokens, 32
+# experts: the 30B layer's per-expert work), scaled x4 to the 128-expert layer, since every size
+# grows with E at equal per-expert work.  A kernel changed since its capture is left out (null).
+PROFILED_TRAFFIC = {}
 
 GEMM_FLOPS = {  # algorithmic FLOPs per launch of each grouped GEMM (BF16 or MXFP8), in units of S*H*I
     "gemm_fwd_gate_up_swiglu": 4, "gemm_fwd_gate_up_save": 4, "gemm_fwd_down_weighted": 2,
@@ -224,8 +225,10 @@ def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
     import torch
 
     dev = torch.device("cuda", local)
-    inp = gen.make_inputs(cfg)
-    h_in = {n: host_tensor(getattr(inp, n)).pin_memory() for n in ("x", "topk_idx", "topk_w", "W13", "W2", "dy")}
+    inp = cached_inputs(gen, cfg)
+    h_in = {n: host_tensor(getattr(inp, n)) for n in ("x", "topk_idx", "topk_w", "W13", "W2", "dy")}
+    if with_e2e:   # the end-to-end leg copies its per-step inputs from pinned host memory
+        h_in = {n: (t.pin_memory() if n not in ("W13", "W2") else t) for n, t in h_in.items()}
     del inp
     d = {n: t.to(dev) for n, t in h_in.items()}
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
@@ -253,7 +256,9 @@ def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
 
     def step():
         # one training step of the checkpointed layer: the weights (and their MXFP8 copies) are
-        # made once, the recompute saves [g|u], the backward reuses both
+        # made once, the recompute saves [g|u], the backward reuses both; a new step is a new epoch
+        # (an optimizer would have updated the weights in place)
+        sc.epoch += 1
         fwd()
         fwd(bd.MOE_FLAG_SAVE_GU | RW)
         bwd(bd.MOE_FLAG_REUSE_FWD | RW)
@@ -306,6 +311,7 @@ def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
 
         def layer_step(bi, bo):
             args = (bi["topk_idx"], bi["topk_w"], d["W13"], d["W2"])
+            sc.epoch += 1
             bd.moe_fwd(bi["x"], *args, bo["y"], sc, flags=0)
             bd.moe_fwd(bi["x"], *args, bo["y"], sc, flags=bd.MOE_FLAG_SAVE_GU | RW)
             bd.moe_bwd(bi["dy"], bi["x"], *args, bo["dx"], d["dW13"], d["dW2"], bo["dtw"], sc,
@@ -353,7 +359,7 @@ def fwd_measure(bd, gen, cfg, steps, warmup, ws, local, peak, peak_src):
     import torch
 
     dev = torch.device("cuda", local)
-    inp = gen.make_inputs(cfg)
+    inp = cached_inputs(gen, cfg)
     d = {n: host_tensor(getattr(inp, n)).to(dev) for n in ("x", "topk_idx", "topk_w", "W13", "W2")}
     del inp
     d["y"] = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
@@ -485,6 +491,63 @@ def summarize(m, peak, peak_src):
             "clocks": m["clocks"], "device_status": m["status"]}
 
 
+# Workloads measured beside the headline one in the default run, each as its own checkpointed
+# layer step: the Qwen3-235B-A22B-shaped layer in BF16 and MXFP8, and Zipf-skewed routing on the
+# 30B shape at 16,384 and 4,096 tokens.
+EXTRA_WORKLOADS = ("qwen3_235b_a22b", "qwen3_235b_a22b_mxfp8", "skew_zipf_16k", "skew_zipf_4k")
+
+
+def peak_table(peaks, src):
+    """Denominators of the fractions.  The timed regions are short (tens of steps, well under a
+    second), so the headline divides by the measured burst bf16 rate; the sustained rate, taken over
+    a seconds-long loop at a lower SM clock, is reported beside it."""
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sust = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    sust_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
+    # MXFP8 at the recipe's nominal dense ratio 4.5 : 2.25; fp8_bwd: two BF16 forwards (2F) and one
+    # MXFP8 backward (2F), so its peak is the harmonic blend 4F / (2F / P + 2F / 2P) = 4P / 3
+    def by_prec(p):
+        return {"bf16": p, "mxfp8": 2.0 * p, "fp8_bwd": 4.0 * p / 3.0, "fp8_fp4": 2.0 * p}
+    names = {"bf16": "", "mxfp8": " x 2 (nominal MXFP8:BF16 ratio)",
+             "fp8_bwd": " blended with 2x it (BF16 forwards, MXFP8 backward): 4/3 x",
+             "fp8_fp4": " x 2 (nominal FP8:BF16 ratio; kind::mxf8f6f4 runs E2M1 at it)"}
+    return {"burst": by_prec(burst), "sustained": by_prec(sust), "sustained_mhz": sust_mhz,
+            "src": {k: f"{src} bf16_tflops (burst){v}" for k, v in names.items()}}
+
+
+_INPUT_CACHE = {}
+
+
+def cached_inputs(gen, cfg):
+    """Seeded inputs of a workload; workloads that differ only in precision share them."""
+    key = (cfg.seed, cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.routing)
+    if key not in _INPUT_CACHE:
+        _INPUT_CACHE.clear()
+        _INPUT_CACHE[key] = gen.make_inputs(cfg)
+    return _INPUT_CACHE[key]
+
+
+def secondary_fracs(sm, prec, pk):
+    """The full layer's fraction of the sustained peak, with the clocks behind both numbers."""
+    return {"frac_of_sustained_peak": sm["full_tflops"] / pk["sustained"][prec],
+            "sustained_peak_tflops": pk["sustained"][prec], "sustained_peak_sm_mhz": pk["sustained_mhz"],
+            "run_sm_mhz": (sm.get("clocks") or {}).get("sm_mhz")}
+
+
+def compact(name, sm):
+    """One workload's headline numbers (repeated last in the JSON line)."""
+    r = {k: round(sm[k], 4) for k in ("fwd_ms", "bwd_ms", "full_ms", "full_tflops", "frac_of_peak") if k in sm}
+    if "fwd_ms_reuse_weights" in sm:
+        r.update({"fwd_ms_reuse_weights": round(sm["fwd_ms_reuse_weights"], 4),
+                  "fwd_tflops_reuse_weights": round(sm["fwd_tflops_reuse_weights"], 1),
+                  "frac_of_peak": round(sm["frac_of_peak_reuse_weights"], 4)})
+    if sm.get("roofline"):
+        r["top_kernel"] = sm["roofline"]["kernel"]
+        r["top_kernel_frac"] = round(sm["roofline"]["frac"], 4)
+    r["sm_mhz"] = (sm.get("clocks") or {}).get("sm_mhz")
+    return r
+
+
 def run_ours(args, rank, ws, local):
     import torch
 
@@ -496,16 +559,13 @@ def run_ours(args, rank, ws, local):
     torch.cuda.set_device(local)
     cfg = gen.CONFIGS[args.config]
     peaks, src = load_peaks()
-    bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    # the recipe's nominal dense ratio MXFP8 : BF16 is 4.5 : 2.25
-    mx_peak = 2.0 * bf16_peak
-    # fp8_bwd: the checkpointed layer is two BF16 forwards (2F) and one MXFP8 backward (2F), so its
-    # peak is the harmonic blend 4F / (2F / P_bf16 + 2F / P_mx)
-    blend_peak = 2.0 * bf16_peak * mx_peak / (bf16_peak + mx_peak)
+    pk = peak_table(peaks, src)
+    summary = {}
     if cfg.precision == "fp8_fp4":
         # a forward-only layer: the line is its forward with the weight copies made once
-        psrc = f"{src} bf16_tflops_sustained x 2 (nominal FP8:BF16 ratio; kind::mxf8f6f4 runs E2M1 at it)"
-        f4 = fwd_measure(bd, gen, cfg, args.steps, args.warmup, ws, local, mx_peak, psrc)
+        f4 = fwd_measure(bd, gen, cfg, args.steps, args.warmup, ws, local, pk["burst"]["fp8_fp4"],
+                         pk["src"]["fp8_fp4"])
+        summary[cfg.name] = compact(cfg.name, f4)
         return {
             "metric": METRIC, "value": f4["fwd_tflops_reuse_weights"] * ws, "unit": "TFLOP/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": f4["fwd_ms_reuse_weights"],
@@ -517,67 +577,69 @@ def run_ours(args, rank, ws, local):
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
             "roofline": f4["roofline"], "gpu_launches": f4["gpu_launches_per_fwd"] * args.steps,
             "clocks": f4["clocks"], "device_status": f4["device_status"], "fp8_fp4_fwd": f4, "cpu_baseline": None,
+            "summary": summary,
         }
-    is_mx = cfg.precision == "mxfp8"
-    peak = {"bf16": bf16_peak, "mxfp8": mx_peak, "fp8_bwd": blend_peak}[cfg.precision]
-    peak_src = (f"{src} bf16_tflops_sustained" + {"bf16": "", "mxfp8": " x 2 (nominal MXFP8:BF16 ratio)",
-                                                  "fp8_bwd": " blended with 2x it (BF16 forwards, MXFP8 backward)"}[
-                    cfg.precision] + " (kernel timed inside a long step)")
+    prec = cfg.precision
     m = measure(bd, gen, cfg, args.steps, args.warmup, ws, local, with_e2e=True)
-    sm = summarize(m, peak, peak_src)
+    sm = summarize(m, pk["burst"][prec], pk["src"][prec])
     line = {
         "metric": METRIC, "value": sm["full_tflops"] * ws, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sm["full_ms"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {"bf16": "bf16", "mxfp8": "mxfp8-e4m3", "fp8_bwd": "bf16 fwd / mxfp8-e4m3 bwd"}[cfg.precision],
+        "dtype": {"bf16": "bf16", "mxfp8": "mxfp8-e4m3", "fp8_bwd": "bf16 fwd / mxfp8-e4m3 bwd"}[prec],
         "data": "synthetic: seeded N(0,1) x/dy, N(0,1/sqrt(fan_in)) weights, uniform top-8 routing, softmax weights",
-        "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} k={cfg.k} {cfg.precision} "
+        "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} k={cfg.k} {prec} "
                                f"{cfg.routing} routing",
                    "step": "fwd + fwd(save [g|u]) + bwd(reuse)", "parallelism": "replicas" if ws > 1 else "single GPU",
                    "l2": "inputs larger than L2 (weights alone 1.13 GiB per step)"},
-        "peak_tflops": {"value": peak, "source": peak_src},
+        "peak_tflops": {"value": pk["burst"][prec], "source": pk["src"][prec]},
     }
     line.update({k: v for k, v in sm.items() if k not in ("clocks", "device_status")})
+    line.update(secondary_fracs(sm, prec, pk))
     line["e2e"] = {"value": 4 * cfg.fwd_flops() / (m["e2e_ms"] * 1e-3) / 1e12 * ws, "unit": "TFLOP/s",
                    "ms_per_step": m["e2e_ms"], "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
                    "copies": m["e2e_copies"]}
     line["clocks"] = sm["clocks"]
     line["device_status"] = sm["device_status"]
-    if not args.no_mx and not is_mx and args.config + "_mxfp8" in gen.CONFIGS:
-        # the same layer in MXFP8 (E4M3 + E8M0 per 32 along K, fp32 weight gradients)
-        mcfg = gen.CONFIGS[args.config + "_mxfp8"]
-        mm = measure(bd, gen, mcfg, args.steps, args.warmup, ws, local, with_e2e=False)
-        msrc = f"{src} bf16_tflops_sustained x 2 (nominal MXFP8:BF16 ratio)"
-        ms = summarize(mm, mx_peak, msrc)
-        ms["workload"] = mcfg.name
-        ms["peak_tflops"] = {"value": mx_peak, "source": msrc}
-        line["mxfp8"] = ms
-    if not args.no_mx and cfg.precision == "bf16" and args.config + "_fp8_bwd" in gen.CONFIGS:
-        # the same layer with the BF16 forward and the MXFP8 backward
-        fcfg = gen.CONFIGS[args.config + "_fp8_bwd"]
-        fm = measure(bd, gen, fcfg, args.steps, args.warmup, ws, local, with_e2e=False)
-        fsrc = f"{src} bf16_tflops_sustained blended with 2x it (BF16 forwards, MXFP8 backward)"
-        fs = summarize(fm, blend_peak, fsrc)
-        fs["workload"] = fcfg.name
-        fs["peak_tflops"] = {"value": blend_peak, "source": fsrc}
-        line["fp8_bwd"] = fs
-    if not args.no_mx and cfg.precision == "bf16" and args.config + "_fp8_fp4" in gen.CONFIGS:
-        # the forward-only FP8 x FP4 layer (E4M3 activations x E2M1 weights run at the FP8 rate),
-        # beside the MXFP8 forward with its weight copies made once too
-        psrc = f"{src} bf16_tflops_sustained x 2 (nominal FP8:BF16 ratio; kind::mxf8f6f4 runs E2M1 at it)"
-        f4 = fwd_measure(bd, gen, gen.CONFIGS[args.config + "_fp8_fp4"], args.steps, args.warmup, ws, local,
-                         mx_peak, psrc)
-        if args.config + "_mxfp8" in gen.CONFIGS:
-            f8 = fwd_measure(bd, gen, gen.CONFIGS[args.config + "_mxfp8"], args.steps, args.warmup, ws, local,
-                             mx_peak, psrc)
-            f4["mxfp8_fwd_ms_reuse_weights"] = f8["fwd_ms_reuse_weights"]
-        line["fp8_fp4_fwd"] = f4
+    summary[cfg.name] = compact(cfg.name, sm)
+
+    def side(name, steps):
+        c = gen.CONFIGS[name]
+        mm = measure(bd, gen, c, steps, args.warmup, ws, local, with_e2e=False)
+        r = summarize(mm, pk["burst"][c.precision], pk["src"][c.precision])
+        r["workload"] = f"{c.name}: T={c.T} H={c.H} I={c.I} E={c.E} k={c.k} {c.precision} {c.routing} routing"
+        r["peak_tflops"] = {"value": pk["burst"][c.precision], "source": pk["src"][c.precision]}
+        r.update(secondary_fracs(r, c.precision, pk))
+        summary[c.name] = compact(c.name, r)
+        return r
+
+    if not args.no_mx and prec == "bf16":
+        # the same layer in MXFP8 (E4M3 + E8M0 per 32 along K, fp32 weight gradients) and with the
+        # BF16 forward and the MXFP8 backward
+        for suffix in ("_mxfp8", "_fp8_bwd"):
+            if args.config + suffix in gen.CONFIGS:
+                line[suffix[1:]] = side(args.config + suffix, args.steps)
+        if args.config + "_fp8_fp4" in gen.CONFIGS:
+            # the forward-only FP8 x FP4 layer beside the MXFP8 forward, both with weight copies made once
+            f4 = fwd_measure(bd, gen, gen.CONFIGS[args.config + "_fp8_fp4"], args.steps, args.warmup, ws, local,
+                             pk["burst"]["fp8_fp4"], pk["src"]["fp8_fp4"])
+            if args.config + "_mxfp8" in gen.CONFIGS:
+                f8 = fwd_measure(bd, gen, gen.CONFIGS[args.config + "_mxfp8"], args.steps, args.warmup, ws, local,
+                                 pk["burst"]["mxfp8"], pk["src"]["mxfp8"])
+                f4["mxfp8_fwd_ms_reuse_weights"] = f8["fwd_ms_reuse_weights"]
+            line["fp8_fp4_fwd"] = f4
+            summary[args.config + "_fp8_fp4"] = compact(args.config + "_fp8_fp4", f4)
+    if not args.no_extra and args.config == "qwen3_30b_a3b":
+        line["workloads"] = {n: side(n, min(args.steps, 20)) for n in EXTRA_WORKLOADS
+                             if not (args.no_mx and gen.CONFIGS[n].precision != "bf16")}
     # the router that precedes the layer (outside the layer step, as in the pages' benchmark)
     line["router"] = router_measure(bd, gen, cfg, 20, peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, budget_s=20.0)
     elif rank == 0:
         line["cpu_baseline"] = None
+    summary["router"] = {"fwd_us": round(line["router"]["fwd_us"], 2), "bwd_us": round(line["router"]["bwd_us"], 2)}
+    line["summary"] = summary      # last, so that a truncated log keeps every workload's headline
     return line
 
 

@@ -82,23 +82,28 @@ typedef struct {
  * forward of an activation-checkpointed layer is that recompute). */
 #define MOE_FLAG_SAVE_GU     0x1u
 /* moe_bwd reuses the routing, the dispatched rows and [g|u] left in scratch by the latest moe_fwd
- * that had MOE_FLAG_SAVE_GU and the same x, topk_idx, topk_w, W13, W2 pointers and desc; returns
- * MOE_ERR_STATE if the scratch handle does not record such a forward. */
+ * that had MOE_FLAG_SAVE_GU and the same x, topk_idx, topk_w, W13, W2 pointers, desc and epoch;
+ * returns MOE_ERR_STATE (before any launch) if the scratch handle does not record such a forward. */
 #define MOE_FLAG_REUSE_FWD   0x2u
 /* Block-scaled precisions only (MOE_MXFP8, MOE_FP8_BWD, MOE_FP8_FP4): W13 and W2 hold the same
- * values as when an earlier call on this scratch (same pointers) quantised them, so their E4M3 /
- * E2M1 copies in scratch are reused instead of being made again (a training step quantises its
- * weights once: forward, recompute and backward share them; a forward-only layer keeps them).
- * Returns MOE_ERR_STATE if the scratch handle records no quantisation of these pointers. */
+ * values as when an earlier call on this scratch (same pointers, same epoch) quantised them, so
+ * their E4M3 / E2M1 copies in scratch are reused instead of being made again (a training step
+ * quantises its weights once: forward, recompute and backward share them; a forward-only layer
+ * keeps them).  Returns MOE_ERR_STATE (before any launch) if the scratch handle records no
+ * quantisation of these pointers at the current epoch. */
 #define MOE_FLAG_REUSE_WEIGHTS 0x4u
 
 /* Host-side handle of a caller-owned device scratch buffer of at least moe_scratch_bytes(desc)
- * bytes.  `state` is written by the library (which forward's results the buffer holds); zero it
- * when the handle is created. */
+ * bytes.  `epoch` is the caller's: a counter it advances whenever x, W13 or W2 may have changed in
+ * place at the same addresses (an optimizer step updates the weights in place), so that the reuse
+ * flags refuse results made before the change.  `state` is written by the library (which forward's
+ * results and which weight copies the buffer holds, and the wait settings of
+ * moe_set_wait_limit); zero `epoch` and `state` when the handle is created. */
 typedef struct {
     void*    data;
     uint64_t bytes;
     moe_desc desc;
+    uint64_t epoch;
     uint64_t state[4];
 } moe_scratch;
 
@@ -144,6 +149,19 @@ int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_id
  * clears it.  Returns MOE_OK, or MOE_ERR_CUDA if the synchronisation itself failed. */
 int moe_read_device_status(moe_scratch* scratch, void* stream, int* status);
 
+/* Every wait of the grouped GEMMs' pipelines is bounded: a wait that lasts longer than the limit
+ * gives up, the kernel records MOE_DEV_TIMEOUT in the status word, drains what it has in flight,
+ * frees its tensor memory and returns (it never traps or hangs: a lesson the pages draw from a
+ * persistent kernel that deadlocked, ic.work analysis, section "算子下沉时代的硬件死锁暗礁").
+ * moe_set_wait_limit sets, for later calls on this scratch handle, the limit in SM clock cycles
+ * (0 restores the default, 4e9 cycles, about 2 s at the maximum SM clock) and test flags:
+ * MOE_TEST_WITHHOLD_LOADS makes the grouped GEMMs issue no operand loads, so that their waits run
+ * out with no copy in flight, which tests this path (outputs are then unspecified).  Host-side
+ * only (stored in scratch->state); returns MOE_ERR_NULL for a NULL handle, MOE_ERR_SHAPE for a
+ * negative limit. */
+#define MOE_TEST_WITHHOLD_LOADS 0x1u
+int moe_set_wait_limit(moe_scratch* scratch, int64_t wait_cycles, uint32_t test_flags);
+
 /* Static message for a MOE_ERR_* code. */
 const char* moe_strerror(int code);
 
@@ -176,7 +194,9 @@ int moe_router_bwd(const moe_tensor* topk_idx, const moe_tensor* topk_w, const m
  * would synchronise the device).  It computes the same routing bookkeeping as moe_fwd:
  *   counts  int32[E]     tokens routed to each expert
  *   offsets int32[E+1]   exclusive prefix of counts
- *   perm    int32[T*k]   slot at each sorted position, stable in slot order s = t*k + j
+ *   perm    int32[T*k]   slot at each sorted position, stable in slot order s = t*k + j; slots
+ *                        whose id is outside [0, E) are dropped, and the positions they leave free,
+ *                        [offsets[E], T*k), hold -1
  *   inv     int32[T*k]   sorted position of each slot (-1 for a slot whose id is outside [0, E))
  * from topk_idx int32[T, k] (all device pointers, 4-byte aligned, caller-owned), asynchronously on
  * `stream`.  It allocates nothing: its working memory is a file-scope static device array of
@@ -193,7 +213,8 @@ int moe_route_static(const int32_t* topk_idx, int64_t T, int64_t k, int64_t E, i
  *   MOE_VIEW_COUNTS   int32[E]        tokens routed to each expert
  *   MOE_VIEW_OFFSETS  int32[E+1]      exclusive prefix of the counts (group offsets)
  *   MOE_VIEW_PERM     int32[T*k]      slot (t*k+j) at each sorted position, stable in slot order
- *   MOE_VIEW_INV      int32[T*k]      sorted position of each slot
+ *                                     (-1 in the positions [OFFSETS[E], T*k) that dropped slots free)
+ *   MOE_VIEW_INV      int32[T*k]      sorted position of each slot (-1 for a dropped slot)
  *   MOE_VIEW_PAD_OFFSETS int32[E+1]   start row of each expert in the padded row layout
  *   MOE_VIEW_XPERM    bf16 [rows, H]  dispatched x rows (padded layout: expert e's rows start at
  *                                     PAD_OFFSETS[e], padding rows are zero)

@@ -21,6 +21,7 @@ MOE_FLAG_SAVE_GU, MOE_FLAG_REUSE_FWD, MOE_FLAG_REUSE_WEIGHTS = 0x1, 0x2, 0x4
 (MOE_VIEW_COUNTS, MOE_VIEW_OFFSETS, MOE_VIEW_PERM, MOE_VIEW_INV, MOE_VIEW_PAD_OFFSETS, MOE_VIEW_XPERM,
  MOE_VIEW_HID, MOE_VIEW_GU, MOE_VIEW_YPART, MOE_VIEW_DG, MOE_VIEW_HW, MOE_VIEW_DYPERM) = range(12)
 MOE_DEV_OK, MOE_DEV_BAD_EXPERT, MOE_DEV_TIMEOUT = 0, 1, 2
+MOE_TEST_WITHHOLD_LOADS = 0x1
 MX_VIEWS = {name: 32 + i for i, name in enumerate(
     ["x_r", "x_r_sf", "x_c", "x_c_sf", "h_r", "h_r_sf", "dy_r", "dy_r_sf", "dy_c", "dy_c_sf", "dg_r", "dg_r_sf",
      "dg_c", "dg_c_sf", "hw_c", "hw_c_sf", "w13_r", "w13_r_sf", "w13_c", "w13_c_sf", "w2_r", "w2_r_sf", "w2_c",
@@ -33,7 +34,7 @@ ERR = {v: k for k, v in ERRORS.items()}
 # every symbol the header declares
 EXPORTS = ("moe_scratch_bytes", "moe_fwd", "moe_bwd", "moe_read_device_status", "moe_strerror",
            "moe_scratch_view", "moe_trace_enable", "moe_trace_reset", "moe_trace_read", "moe_route_static",
-           "moe_router_fwd", "moe_router_bwd")
+           "moe_router_fwd", "moe_router_bwd", "moe_set_wait_limit")
 
 
 class MoeTensor(ctypes.Structure):
@@ -48,7 +49,7 @@ class MoeDesc(ctypes.Structure):
 
 class MoeScratch(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("bytes", ctypes.c_uint64), ("desc", MoeDesc),
-                ("state", ctypes.c_uint64 * 4)]
+                ("epoch", ctypes.c_uint64), ("state", ctypes.c_uint64 * 4)]
 
 
 _P = ctypes.POINTER
@@ -84,6 +85,8 @@ def _load() -> ctypes.CDLL:
     lib.moe_router_fwd.restype = ctypes.c_int
     lib.moe_router_bwd.argtypes = [_P(MoeTensor)] * 4 + [ctypes.c_void_p]
     lib.moe_router_bwd.restype = ctypes.c_int
+    lib.moe_set_wait_limit.argtypes = [_P(MoeScratch), ctypes.c_int64, ctypes.c_uint32]
+    lib.moe_set_wait_limit.restype = ctypes.c_int
     return lib
 
 
@@ -148,6 +151,21 @@ class Scratch:
     @property
     def desc(self) -> MoeDesc:
         return self.handle.desc
+
+    @property
+    def epoch(self) -> int:
+        """The caller's counter of in-place updates of x / W13 / W2 (see MOE_FLAG_REUSE_*)."""
+        return int(self.handle.epoch)
+
+    @epoch.setter
+    def epoch(self, value: int) -> None:
+        self.handle.epoch = value
+
+    def set_wait_limit(self, cycles: int = 0, test_flags: int = 0) -> None:
+        """Pipeline wait limit in SM cycles for later calls (0: the default) and MOE_TEST_* flags."""
+        rc = LIB.moe_set_wait_limit(ctypes.byref(self.handle), cycles, test_flags)
+        if rc:
+            raise MoeError(rc, "moe_set_wait_limit")
 
     def view(self, which: int, dtype: torch.dtype, shape) -> torch.Tensor:
         off, nbytes = view_span(self.handle.desc, which)

@@ -22,8 +22,12 @@ __device__ __forceinline__ void set_status(int* status, int code) {
 }
 
 // A wait that outlives this many SM cycles (about 2 s at 2 GHz) is treated as a hang: the
-// kernel records MOE_DEV_TIMEOUT and leaves its loops.  Legitimate waits are microseconds.
+// kernel records MOE_DEV_TIMEOUT and leaves its loops.  Legitimate waits are microseconds.  This is
+// the default; a caller may set another limit per scratch buffer (moe_set_wait_limit).
 constexpr long long kWaitTimeoutCycles = 4000000000ll;
+// While a kernel that gave up drains its in-flight copies and MMAs before exiting, each wait is
+// bounded by this many cycles whatever the configured limit (in-flight work ends in microseconds).
+constexpr long long kDrainCycles = kWaitTimeoutCycles / 8;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,15 +61,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Gives up (returns false) when
-// *abort becomes non-zero or the wait exceeds kWaitTimeoutCycles; in the latter case it raises
-// *abort itself and records MOE_DEV_TIMEOUT.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+// *abort becomes non-zero or the wait exceeds `limit` cycles; in the latter case it raises *abort
+// itself and records MOE_DEV_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                          long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitTimeoutCycles) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             set_status(status, MOE_DEV_TIMEOUT);
             return false;
@@ -121,7 +126,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
-// ---- clusters of two CTAs: B tiles multicast to both, stage releases signalled to both ------
+// ---- clusters of two CTAs (two-SM MMAs): rank, cluster barrier ---------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -132,25 +137,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// TMA tile load delivered to the same shared-memory offset in every CTA of `mask`; each
-// destination CTA's mbarrier at `bar`'s offset receives the transaction bytes.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                             uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-
 // ------------------------------------------------------------------------------------------
 // tcgen05: tensor memory, MMA, commit, loads
 // ------------------------------------------------------------------------------------------
@@ -201,15 +187,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// As mma_commit, arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
 }
 
 // ---- CTA pairs driving one MMA (cta_group::2): the leader CTA (rank 0) issues each M = 256 MMA,
@@ -278,13 +255,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                                  long long limit) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitTimeoutCycles) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             set_status(status, MOE_DEV_TIMEOUT);
             return false;

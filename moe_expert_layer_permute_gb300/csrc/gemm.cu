@@ -153,6 +153,8 @@ struct GemmArgs {
     int r_atoms;               // padded row capacity / 128 (K atoms of the row-blocked scales)
     uint32_t b_fmt;            // B-format bits OR-ed into the block-scaled instruction descriptor
                                // (kFmtE2M1B: MXFP4 weights, unpacked to 16-byte rows by the TMA)
+    long long wait_limit;      // cycles after which a pipeline wait gives up (MOE_DEV_TIMEOUT)
+    int withhold_loads;        // test of the bounded waits: the producer issues no operand loads
 };
 
 struct Tile {
@@ -220,7 +222,7 @@ __device__ __forceinline__ Tile decode_tile(int L, const GemmArgs& a, const int*
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > kWaitTimeoutCycles / 8) break;
+        if (clock64() - t0 > kDrainCycles) break;
 }
 
 // Epilogue of a 128 x 256 MXFP8 tile from registers: d holds columns [128 h, 128 h + 128) of
@@ -295,16 +297,16 @@ __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& 
 template <bool TWO, bool MX, int BN, bool WGRAD>
 constexpr int ring_stages() { return (TWO || (MX && BN == 128 && WGRAD)) ? 6 : kStages; }
 
-// PAIR: clusters of two CTAs on two m-tiles of one expert and the same n-tile.  Without TWO each
-// CTA runs its own MMAs and the pair only shares B by TMA multicast; with TWO the leader CTA
+// TWO: clusters of two CTAs on two m-tiles of one expert and the same n-tile; the leader CTA
 // issues cta_group::2 MMAs (M = 256) over both CTAs' shared memory and tensor memory, each CTA
-// holding half of every B tile.
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool PAIR, bool TWO>
+// holding half of every B tile, which it loads itself (no load is multicast).
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool TWO>
 __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const GemmArgs a) {
-    static_assert(!TWO || (PAIR && !MX), "two-SM MMAs run in CTA pairs, BF16 only");
+    static_assert(!TWO || !MX, "two-SM MMAs run in CTA pairs, BF16 only");
+    constexpr bool PAIR = TWO;                           // clusters of two CTAs exist only for them
     constexpr int kStages = ring_stages<TWO, MX, BN, WGRAD>();
     constexpr int kElems = MX ? 128 : 64;                // K elements per stage
     constexpr int kMmaK = MX ? 32 : 16;                  // K elements per MMA
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
         }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, (PAIR && !TWO) ? 2 : 1);   // PAIR: both CTAs' MMAs release each stage
+            mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull + b, 1);
@@ -383,7 +385,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();   // the peer's barriers exist before any multicast reaches them
+    if (PAIR) cluster_sync();   // the peer's barriers exist before any copy or commit reaches them
     tc_fence_after();
     const uint32_t tmem_base = *tslot;
     const int num_tiles = WGRAD ? a.E * (PAIR ? a.m_tiles / 2 : a.m_tiles) * a.n_tiles
@@ -399,13 +401,15 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             // bytes one stage's copies complete: a packed-E2M1 B tile counts the bytes it reads
             // (half a byte a value) although it lands in shared memory as a byte a value
             const uint32_t stage_tx = kStageBytes - (a.b_fmt ? kBTileBytes / 2 : 0);
-            for (int L = unit0; L < num_tiles && ok; L += unit_stride) {
+            // (with withhold_loads nothing is issued, so the MMA warp's first wait runs out while no
+            // copy is in flight)
+            for (int L = unit0; L < num_tiles && ok && !a.withhold_loads; L += unit_stride) {
                 const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
                 // first B row of the tile (K-major B); MXFP8 gate/up weights are stored with
                 // 128-row blocks of [64 gate | 64 up] rows, so the split tile is one block
                 const int b_row0 = t.e * a.b_rows_e + ((SPLIT && MX) ? t.nt * BN : t.n0);
                 for (int kb = 0; kb < t.kb; ++kb) {
-                    if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, a.status)) { ok = false; break; }
+                    if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, a.status, a.wait_limit)) { ok = false; break; }
                     uint8_t* dA = sA + stage * kATileBytes;
                     uint8_t* dB = sB + stage * kBTileBytes;
                     const int k0 = kb * kElems;
@@ -442,26 +446,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         for (int c = 0; c < kBM / kMnChunk; ++c)
                             tma_load_2d(dA + c * kMnLbo, &tmA, full + stage, t.m0 + kMnChunk * c, t.row0 + k0);
                     }
-                    if (PAIR) {
-                        // each CTA loads half of the B tile and multicasts it to both
-                        if (!B_MN) {
-                            const int brow = (SPLIT && !MX) ? t.e * a.b_rows_e + rank * a.b_up + t.n0
-                                                            : b_row0 + rank * (BN / 2);
-                            tma_load_2d_mc(dB + rank * (BN / 2) * kRowBytes, &tmB, full + stage, k0, brow, kPeers);
-                        } else {
-                            const int krow = WGRAD ? t.row0 + k0 : t.e * a.b_rows_e + k0;
-                            constexpr int nch = BN / kMnChunk;
-                            if constexpr (nch >= 2) {
-#pragma unroll
-                                for (int c = rank * nch / 2; c < (rank + 1) * nch / 2; ++c)
-                                    tma_load_2d_mc(dB + c * kMnLbo, &tmB, full + stage, t.n0 + kMnChunk * c, krow,
-                                                   kPeers);
-                            } else {   // one MN chunk: half of its K rows each
-                                tma_load_2d_mc(dB + rank * (kElems / 2) * kRowBytes, &tmB, full + stage, t.n0,
-                                               krow + rank * (kElems / 2), kPeers);
-                            }
-                        }
-                    } else if (!B_MN) {
+                    if (!B_MN) {
                         if (SPLIT && !MX) {
                             tma_load_2d(dB, &tmB, full + stage, k0, t.e * a.b_rows_e + t.n0);
                             tma_load_2d(dB + (BN / 2) * kRowBytes, &tmB, full + stage, k0,
@@ -494,12 +479,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                                 mn_tile = t.n0 / 128 + c;
                                 kt = t.row0 / 128 + kb;
                             }
-                            if (!PAIR)
-                                bulk_load(dS + kSfAtom * (1 + c), a.sfB + (mn_tile * a.sfB_kt + kt) * kSfAtom, kSfAtom,
-                                          full + stage);
-                            else if (rank == 0)   // B's scales go to both CTAs
-                                bulk_load_mc(dS + kSfAtom * (1 + c), a.sfB + (mn_tile * a.sfB_kt + kt) * kSfAtom,
-                                             kSfAtom, full + stage, kPeers);
+                            bulk_load(dS + kSfAtom * (1 + c), a.sfB + (mn_tile * a.sfB_kt + kt) * kSfAtom, kSfAtom,
+                                      full + stage);
                         }
                     }
                     ++issued;
@@ -540,12 +521,12 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             long long consumed = 0;
             for (int L = unit0; L < num_tiles && ok; L += unit_stride) {
                 const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
-                if (!(TWO ? mbar_wait_cluster(tempty + acc, acc_phase ^ 1u, abort_flag, a.status)
-                          : mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag, a.status))) { ok = false; break; }
+                if (!(TWO ? mbar_wait_cluster(tempty + acc, acc_phase ^ 1u, abort_flag, a.status, a.wait_limit)
+                          : mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag, a.status, a.wait_limit))) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < t.kb; ++kb) {
-                    if (!mbar_wait(full + stage, phase, abort_flag, a.status)) { ok = false; break; }
+                    if (!mbar_wait(full + stage, phase, abort_flag, a.status, a.wait_limit)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = a_base + stage * kATileBytes, sb = b_base + stage * kBTileBytes;
                     if constexpr (MX) {
@@ -576,8 +557,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                     }
                     if (TWO)
                         mma_commit_pair_mc(empty + stage, kPeers);
-                    else if (PAIR)
-                        mma_commit_mc(empty + stage, kPeers);
                     else
                         mma_commit(empty + stage);
                     ++consumed;
@@ -627,7 +606,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
         uint32_t acc_phase = 0;
         for (int L = unit0; L < num_tiles; L += unit_stride) {
             const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
-            if (!mbar_wait(tfull + acc, acc_phase, abort_flag, a.status)) break;
+            if (!mbar_wait(tfull + acc, acc_phase, abort_flag, a.status, a.wait_limit)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + lane_addr + (uint32_t)(acc * BN);
             const long long grow = (long long)t.m0 + r;
@@ -885,7 +864,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (PAIR) cluster_sync();   // no multicast or release from the peer is still in flight
+    if (PAIR) cluster_sync();   // no commit or release from the peer is still in flight
     if (warp == 1) {
         tc_fence_after();
         if constexpr (TWO) tmem_dealloc_pair(tmem_base, kTmemCols);
@@ -961,12 +940,6 @@ static bool tmap_2d_sw64(CUtensorMap* m, const void* ptr, int esize, uint64_t in
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The weight-gradient products run as clusters of two CTAs sharing B tiles (PAIR): their m-tiles
-// (feature rows) always come in pairs of one expert.  For the grouped-M products a pair needs two
-// m-tiles of one expert, and the duplicate tile of every odd expert (about 6% more MMA work at
-// 1024 rows per expert) outweighed the saved L2 traffic on GB300, so they run one CTA per tile.
-template <bool WGRAD>
-constexpr bool use_pairs() { return WGRAD; }
 // Two-SM MMAs (256 x 256 per CTA pair, each SM holding half of every B tile) for the BF16 weight
 // gradients and the backward gate/up product, where they measured 6-10% faster on GB300; the
 // forward products and the SwiGLU backward keep one CTA per 128 x 256 tile (a grouped-M pair
@@ -978,8 +951,8 @@ template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
                        const CUtensorMap* tc = nullptr, const CUtensorMap* td = nullptr) {
     constexpr bool TWO = use_two<BN, MX, WGRAD, EPI>();
-    constexpr bool PAIR = TWO || use_pairs<WGRAD>();
-    auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, PAIR, TWO>;
+    constexpr bool PAIR = TWO;
+    auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, TWO>;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
     const size_t out_bytes = tma_out<EPI, MX, BN>()
@@ -1164,8 +1137,8 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
         case GemmKind::WgradDown:
             // weight gradients keep 128 x 128 tiles with two accumulators: their contraction over an
             // expert's rows is short, so a drained single accumulator would stall the MMAs, and the
-            // fp32 output stores need the epilogue to overlap the next tile; a pair splits B's K rows
-            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 64) ||
+            // fp32 output stores need the epilogue to overlap the next tile
+            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 128) ||
                 !tmap_2d(&tc, out, oes, I, E * H, 32))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / 128);
@@ -1174,7 +1147,7 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
             return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
         case GemmKind::WgradGateUp:
-            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 64) ||
+            if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 128) ||
                 !tmap_2d(&tc, out, oes, H, E * 2 * I, 32))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 128);
@@ -1200,6 +1173,8 @@ cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, b
     a.I = (int)L.I;
     a.out_f32 = out_f32 ? 1 : 0;
     a.save_gu = save_gu ? 1 : 0;
+    a.wait_limit = c.wait_limit > 0 ? c.wait_limit : kWaitTimeoutCycles;
+    a.withhold_loads = (c.test_flags & MOE_TEST_WITHHOLD_LOADS) ? 1 : 0;
     const bool fwd = kind == GemmKind::FwdGateUp || kind == GemmKind::FwdGateUpSaveOnly || kind == GemmKind::FwdDown;
     const bool mx = fwd ? L.mx_fwd : L.mx_bwd;   // fp8_bwd: BF16 forward products, MXFP8 backward ones
     const int trace_id = (mx ? kTraceGemmMx : kTraceGemm) + (int)kind;

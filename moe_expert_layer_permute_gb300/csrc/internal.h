@@ -52,10 +52,20 @@ struct Ctx {
     int* status;       // device status word
     int num_sms;
     const float* topk_w;  // routing weights [T*k] (caller's tensor)
+    long long wait_limit = 0;   // pipeline wait limit in cycles (0: the default)
+    uint32_t test_flags = 0;    // MOE_TEST_* (moe_set_wait_limit)
 };
 
 // routing: counts, offsets, padded offsets, m-tile prefix, expert order, perm / inv / pos / row_slot
 cudaError_t launch_routing(const Ctx& c, const int32_t* topk_idx);
+// The routing kernels on explicit buffers: hist and base hold 2 * ceil(S / kRouteChunk) * E ints of
+// working memory; pad_off, mtile, order, pos, row_slot (the padded row layout) and status may all
+// be null together, in which case only counts, offsets, perm and inv are produced.
+struct RoutingBufs {
+    int *hist, *base, *cnt, *off, *pad_off, *mtile, *order, *perm, *inv, *pos, *row_slot;
+};
+cudaError_t launch_routing_kernels(cudaStream_t st, const int32_t* topk_idx, int S, int E, const RoutingBufs& r,
+                                   int* status);
 // dst[r] = src[row_slot[r] / k] for every padded row r (zeros on padding rows); up to two pairs
 cudaError_t launch_gather(const Ctx& c, const void* src0, void* dst0, const void* src1, void* dst1);
 // out[t] = sum_j part[pos[t*k+j]] (fixed j order); optionally dtopk_w[s] = sum_n dtw[pos[s], n]

@@ -195,26 +195,49 @@ static int check_desc_scratch(moe_scratch* s, Layout* L) {
     return MOE_OK;
 }
 
+// Combines v into the hash h; the splitmix64 finaliser spreads every input bit over the whole
+// word, so that a change in any input (an epoch advanced by one included) changes the high bits.
 static uint64_t mix(uint64_t h, uint64_t v) {
-    h ^= v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
-    return h;
+    uint64_t z = h ^ (v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2));
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
 }
-static uint64_t fwd_tag(const moe_desc* d, const void* x, const void* idx, const void* w, const void* w13,
+// Tags of what a scratch buffer holds: the inputs' addresses and the caller's epoch (advanced
+// whenever those buffers may have changed in place), never the device data itself.
+static uint64_t fwd_tag(const moe_scratch* s, const void* x, const void* idx, const void* w, const void* w13,
                         const void* w2) {
+    const moe_desc* d = &s->desc;
     uint64_t h = 0x6D6F655F66776400ull;
     for (uint64_t v : {(uint64_t)d->T, (uint64_t)d->H, (uint64_t)d->I, (uint64_t)d->E, (uint64_t)d->k,
                        (uint64_t)d->precision, (uint64_t)(uintptr_t)x, (uint64_t)(uintptr_t)idx,
-                       (uint64_t)(uintptr_t)w, (uint64_t)(uintptr_t)w13, (uint64_t)(uintptr_t)w2})
+                       (uint64_t)(uintptr_t)w, (uint64_t)(uintptr_t)w13, (uint64_t)(uintptr_t)w2, s->epoch})
         h = mix(h, v);
     return h | 1ull;  // never 0 (0 = no saved forward)
 }
 
-static uint64_t weights_tag(const moe_desc* d, const void* w13, const void* w2) {
+static uint64_t weights_tag(const moe_scratch* s, const void* w13, const void* w2) {
+    const moe_desc* d = &s->desc;
     uint64_t h = 0x6D6F655F77717500ull;
-    for (uint64_t v : {(uint64_t)d->H, (uint64_t)d->I, (uint64_t)d->E, (uint64_t)(uintptr_t)w13,
-                       (uint64_t)(uintptr_t)w2})
+    for (uint64_t v : {(uint64_t)d->H, (uint64_t)d->I, (uint64_t)d->E, (uint64_t)d->precision,
+                       (uint64_t)(uintptr_t)w13, (uint64_t)(uintptr_t)w2, s->epoch})
         h = mix(h, v);
     return h | 1ull;
+}
+
+// MOE_FLAG_REUSE_WEIGHTS is honoured only if this scratch holds copies of these weights made at
+// the current epoch; checked before anything is launched.
+static int check_weight_reuse(const moe_scratch* s, bool needs_copies, const void* w13, const void* w2) {
+    if (!needs_copies || !(s->desc.flags & MOE_FLAG_REUSE_WEIGHTS)) return MOE_OK;
+    return s->state[1] == weights_tag(s, w13, w2) ? MOE_OK : MOE_ERR_STATE;
+}
+
+static Ctx make_ctx(cudaStream_t st, moe_scratch* s, const Layout* L, int nsm, const void* topk_w) {
+    char* base = reinterpret_cast<char*>(s->data);
+    Ctx c{st, base, L, reinterpret_cast<int*>(base + L->ctrl), nsm, reinterpret_cast<const float*>(topk_w)};
+    c.wait_limit = (long long)s->state[2];
+    c.test_flags = (uint32_t)s->state[3];
+    return c;
 }
 
 // MX copies of the weights: for an MX forward W13 blocked along H (gate/up row blocks) and W2
@@ -226,7 +249,7 @@ static int mx_weights(const Ctx& c, moe_scratch* s, const void* W13, const void*
     const Layout& L = *c.L;
     const MxLayout& M = L.mx;
     const moe_desc* d = &s->desc;
-    const uint64_t tag = weights_tag(d, W13, W2);
+    const uint64_t tag = weights_tag(s, W13, W2);
     if (d->flags & MOE_FLAG_REUSE_WEIGHTS) return s->state[1] == tag ? MOE_OK : MOE_ERR_STATE;
     char* b = c.base;
     auto fw = [&](size_t off) { return L.mx_fwd ? b + off : nullptr; };
@@ -282,7 +305,8 @@ int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* t
     if ((rc = check_tensor(W13, MOE_DT_BF16, 3, E, 2 * I, H))) return rc;
     if ((rc = check_tensor(W2, MOE_DT_BF16, 3, E, H, I))) return rc;
     if ((rc = check_tensor(y, MOE_DT_BF16, 2, T, H, 0))) return rc;
-    const uint64_t tag = fwd_tag(d, x->data, topk_idx->data, topk_w->data, W13->data, W2->data);
+    if (T > 0 && (rc = check_weight_reuse(scratch, L.mx_fwd, W13->data, W2->data))) return rc;
+    const uint64_t tag = fwd_tag(scratch, x->data, topk_idx->data, topk_w->data, W13->data, W2->data);
     const bool save = (d->flags & MOE_FLAG_SAVE_GU) != 0;
     if (T == 0) {
         scratch->state[0] = save ? tag : 0;
@@ -292,7 +316,7 @@ int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* t
     if (nsm <= 0) return MOE_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     char* base = reinterpret_cast<char*>(scratch->data);
-    Ctx c{st, base, &L, reinterpret_cast<int*>(base + L.ctrl), nsm, reinterpret_cast<const float*>(topk_w->data)};
+    const Ctx c = make_ctx(st, scratch, &L, nsm, topk_w->data);
     MOE_TRY_CUDA(launch_routing(c, reinterpret_cast<const int32_t*>(topk_idx->data)));
     if (L.mx_fwd) {
         // dispatch and quantise in one pass; a forward that saves for the backward also makes the
@@ -336,9 +360,10 @@ int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_id
     if ((rc = check_weight_grad(dW13, 3, E, 2 * I, H, &f32_13))) return rc;
     if ((rc = check_weight_grad(dW2, 3, E, H, I, &f32_2))) return rc;
     if ((rc = check_tensor(dtopk_w, MOE_DT_F32, 2, T, k, 0))) return rc;
-    const uint64_t tag = fwd_tag(d, x->data, topk_idx->data, topk_w->data, W13->data, W2->data);
+    const uint64_t tag = fwd_tag(scratch, x->data, topk_idx->data, topk_w->data, W13->data, W2->data);
     const bool reuse = (d->flags & MOE_FLAG_REUSE_FWD) != 0;
     if (reuse && scratch->state[0] != tag) return MOE_ERR_STATE;
+    if (T > 0 && (rc = check_weight_reuse(scratch, L.mx_on, W13->data, W2->data))) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (T == 0) {
         MOE_TRY_CUDA(cudaMemsetAsync(dW13->data, 0, (size_t)E * 2 * I * H * (f32_13 ? 4 : 2), st));
@@ -348,7 +373,7 @@ int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_id
     const int nsm = num_sms_current();
     if (nsm <= 0) return MOE_ERR_CUDA;
     char* base = reinterpret_cast<char*>(scratch->data);
-    Ctx c{st, base, &L, reinterpret_cast<int*>(base + L.ctrl), nsm, reinterpret_cast<const float*>(topk_w->data)};
+    const Ctx c = make_ctx(st, scratch, &L, nsm, topk_w->data);
     const MxLayout& M = L.mx;
     if (L.mx_on && (rc = mx_weights(c, scratch, W13->data, W2->data))) return rc;
     if (!reuse) {
@@ -386,6 +411,14 @@ int moe_read_device_status(moe_scratch* scratch, void* stream, int* status) {
     MOE_TRY_CUDA(cudaMemsetAsync(scratch->data, 0, sizeof(int), st));
     MOE_TRY_CUDA(cudaStreamSynchronize(st));
     *status = v;
+    return MOE_OK;
+}
+
+int moe_set_wait_limit(moe_scratch* scratch, int64_t wait_cycles, uint32_t test_flags) {
+    if (!scratch) return MOE_ERR_NULL;
+    if (wait_cycles < 0) return MOE_ERR_SHAPE;
+    scratch->state[2] = (uint64_t)wait_cycles;
+    scratch->state[3] = test_flags & MOE_TEST_WITHHOLD_LOADS;
     return MOE_OK;
 }
 

@@ -15,7 +15,10 @@
 //                 base[b][e] + (slots of e earlier in the chunk), ranking ties inside a warp with
 //                 __match_any_sync and across the block's warps with per-warp counts.
 // Expert ids outside [0, E) are never used as an index: they are counted nowhere, recorded as
-// MOE_DEV_BAD_EXPERT in the status word, and their slots get inv = pos = -1.
+// MOE_DEV_BAD_EXPERT in the status word (when there is one), their slots get inv = pos = -1, and
+// the sorted positions they leave free, [offsets[E], T*k), hold perm = -1.
+// The padded-layout outputs (pad_off, mtile, order, pos, row_slot) and the status word are
+// optional: the allocation-free entry point (route_static.cu) runs the same kernels without them.
 #include "common.cuh"
 #include "internal.h"
 
@@ -82,25 +85,29 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict_
     if (e < E) {
         cnt[e] = c;
         off[e] = c_incl - c;
-        mtile[e] = t_incl - tiles;
-        pad_off[e] = (t_incl - tiles) * kBM;
-        if (e == E - 1) {
-            off[E] = c_incl;
-            mtile[E] = t_incl;
-            pad_off[E] = t_incl * kBM;
+        if (e == E - 1) off[E] = c_incl;
+        if (pad_off) {
+            mtile[e] = t_incl - tiles;
+            pad_off[e] = (t_incl - tiles) * kBM;
+            if (e == E - 1) {
+                mtile[E] = t_incl;
+                pad_off[E] = t_incl * kBM;
+            }
         }
         int run = c_incl - c;
         for (int b = 0; b < nb; ++b) {
             base[(size_t)b * E + e] = run;
             run += hist[(size_t)b * E + e];
         }
-        // rank by count, largest first, ties by expert id (used to order weight-gradient tiles)
-        int rank = 0;
-        for (int f = 0; f < E; ++f) {
-            const int cf = sh_cnt[f];
-            rank += (cf > c) || (cf == c && f < e);
+        if (order) {
+            // rank by count, largest first, ties by expert id (used to order weight-gradient tiles)
+            int rank = 0;
+            for (int f = 0; f < E; ++f) {
+                const int cf = sh_cnt[f];
+                rank += (cf > c) || (cf == c && f < e);
+            }
+            order[rank] = e;
         }
-        order[rank] = e;
     }
 }
 
@@ -131,14 +138,16 @@ __global__ void __launch_bounds__(kRouteThreads) route_place_kernel(
             int before = 0;
             for (int w = 0; w < warp; ++w) before += wc[w * E + e];
             const int p = ctr[e] + before + rank;
-            const int pp = p - off[e] + pad_off[e];
             perm[p] = s;
             inv[s] = p;
-            pos[s] = pp;
-            row_slot[pp] = s;
+            if (pos) {
+                const int pp = p - off[e] + pad_off[e];
+                pos[s] = pp;
+                row_slot[pp] = s;
+            }
         } else if (valid) {
             inv[s] = -1;
-            pos[s] = -1;
+            if (pos) pos[s] = -1;
         }
         __syncthreads();
         for (int f = tid; f < E; f += kRouteThreads) {
@@ -152,41 +161,44 @@ __global__ void __launch_bounds__(kRouteThreads) route_place_kernel(
         }
         __syncthreads();
     }
+    // sorted positions left free by dropped slots (none for valid ids)
+    for (int p = off[E] + blockIdx.x * kRouteThreads + tid; p < S; p += gridDim.x * kRouteThreads) perm[p] = -1;
     // padding rows of the groups this block owns
-    for (int f = blockIdx.x; f < E; f += gridDim.x) {
-        const int lo = pad_off[f] + cnt[f], hi = pad_off[f + 1];
-        for (int r = lo + tid; r < hi; r += kRouteThreads) row_slot[r] = -1;
+    if (row_slot) {
+        for (int f = blockIdx.x; f < E; f += gridDim.x) {
+            const int lo = pad_off[f] + cnt[f], hi = pad_off[f + 1];
+            for (int r = lo + tid; r < hi; r += kRouteThreads) row_slot[r] = -1;
+        }
     }
+}
+
+cudaError_t launch_routing_kernels(cudaStream_t st, const int32_t* topk_idx, int S, int E, const RoutingBufs& r,
+                                   int* status) {
+    const int nb = (S + kRouteChunk - 1) / kRouteChunk;
+    if (nb > 0) {
+        trace_begin(st, kTraceRouteHist);
+        route_hist_kernel<<<nb, kRouteThreads, E * sizeof(int), st>>>(topk_idx, S, E, r.hist, status);
+        trace_end(st, kTraceRouteHist);
+    }
+    trace_begin(st, kTraceRouteScan);
+    route_scan_kernel<<<1, 1024, 0, st>>>(r.hist, nb, E, r.cnt, r.off, r.pad_off, r.mtile, r.order, r.base);
+    trace_end(st, kTraceRouteScan);
+    if (nb > 0) {
+        trace_begin(st, kTraceRoutePlace);
+        const size_t sm = (size_t)(E + 8 * E) * sizeof(int);
+        route_place_kernel<<<nb, kRouteThreads, sm, st>>>(topk_idx, S, E, r.base, r.off, r.pad_off, r.cnt, r.perm,
+                                                          r.inv, r.pos, r.row_slot);
+        trace_end(st, kTraceRoutePlace);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_routing(const Ctx& c, const int32_t* topk_idx) {
     const Layout& L = *c.L;
-    int* hist = reinterpret_cast<int*>(c.base + L.hist);
-    int* cnt = reinterpret_cast<int*>(c.base + L.cnt);
-    int* off = reinterpret_cast<int*>(c.base + L.off);
-    int* pad_off = reinterpret_cast<int*>(c.base + L.pad_off);
-    int* mtile = reinterpret_cast<int*>(c.base + L.mtile);
-    int* order = reinterpret_cast<int*>(c.base + L.order);
-    int* base = reinterpret_cast<int*>(c.base + L.base);
-    const int S = (int)L.S, E = (int)L.E, nb = (int)L.nb_route;
-    if (nb > 0) {
-        trace_begin(c.st, kTraceRouteHist);
-        route_hist_kernel<<<nb, kRouteThreads, E * sizeof(int), c.st>>>(topk_idx, S, E, hist, c.status);
-        trace_end(c.st, kTraceRouteHist);
-    }
-    trace_begin(c.st, kTraceRouteScan);
-    route_scan_kernel<<<1, 1024, 0, c.st>>>(hist, nb, E, cnt, off, pad_off, mtile, order, base);
-    trace_end(c.st, kTraceRouteScan);
-    if (nb > 0) {
-        trace_begin(c.st, kTraceRoutePlace);
-        const size_t sm = (size_t)(E + 8 * E) * sizeof(int);
-        route_place_kernel<<<nb, kRouteThreads, sm, c.st>>>(
-            topk_idx, S, E, base, off, pad_off, cnt, reinterpret_cast<int*>(c.base + L.perm),
-            reinterpret_cast<int*>(c.base + L.inv), reinterpret_cast<int*>(c.base + L.pos),
-            reinterpret_cast<int*>(c.base + L.row_slot));
-        trace_end(c.st, kTraceRoutePlace);
-    }
-    return cudaGetLastError();
+    auto at = [&](size_t off) { return reinterpret_cast<int*>(c.base + off); };
+    const RoutingBufs r{at(L.hist), at(L.base), at(L.cnt), at(L.off), at(L.pad_off), at(L.mtile),
+                        at(L.order),  at(L.perm), at(L.inv), at(L.pos), at(L.row_slot)};
+    return launch_routing_kernels(c.st, topk_idx, (int)L.S, (int)L.E, r, c.status);
 }
 
 }  // namespace moe

@@ -6,8 +6,9 @@ no activation). The top-k expert ids and their weights stand in for a router, wh
 leave out of their single-layer benchmark ("random routing, router cost excluded": ic.work
 analysis, section "跑分背后的理想假设与闭源软肋"; MarkTechPost, "How fast is Prime Mega MoE?").
 
-Recipe (every array from numpy PCG64, one independent stream per tensor, keyed by
-`(seed, stream id)`):
+Recipe (every array from numpy PCG64; a tensor is drawn in chunks of 2^24 elements, chunk c of
+tensor stream id i from its own generator keyed by `(seed, i, c)`, so that chunks can be drawn
+in parallel and the result does not depend on the number of threads):
 
 * x, dy ~ N(0, 1); W13 [E, 2I, H] ~ N(0, std = 1/sqrt(H)); W2 [E, H, I] ~ N(0, std = 1/sqrt(I)).
   All are drawn in float32 and rounded to bf16 (round to nearest, ties to even).
@@ -22,7 +23,9 @@ Recipe (every array from numpy PCG64, one independent stream per tensor, keyed b
 """
 from __future__ import annotations
 
+import concurrent.futures as _cf
 import dataclasses
+import os
 
 import numpy as np
 
@@ -92,24 +95,43 @@ def _rng(seed: int, stream: int) -> np.random.Generator:
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round float32 to bf16 (nearest, ties to even); returns the uint16 bit patterns."""
     u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
-    r = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
-    return ((u + r) >> np.uint32(16)).astype(np.uint16)
+    r = u >> np.uint32(16)
+    r &= np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _normal_bf16(rng: np.random.Generator, shape, std: float) -> np.ndarray:
+_CHUNK = 1 << 24
+
+
+def _normal_bf16(seed: int, stream: int, shape, std: float) -> np.ndarray:
+    """N(0, std^2) rounded to bf16, chunk c from the generator keyed (seed, stream, c)."""
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
-    chunk = 1 << 24
-    for s in range(0, n, chunk):
-        c = min(chunk, n - s)
-        v = rng.standard_normal(c, dtype=np.float32)
+
+    def fill(c: int) -> None:
+        s0 = c * _CHUNK
+        m = min(_CHUNK, n - s0)
+        v = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, stream, c]))).standard_normal(
+            m, dtype=np.float32)
         if std != 1.0:
             v *= np.float32(std)
-        out[s:s + c] = f32_to_bf16_bits(v)
+        out[s0:s0 + m] = f32_to_bf16_bits(v)
+
+    chunks = (n + _CHUNK - 1) // _CHUNK
+    workers = min(chunks, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 1)
+    if workers <= 1:
+        for c in range(chunks):
+            fill(c)
+    else:
+        with _cf.ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(fill, range(chunks)))
     return out.reshape(shape)
 
 
@@ -170,10 +192,10 @@ def make_inputs(cfg: LayerConfig | str, *, with_weights: bool = True, with_dy: b
         cfg = CONFIGS[cfg]
     T, H, I, E = cfg.T, cfg.H, cfg.I, cfg.E
     idx, w = routing(cfg)
-    x = _normal_bf16(_rng(cfg.seed, _S_X), (T, H), 1.0)
-    W13 = _normal_bf16(_rng(cfg.seed, _S_W13), (E, 2 * I, H), 1.0 / np.sqrt(H)) if with_weights else None
-    W2 = _normal_bf16(_rng(cfg.seed, _S_W2), (E, H, I), 1.0 / np.sqrt(I)) if with_weights else None
-    dy = _normal_bf16(_rng(cfg.seed, _S_DY), (T, H), 1.0) if with_dy else None
+    x = _normal_bf16(cfg.seed, _S_X, (T, H), 1.0)
+    W13 = _normal_bf16(cfg.seed, _S_W13, (E, 2 * I, H), 1.0 / np.sqrt(H)) if with_weights else None
+    W2 = _normal_bf16(cfg.seed, _S_W2, (E, H, I), 1.0 / np.sqrt(I)) if with_weights else None
+    dy = _normal_bf16(cfg.seed, _S_DY, (T, H), 1.0) if with_dy else None
     return LayerInputs(cfg, x, idx, w, W13, W2, dy)
 
 

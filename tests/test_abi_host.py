@@ -240,3 +240,52 @@ def test_router_argument_checks(bd):
     assert bwd(f.t((64, 8), I32), f.t((64, 8), F32), f.t((64, 7), F32), f.t((64, 100), F32)) == E["MOE_ERR_SHAPE"]
     assert bwd(f.t((64, 8), I32), f.t((64, 8), F32), f.t((64, 8), F32), f.t((63, 100), F32)) == E["MOE_ERR_SHAPE"]
     assert bd.LIB.moe_router_bwd(None, None, None, None, None) == E["MOE_ERR_NULL"]
+
+
+def _bwd_call(bd, a, s, T=256, H=256, I=128, E=8, k=2):
+    f = _Fake(bd)
+    f.addr = 1 << 36
+    dy = f.t((T, H), 0); dx = f.t((T, H), 0)
+    dW13 = f.t((E, 2 * I, H), 1); dW2 = f.t((E, H, I), 1); dtw = f.t((T, k), 1)
+    return bd.LIB.moe_bwd(ctypes.byref(dy), *[ctypes.byref(a[n]) for n in ("x", "idx", "w", "W13", "W2")],
+                          ctypes.byref(dx), ctypes.byref(dW13), ctypes.byref(dW2), ctypes.byref(dtw),
+                          ctypes.byref(s), None)
+
+
+def test_epoch_invalidates_a_saved_forward(bd):
+    """A forward saved at one epoch is not reused at another: the caller advances the epoch when
+    its buffers change in place (an optimizer step), and MOE_FLAG_REUSE_FWD then refuses."""
+    a, s = _fwd_args(bd, T=0)
+    s.desc.flags = bd.MOE_FLAG_SAVE_GU
+    assert _call_fwd(bd, a, s) == bd.ERR["MOE_OK"]                 # T = 0: records the forward, launches nothing
+    s.desc.flags = bd.MOE_FLAG_REUSE_FWD
+    ok = _bwd_call(bd, a, s, T=0)
+    assert ok in (bd.ERR["MOE_OK"], bd.ERR["MOE_ERR_CUDA"])       # past the state check (zeroing dW needs a GPU)
+    s.epoch += 1
+    assert _bwd_call(bd, a, s, T=0) == bd.ERR["MOE_ERR_STATE"]
+    s.epoch -= 1
+    assert _bwd_call(bd, a, s, T=0) == ok
+
+
+def test_weight_reuse_without_copies_is_refused_before_any_launch(bd):
+    for prec in (bd.MOE_MXFP8, bd.MOE_FP8_FP4):
+        a, s = _fwd_args(bd)
+        s.desc.precision = prec
+        s.bytes = bd.moe_scratch_bytes(s.desc)
+        s.desc.flags = bd.MOE_FLAG_REUSE_WEIGHTS
+        assert _call_fwd(bd, a, s) == bd.ERR["MOE_ERR_STATE"]
+    a, s = _fwd_args(bd)
+    s.desc.precision = bd.MOE_FP8_BWD
+    s.bytes = bd.moe_scratch_bytes(s.desc)
+    s.desc.flags = bd.MOE_FLAG_REUSE_WEIGHTS
+    assert _bwd_call(bd, a, s) == bd.ERR["MOE_ERR_STATE"]
+
+
+def test_set_wait_limit_arguments(bd):
+    s = bd.MoeScratch()
+    assert bd.LIB.moe_set_wait_limit(None, 0, 0) == bd.ERR["MOE_ERR_NULL"]
+    assert bd.LIB.moe_set_wait_limit(ctypes.byref(s), -1, 0) == bd.ERR["MOE_ERR_SHAPE"]
+    assert bd.LIB.moe_set_wait_limit(ctypes.byref(s), 12345, 0xFF) == bd.ERR["MOE_OK"]
+    assert (s.state[2], s.state[3]) == (12345, bd.MOE_TEST_WITHHOLD_LOADS)   # unknown flags dropped
+    assert bd.LIB.moe_set_wait_limit(ctypes.byref(s), 0, 0) == bd.ERR["MOE_OK"]
+    assert (s.state[2], s.state[3]) == (0, 0)

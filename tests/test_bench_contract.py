@@ -35,7 +35,7 @@ def test_summary_roofline_and_launches():
     flops = 4.0 * cfg.S * cfg.H * cfg.I                      # 2 S H 2I per launch
     assert roof["achieved"] == pytest.approx(flops / (12.0 / 20 * 1e-3) / 1e12)
     assert roof["frac"] == pytest.approx(roof["achieved"] / peak)
-    assert roof["traffic"] == bench.PROFILED_TRAFFIC[(cfg.name, "gemm_fwd_gate_up_swiglu")]
+    assert roof["traffic"] == bench.PROFILED_TRAFFIC.get((cfg.name, "gemm_fwd_gate_up_swiglu"))
     # throughput of the checkpointed layer: 4 x forward FLOPs over the step
     assert sm["full_tflops"] == pytest.approx(4 * cfg.fwd_flops() / (4.4e-3) / 1e12)
     assert sm["frac_of_peak"] == pytest.approx(sm["full_tflops"] / peak)
@@ -59,3 +59,23 @@ def test_oracle_step_units(precision, units):
     a = (inp.f64("x"), inp.topk_idx, inp.f64("topk_w"), inp.f64("W13"), inp.f64("W2"))
     assert bench.oracle_step(cfg, a, inp.f64("dy")) == units
     assert np.isfinite(a[0]).all()
+
+
+def test_peak_table_uses_the_burst_rate():
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "clocks_under_load": {"sm_mhz_median": 1450.0}}
+    pk = bench.peak_table(peaks, "measured")
+    assert pk["burst"]["bf16"] == 1900.0 and pk["burst"]["mxfp8"] == 3800.0
+    # fp8_bwd: two BF16 forwards and one MXFP8 backward of equal FLOPs, 4F / (2F / P + 2F / 2P)
+    assert pk["burst"]["fp8_bwd"] == pytest.approx(4.0 / (2.0 / 1900.0 + 2.0 / 3800.0))
+    assert pk["sustained"]["bf16"] == 1700.0 and pk["sustained_mhz"] == 1450.0
+    fb = bench.peak_table({}, "fallback")
+    assert fb["burst"]["bf16"] == bench.FALLBACK_PEAKS["bf16_tflops"]
+
+
+def test_compact_summary_of_a_measurement():
+    cfg = gen.CONFIGS["qwen3_30b_a3b"]
+    sm = bench.summarize(_measurement(cfg), 1900.0, "test peak")
+    c = bench.compact(cfg.name, sm)
+    assert c["full_ms"] == 4.4 and c["top_kernel"] == "gemm_fwd_gate_up_swiglu"
+    assert c["frac_of_peak"] == pytest.approx(sm["full_tflops"] / 1900.0, rel=1e-3)
+    assert c["sm_mhz"] == 1900.0

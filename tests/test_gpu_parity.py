@@ -223,6 +223,13 @@ def test_bad_expert_ids_are_flagged_not_used(cuda_lib):
     torch.cuda.synchronize()
     assert L.status() == cuda_lib.MOE_DEV_BAD_EXPERT
     assert L.status() == 0                     # reading clears the word
+    # dropped slots: inv = -1, and the two positions they free at the end of perm hold -1
+    S = cfg.S
+    inv = L.view(cuda_lib.MOE_VIEW_INV, torch.int32, (S,)).cpu().numpy()
+    perm = L.view(cuda_lib.MOE_VIEW_PERM, torch.int32, (S,)).cpu().numpy()
+    assert inv[3 * 2 + 0] == -1 and inv[10 * 2 + 1] == -1
+    assert np.array_equal(perm[S - 2:], [-1, -1]) and (perm[:S - 2] >= 0).all()
+    assert np.array_equal(inv[perm[:S - 2]], np.arange(S - 2))
     # the valid slots still produce the layer over the valid slots only
     keep = (idx >= 0) & (idx < 8)
     w = np.where(keep, inp.topk_w, 0.0)
