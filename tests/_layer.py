@@ -18,6 +18,21 @@ def rel_fro(got, ref) -> float:
     return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
 
 
+def max_row_rel(got, ref, floor: float = 0.1) -> float:
+    """Largest relative error of any row (last axis): ||got_r - ref_r|| / max(||ref_r||, floor * rms
+    row norm).  The floor keeps rows whose reference is zero (or nearly) from dividing by zero while
+    still requiring their output to be near zero.  Beside the whole-tensor Frobenius error this
+    catches a handful of wrong rows, which a large tensor's Frobenius norm could absorb."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    g = got.reshape(-1, got.shape[-1])
+    r = ref.reshape(-1, ref.shape[-1])
+    rn = np.linalg.norm(r, axis=1)
+    rms = float(np.sqrt(np.mean(rn ** 2))) if rn.size else 0.0
+    den = np.maximum(rn, max(floor * rms, 1e-300))
+    return float(np.max(np.linalg.norm(g - r, axis=1) / den)) if rn.size else 0.0
+
+
 def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 

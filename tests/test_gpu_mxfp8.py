@@ -10,10 +10,14 @@ import torch
 import oracle
 from moe_expert_layer_permute_gb300 import inputs as gen
 
-from _layer import DeviceLayer, decode_mx, f64, rel_fro
+from _layer import DeviceLayer, decode_mx, f64, max_row_rel, rel_fro
 
 pytestmark = pytest.mark.gpu
 TOL = 3e-2
+# per row of y, dx, dW13, dW2: twice the whole-tensor bound.  Against the quantise-aware oracle the
+# differences (fp32 against fp64 arithmetic, a rare code flipped at a near-tie) spread over rows of
+# at least 128 elements, while a wrong row is off by order one.
+ROW_TOL = 6e-2
 
 
 def mx(cfg):
@@ -100,6 +104,7 @@ def test_forward(cuda_lib, name):
     y_ref = oracle.forward(*_args(inp), mxfp8=True)
     err = rel_fro(f64(L.y), y_ref)
     assert err < TOL, err
+    assert max_row_rel(f64(L.y), y_ref) < ROW_TOL
     # and it is an MXFP8 result: closer to the quantised oracle than to the BF16 one
     assert err < rel_fro(f64(L.y), oracle.forward(*_args(inp)))
 
@@ -120,6 +125,8 @@ def test_backward(cuda_lib, name, reuse):
     for got, n in ((L.dx, "dx"), (L.dW13, "dW13"), (L.dW2, "dW2"), (L.dtw, "dtopk_w")):
         err = rel_fro(f64(got), ref[n])
         assert err < TOL, (n, err)
+        if n != "dtopk_w":
+            assert max_row_rel(f64(got), ref[n]) < ROW_TOL, (n, max_row_rel(f64(got), ref[n]))
 
 
 def test_weight_reuse_is_exact_and_checked(cuda_lib):
