@@ -296,7 +296,6 @@ __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& 
 // 578 µs with four against 592-596 µs with six)
 template <bool TWO, bool MX, int BN, bool WGRAD>
 constexpr int ring_stages() { return (TWO || (MX && BN == 128 && WGRAD)) ? 6 : kStages; }
-// (two-SM block-scaled tiles: 33.5 KB a stage, six beside the eight 2 KB output boxes)
 
 // TWO: clusters of two CTAs on two m-tiles of one expert and the same n-tile; the leader CTA
 // issues cta_group::2 MMAs (M = 256) over both CTAs' shared memory and tensor memory, each CTA
@@ -305,11 +304,8 @@ template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX
 __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
-                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const GemmArgs a) {
-    // tmSA / tmSB (two-SM block-scaled products only): the scale arrays viewed as [bytes / 128, 128]
-    // bytes, one 512-byte atom a box
-    static_assert(!TWO || !MX || (BN == 256 && !WGRAD), "two-SM block-scaled tiles are 256 x 256 grouped-M");
+    static_assert(!TWO || !MX, "two-SM MMAs run in CTA pairs, BF16 only");
     constexpr bool PAIR = TWO;                           // clusters of two CTAs exist only for them
     constexpr int kStages = ring_stages<TWO, MX, BN, WGRAD>();
     constexpr int kElems = MX ? 128 : 64;                // K elements per stage
@@ -420,7 +416,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                     if (TWO) {
                         // both CTAs' copies land on the leader's barrier, which expects both
                         const uint32_t lbar = cluster_addr(full + stage, 0);
-                        if (rank == 0) mbar_arrive_expect_tx(full + stage, 2 * stage_tx);
+                        if (rank == 0) mbar_arrive_expect_tx(full + stage, 2 * kStageBytes);
                         if (!A_MN) {
                             tma_load_2d_pair(dA, &tmA, lbar, k0, t.m0);
                         } else {
@@ -429,10 +425,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                                 tma_load_2d_pair(dA + c * kMnLbo, &tmA, lbar, t.m0 + kMnChunk * c, t.row0 + k0);
                         }
                         if (!B_MN) {
-                            // BF16 gate/up: the leader's half is gate rows, the peer's the up rows; else
-                            // (MXFP8 [64 gate | 64 up] blocks included) each CTA takes 128 consecutive rows
-                            const int brow = (SPLIT && !MX) ? t.e * a.b_rows_e + rank * a.b_up + t.n0
-                                                            : b_row0 + rank * (BN / 2);
+                            const int brow = SPLIT ? t.e * a.b_rows_e + rank * a.b_up + t.n0 : b_row0 + rank * (BN / 2);
                             tma_load_2d_pair(dB, &tmB, lbar, k0, brow);
                         } else {
                             const int krow = WGRAD ? t.row0 + k0 : t.e * a.b_rows_e + k0;
@@ -440,19 +433,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
 #pragma unroll
                             for (int c = 0; c < nch / 2; ++c)
                                 tma_load_2d_pair(dB + c * kMnLbo, &tmB, lbar, t.n0 + kMnChunk * (rank * nch / 2 + c), krow);
-                        }
-                        if constexpr (MX) {
-                            // this CTA's A atom and all of B's atoms: each SM's tensor cores read the scales
-                            // from its own tensor memory
-                            uint8_t* dS = sSF + stage * kSfBytes;
-                            tma_load_2d_pair(dS, &tmSA, lbar, 0, 4 * ((t.m0 / 128) * a.sfA_kt + kb));
-#pragma unroll
-                            for (int c = 0; c < kSfBAtoms; ++c) {
-                                const long long atom = !B_MN ? (long long)(b_row0 / 128 + c) * a.sfB_kt + kb
-                                                             : (long long)(t.n0 / 128 + c) * a.sfB_kt +
-                                                                   (long long)t.e * a.b_rows_e / 128 + kb;
-                                tma_load_2d_pair(dS + kSfAtom * (1 + c), &tmSB, lbar, 0, (int)(4 * atom));
-                            }
                         }
                         ++issued;
                         if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -553,19 +533,16 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         const uint32_t sf_cols = tmem_base + kAccStages * BN + stage * kSfCols;
                         const uint32_t ss = sf_base + stage * kSfBytes;
 #pragma unroll
-                        for (int c = 0; c <= kSfBAtoms; ++c) {
-                            if constexpr (TWO) tmem_cp_sf_atom_pair(sf_cols + 4 * c, sdesc_plain(ss + kSfAtom * c, 128));
-                            else tmem_cp_sf_atom(sf_cols + 4 * c, sdesc_plain(ss + kSfAtom * c, 128));
-                        }
+                        for (int c = 0; c <= kSfBAtoms; ++c)
+                            tmem_cp_sf_atom(sf_cols + 4 * c, sdesc_plain(ss + kSfAtom * c, 128));
 #pragma unroll
                         for (int ks = 0; ks < kElems / kMmaK; ++ks) {
                             const uint64_t ad = A_MN ? sdesc_sw128(sa + ks * kMnStep, kMnLbo, 1024)
                                                      : sdesc_sw128(sa + ks * kKStep, 16, 1024);
                             const uint64_t bd = B_MN ? sdesc_sw128(sb + ks * kMnStep, kMnLbo, 1024)
                                                      : sdesc_sw128(sb + ks * kKStep, 16, 1024);
-                            const uint32_t id = idesc_mxf8(TWO ? 2 * kBM : kBM, BN, A_MN, B_MN, ks, ks) | a.b_fmt;
-                            if constexpr (TWO) mma_mxf8_pair(d_tmem, ad, bd, id, sf_cols, sf_cols + 4, (kb | ks) != 0);
-                            else mma_mxf8(d_tmem, ad, bd, id, sf_cols, sf_cols + 4, (kb | ks) != 0);
+                            mma_mxf8(d_tmem, ad, bd, idesc_mxf8(kBM, BN, A_MN, B_MN, ks, ks) | a.b_fmt, sf_cols,
+                                     sf_cols + 4, (kb | ks) != 0);
                         }
                     } else {
 #pragma unroll
@@ -645,10 +622,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 tmem_ld32(tcol + 96, d + 96);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    if (TWO && rank == 1) mbar_arrive_cluster(tempty + acc, 0);   // the leader's MMAs reuse it
-                    else mbar_arrive(tempty + acc);
-                }
+                if (lane == 0) mbar_arrive(tempty + acc);
                 if (t.valid)
                     epilogue_drained<BN, EPI, kTmaOut>(a, t, grow, half, d, &tmC, &tmD,
                                                        sOut + (warp - 2) * out_box_bytes<EPI, kSingle>(), lane,
@@ -952,20 +926,6 @@ static bool tmap_2d_fp4(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D tensor map over an array of 512-byte scale atoms viewed as [bytes / 128, 128] bytes, box
-// {128, 4}: one atom a copy, unswizzled (the two-SM block-scaled products load their atoms by TMA)
-static bool tmap_sf(CUtensorMap* m, const void* ptr, uint64_t bytes) {
-    EncodeTiledFn enc = get_encode();
-    if (!enc || bytes < 512 || bytes % 512 != 0) return false;
-    const cuuint64_t dims[2] = {128, bytes / 128};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {128, 4};
-    const cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // 2-D tensor map with box {64 bytes, box_rows} and 64-byte swizzle (staged SwiGLU-backward outputs)
 static bool tmap_2d_sw64(CUtensorMap* m, const void* ptr, int esize, uint64_t inner, uint64_t outer,
                          uint32_t box_rows) {
@@ -984,20 +944,15 @@ static bool tmap_2d_sw64(CUtensorMap* m, const void* ptr, int esize, uint64_t in
 // gradients and the backward gate/up product, where they measured 6-10% faster on GB300; the
 // forward products and the SwiGLU backward keep one CTA per 128 x 256 tile (a grouped-M pair
 // needs two m-tiles of one expert, and the duplicated odd tiles cancel the gain there).
-// The MXFP8 128 x 256 products (forward gate/up and down, backward gate/up) run two-SM too: a
-// one-SM 128 x 256 block-scaled tile asks about 168 bytes a clock of shared-memory traffic (operand
-// reads plus the TMA fills) against the SM's 128, a pair holding half of B each about 112.
 template <int BN, bool MX, bool WGRAD, int EPI>
-constexpr bool use_two() { return BN == 256 && (MX ? !WGRAD : (WGRAD || EPI == EPI_PLAIN)); }
+constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN); }
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
-                       const CUtensorMap* tc = nullptr, const CUtensorMap* td = nullptr,
-                       const CUtensorMap* tsa = nullptr, const CUtensorMap* tsb = nullptr) {
+                       const CUtensorMap* tc = nullptr, const CUtensorMap* td = nullptr) {
     constexpr bool TWO = use_two<BN, MX, WGRAD, EPI>();
     constexpr bool PAIR = TWO;
     auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, TWO>;
-    if (TWO && MX && (!tsa || !tsb)) return cudaErrorInvalidValue;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
     const size_t out_bytes = tma_out<EPI, MX, BN>()
@@ -1007,8 +962,6 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     if (tma_out<EPI, MX, BN>() && !tc) return cudaErrorInvalidValue;
     const CUtensorMap& tcm = tc ? *tc : ta;   // kernels without a TMA-stored output never read it
     const CUtensorMap& tdm = td ? *td : tcm;
-    const CUtensorMap& tsam = tsa ? *tsa : ta;   // scale maps: read by the two-SM block-scaled products only
-    const CUtensorMap& tsbm = tsb ? *tsb : ta;
     const size_t smem = fixed + (size_t)2 * (a.E + 1) * 4;
     const size_t smem_max = fixed + (size_t)2 * (kMaxExperts + 1) * 4;
     static std::once_flag once;
@@ -1037,7 +990,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (!PAIR) {
-        kern<<<c.num_sms, kThreads, smem, c.st>>>(ta, tb, tcm, tdm, tsam, tsbm, a);
+        kern<<<c.num_sms, kThreads, smem, c.st>>>(ta, tb, tcm, tdm, a);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -1052,7 +1005,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     cfg.stream = c.st;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tcm, tdm, tsam, tsbm, a);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tcm, tdm, a);
 }
 
 int bwd_down_bn(int64_t I) { return (I % 256 == 0) ? 256 : 128; }
@@ -1130,17 +1083,15 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
     const int64_t H = L.H, I = L.I, E = L.E, R = L.rows;
     auto u8 = [&](size_t off) { return reinterpret_cast<const uint8_t*>(b + off); };
     const int oes = a.out_f32 ? 4 : 2;   // weight-gradient output element size
-    CUtensorMap ta, tb, tc, td, tsa, tsb;
+    CUtensorMap ta, tb, tc, td;
     switch (kind) {
         case GemmKind::FwdGateUp:
         case GemmKind::FwdGateUpSaveOnly:
-            // 256 weight rows = two [64 gate | 64 up] blocks = 128 I-columns per tile (a CTA pair: one
-            // block each)
+            // 256 weight rows = two [64 gate | 64 up] blocks = 128 I-columns per tile
             if (!tmap_2d(&ta, b + M.x_r, 1, H, R, 128) ||
-                !(L.fp4w ? tmap_2d_fp4(&tb, b + M.w13_r, H, E * 2 * I, 128)
-                         : tmap_2d(&tb, b + M.w13_r, 1, H, E * 2 * I, 128)) ||
-                !tmap_2d_sw64(&td, b + L.gu, 2, 2 * I, R, 32) || !tmap_sf(&tsa, b + M.x_r_sf, (uint64_t)R * H / 32) ||
-                !tmap_sf(&tsb, b + M.w13_r_sf, (uint64_t)E * 2 * I * H / 32))
+                !(L.fp4w ? tmap_2d_fp4(&tb, b + M.w13_r, H, E * 2 * I, 256)
+                         : tmap_2d(&tb, b + M.w13_r, 1, H, E * 2 * I, 256)) ||
+                !tmap_2d_sw64(&td, b + L.gu, 2, 2 * I, R, 32))
                 return cudaErrorInvalidValue;
             a.b_fmt = L.fp4w ? kFmtE2M1B : 0u;
             a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 128); a.b_rows_e = (int)(2 * I);
@@ -1149,20 +1100,19 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.out0 = b + L.hid; a.out1 = b + L.gu;
             a.q0 = reinterpret_cast<uint8_t*>(b + M.h_r); a.q0_sf = reinterpret_cast<uint8_t*>(b + M.h_r_sf);
             return kind == GemmKind::FwdGateUp
-                       ? run<256, false, false, true, false, EPI_SWIGLU, true>(c, ta, tb, a, &td, &td, &tsa, &tsb)
-                       : run<256, false, false, true, false, EPI_GU_ONLY, true>(c, ta, tb, a, &td, &td, &tsa, &tsb);
+                       ? run<256, false, false, true, false, EPI_SWIGLU, true>(c, ta, tb, a, &td, &td)
+                       : run<256, false, false, true, false, EPI_GU_ONLY, true>(c, ta, tb, a, &td, &td);
         case GemmKind::FwdDown:
             if (!tmap_2d(&ta, b + M.h_r, 1, I, R, 128) ||
-                !(L.fp4w ? tmap_2d_fp4(&tb, b + M.w2_r, I, E * H, 128) : tmap_2d(&tb, b + M.w2_r, 1, I, E * H, 128)) ||
-                !tmap_2d_sw64(&tc, b + L.ypart, 2, H, R, 32) || !tmap_sf(&tsa, b + M.h_r_sf, (uint64_t)R * I / 32) ||
-                !tmap_sf(&tsb, b + M.w2_r_sf, (uint64_t)E * H * I / 32))
+                !(L.fp4w ? tmap_2d_fp4(&tb, b + M.w2_r, I, E * H, 256) : tmap_2d(&tb, b + M.w2_r, 1, I, E * H, 256)) ||
+                !tmap_2d_sw64(&tc, b + L.ypart, 2, H, R, 32))
                 return cudaErrorInvalidValue;
             a.b_fmt = L.fp4w ? kFmtE2M1B : 0u;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 128); a.b_rows_e = (int)H;
             a.sfA = u8(M.h_r_sf); a.sfA_kt = (int)(I / 128);
             a.sfB = u8(M.w2_r_sf); a.sfB_kt = (int)(I / 128);
             a.out0 = b + L.ypart; a.ld0 = (int)H;
-            return run<256, false, false, false, false, EPI_WEIGHTED, true>(c, ta, tb, a, &tc, nullptr, &tsa, &tsb);
+            return run<256, false, false, false, false, EPI_WEIGHTED, true>(c, ta, tb, a, &tc);
         case GemmKind::BwdDown:
             if (!tmap_2d(&ta, b + M.dy_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w2_c, 1, I, E * H, 128))
                 return cudaErrorInvalidValue;
@@ -1177,14 +1127,13 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             return run<128, false, true, false, false, EPI_SWIGLU_BWD, true>(c, ta, tb, a);
         case GemmKind::BwdGateUp:
             if (!tmap_2d(&ta, b + M.dg_r, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.w13_c, 1, H, E * 2 * I, 128) ||
-                !tmap_2d_sw64(&tc, b + L.ypart, 2, H, R, 32) || !tmap_sf(&tsa, b + M.dg_r_sf, (uint64_t)R * 2 * I / 32) ||
-                !tmap_sf(&tsb, b + M.w13_c_sf, (uint64_t)E * 2 * I * H / 32))
+                !tmap_2d_sw64(&tc, b + L.ypart, 2, H, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(2 * I / 128); a.b_rows_e = (int)(2 * I);
             a.sfA = u8(M.dg_r_sf); a.sfA_kt = (int)(2 * I / 128);
             a.sfB = u8(M.w13_c_sf); a.sfB_kt = (int)(E * 2 * I / 128);
             a.out0 = b + L.ypart; a.ld0 = (int)H;
-            return run<256, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a, &tc, nullptr, &tsa, &tsb);
+            return run<256, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a, &tc);
         case GemmKind::WgradDown:
             // weight gradients keep 128 x 128 tiles with two accumulators: their contraction over an
             // expert's rows is short, so a drained single accumulator would stall the MMAs, and the
