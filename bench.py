@@ -148,6 +148,7 @@ PROFILED_TRAFFIC = {("qwen3_30b_a3b", "gemm_fwd_gate_up_swiglu"): 4 * (343.536e6
 GEMM_FLOPS = {  # algorithmic FLOPs per launch of each grouped GEMM (BF16 or MXFP8), in units of S*H*I
     "gemm_fwd_gate_up_swiglu": 4, "gemm_fwd_gate_up_save": 4, "gemm_fwd_down_weighted": 2,
     "gemm_bwd_down_swiglu_bwd": 2, "gemm_bwd_gate_up": 4, "gemm_wgrad_down": 2, "gemm_wgrad_gate_up": 4,
+    "gemm_fwd_down_reduce": 2,
 }
 
 
@@ -221,8 +222,9 @@ def timed(fn, n, ws, stream):
     return allreduce_max(e0.elapsed_time(e1), ws)
 
 
-def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
-    """Times fwd, bwd and the checkpointed layer for one workload; returns a dict of results."""
+def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e, fwd_flags=0):
+    """Times fwd, bwd and the checkpointed layer for one workload; returns a dict of results.
+    fwd_flags are OR-ed into every forward call (MOE_FLAG_FUSED_COMBINE for the fused variant)."""
     import torch
 
     dev = torch.device("cuda", local)
@@ -249,7 +251,7 @@ def measure(bd, gen, cfg, steps, warmup, ws, local, with_e2e):
     RW = bd.MOE_FLAG_REUSE_WEIGHTS if mx else 0
 
     def fwd(flags=0):
-        bd.moe_fwd(d["x"], d["topk_idx"], d["topk_w"], d["W13"], d["W2"], d["y"], sc, flags=flags)
+        bd.moe_fwd(d["x"], d["topk_idx"], d["topk_w"], d["W13"], d["W2"], d["y"], sc, flags=flags | fwd_flags)
 
     def bwd(flags=0):
         bd.moe_bwd(d["dy"], d["x"], d["topk_idx"], d["topk_w"], d["W13"], d["W2"], d["dx"], d["dW13"], d["dW2"],
@@ -604,15 +606,20 @@ def run_ours(args, rank, ws, local):
     line["device_status"] = sm["device_status"]
     summary[cfg.name] = compact(cfg.name, sm)
 
-    def side(name, steps):
+    def side(name, steps, fwd_flags=0, label=None):
         c = gen.CONFIGS[name]
-        mm = measure(bd, gen, c, steps, args.warmup, ws, local, with_e2e=False)
+        mm = measure(bd, gen, c, steps, args.warmup, ws, local, with_e2e=False, fwd_flags=fwd_flags)
         r = summarize(mm, pk["burst"][c.precision], pk["src"][c.precision])
         r["workload"] = f"{c.name}: T={c.T} H={c.H} I={c.I} E={c.E} k={c.k} {c.precision} {c.routing} routing"
         r["peak_tflops"] = {"value": pk["burst"][c.precision], "source": pk["src"][c.precision]}
         r.update(secondary_fracs(r, c.precision, pk))
-        summary[c.name] = compact(c.name, r)
+        summary[label or c.name] = compact(c.name, r)
         return r
+
+    if not args.no_extra and prec == "bf16":
+        # the combine fused into the down projection (atomic fp32 reduction by token, opt-in flag)
+        line["fused_combine"] = side(args.config, args.steps, bd.MOE_FLAG_FUSED_COMBINE,
+                                     label=args.config + "_fused_combine")
 
     if not args.no_mx and prec == "bf16":
         # the same layer in MXFP8 (E4M3 + E8M0 per 32 along K, fp32 weight gradients) and with the

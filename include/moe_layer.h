@@ -92,6 +92,14 @@ typedef struct {
  * keeps them).  Returns MOE_ERR_STATE (before any launch) if the scratch handle records no
  * quantisation of these pointers at the current epoch. */
 #define MOE_FLAG_REUSE_WEIGHTS 0x4u
+/* moe_fwd only, BF16 forward (MOE_BF16, MOE_FP8_BWD; MOE_ERR_UNSUPPORTED for the others): the
+ * combine is fused into the down projection, one call with no intermediate Ypart rows (the pages'
+ * single fused layer: MarkTechPost, "Prime Intellect Releases Prime Mega MoE", section "How does
+ * the fused kernel work?").  The down GEMM's epilogue adds w * o of every routed row into an fp32
+ * [T, H] accumulator in scratch by vector atomic reductions, and a final pass rounds it to y.  y is
+ * then not bitwise reproducible: the fp32 additions follow the tiles' timing, so runs may differ in
+ * the last bit of an element; without the flag the combine sums in a fixed order. */
+#define MOE_FLAG_FUSED_COMBINE 0x8u
 
 /* Host-side handle of a caller-owned device scratch buffer of at least moe_scratch_bytes(desc)
  * bytes.  `epoch` is the caller's: a counter it advances whenever x, W13 or W2 may have changed in

@@ -17,7 +17,7 @@ from . import build as _build
 # ---- C structures ---------------------------------------------------------------------------
 MOE_BF16, MOE_MXFP8, MOE_FP8_BWD, MOE_FP8_FP4 = 0, 1, 2, 3
 MOE_DT_BF16, MOE_DT_F32, MOE_DT_I32 = 0, 1, 2
-MOE_FLAG_SAVE_GU, MOE_FLAG_REUSE_FWD, MOE_FLAG_REUSE_WEIGHTS = 0x1, 0x2, 0x4
+MOE_FLAG_SAVE_GU, MOE_FLAG_REUSE_FWD, MOE_FLAG_REUSE_WEIGHTS, MOE_FLAG_FUSED_COMBINE = 0x1, 0x2, 0x4, 0x8
 (MOE_VIEW_COUNTS, MOE_VIEW_OFFSETS, MOE_VIEW_PERM, MOE_VIEW_INV, MOE_VIEW_PAD_OFFSETS, MOE_VIEW_XPERM,
  MOE_VIEW_HID, MOE_VIEW_GU, MOE_VIEW_YPART, MOE_VIEW_DG, MOE_VIEW_HW, MOE_VIEW_DYPERM) = range(12)
 MOE_DEV_OK, MOE_DEV_BAD_EXPERT, MOE_DEV_TIMEOUT = 0, 1, 2

@@ -39,7 +39,7 @@ constexpr int kRowBytes = 128;                       // bytes of K per smem row 
 constexpr int kATileBytes = kBM * kRowBytes;         // 16 KB
 constexpr int kSfAtom = 512;                         // 128 MN x 4 K-blocks of E8M0 scales
 
-enum Epi : int { EPI_SWIGLU = 0, EPI_GU_ONLY, EPI_WEIGHTED, EPI_SWIGLU_BWD, EPI_PLAIN, EPI_WGRAD };
+enum Epi : int { EPI_SWIGLU = 0, EPI_GU_ONLY, EPI_WEIGHTED, EPI_SWIGLU_BWD, EPI_PLAIN, EPI_WGRAD, EPI_WEIGHTED_RED };
 
 // Epilogue warps: the SwiGLU backward reads [g|u] and writes three outputs per element and needs
 // two warps per TMEM lane quarter to keep up with the MMAs; the other epilogues use one.
@@ -54,7 +54,8 @@ constexpr int gemm_threads() { return 64 + 32 * epi_warps<EPI, SINGLE>(); }
 template <int EPI, bool MX, int BN>
 constexpr bool tma_out() {
     return (!(MX && BN == 256) && epi_warps<EPI, MX && BN == 256>() == 4 &&
-            (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WGRAD)) ||
+            (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WGRAD ||
+             EPI == EPI_WEIGHTED_RED)) ||
            (!MX && EPI == EPI_SWIGLU_BWD) ||
            (MX && BN == 256 && (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY));
 }
@@ -153,6 +154,8 @@ struct GemmArgs {
     int r_atoms;               // padded row capacity / 128 (K atoms of the row-blocked scales)
     uint32_t b_fmt;            // B-format bits OR-ed into the block-scaled instruction descriptor
                                // (kFmtE2M1B: MXFP4 weights, unpacked to 16-byte rows by the TMA)
+    float* yacc;               // fused combine: fp32 [T, H] accumulator the epilogue reduces into
+    int k;                     // routed slots per token (slot / k = token)
     long long wait_limit;      // cycles after which a pipeline wait gives up (MOE_DEV_TIMEOUT)
     int withhold_loads;        // test of the bounded waits: the producer issues no operand loads
 };
@@ -700,6 +703,30 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                             box_store(&tmC, box, lane, t.n0 + 64 * b, orow);
                         }
                     }
+                } else if constexpr (EPI == EPI_WEIGHTED_RED) {
+                    // w o of the warp's 32 rows, 32 fp32 columns at a time, staged row-major in the box;
+                    // then 8 lanes per row add 16 bytes each into the row's token of the accumulator,
+                    // so one vector reduction instruction covers four whole 128-byte row segments
+                    const int slot = a.row_slot[grow];
+                    const float w = slot >= 0 ? a.topk_w[slot] : 0.f;
+                    const int tok = slot >= 0 ? slot / a.k : -1;
+#pragma unroll 1
+                    for (int b = 0; b < BN / 32; ++b) {
+                        tmem_ld32(tacc + 32 * b, v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] *= w;
+                        __syncwarp();                       // the box's previous chunk is read out
+                        box_put_f32x32(sbox, lane, v);
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int rr = 4 * i + (lane >> 3), ch = lane & 7;
+                            const int trow = __shfl_sync(0xffffffffu, tok, rr);
+                            const uint4 q = ld_shared_v4(sbox + rr * 128 + ((ch ^ (rr & 7)) << 4));
+                            if (trow >= 0)
+                                red_add_f32x4(a.yacc + (long long)trow * a.ld0 + t.n0 + 32 * b + 4 * ch, q);
+                        }
+                    }
                 } else {   // EPI_WEIGHTED, EPI_PLAIN: one bf16 row block
                     float w = 1.f;
                     if constexpr (EPI == EPI_WEIGHTED) {
@@ -1034,6 +1061,13 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 64); a.b_rows_e = (int)H;
             a.out0 = b + L.ypart; a.ld0 = (int)H;
             return run<256, false, false, false, false, EPI_WEIGHTED, false>(c, ta, tb, a, &tc);
+        case GemmKind::FwdDownReduce:
+            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 256))
+                return cudaErrorInvalidValue;
+            a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 64); a.b_rows_e = (int)H;
+            a.yacc = reinterpret_cast<float*>(b + L.ypart); a.ld0 = (int)H;
+            // the reducing epilogue stages in its box but stores nothing by TMA: no output map
+            return run<256, false, false, false, false, EPI_WEIGHTED_RED, false>(c, ta, tb, a, &ta);
         case GemmKind::BwdDown: {
             const int bn = bwd_down_bn(I);
             if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 64) ||
@@ -1171,11 +1205,13 @@ cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, b
     a.status = c.status;
     a.E = (int)L.E;
     a.I = (int)L.I;
+    a.k = (int)L.k;
     a.out_f32 = out_f32 ? 1 : 0;
     a.save_gu = save_gu ? 1 : 0;
     a.wait_limit = c.wait_limit > 0 ? c.wait_limit : kWaitTimeoutCycles;
     a.withhold_loads = (c.test_flags & MOE_TEST_WITHHOLD_LOADS) ? 1 : 0;
-    const bool fwd = kind == GemmKind::FwdGateUp || kind == GemmKind::FwdGateUpSaveOnly || kind == GemmKind::FwdDown;
+    const bool fwd = kind == GemmKind::FwdGateUp || kind == GemmKind::FwdGateUpSaveOnly || kind == GemmKind::FwdDown ||
+                     kind == GemmKind::FwdDownReduce;
     const bool mx = fwd ? L.mx_fwd : L.mx_bwd;   // fp8_bwd: BF16 forward products, MXFP8 backward ones
     const int trace_id = (mx ? kTraceGemmMx : kTraceGemm) + (int)kind;
     trace_begin(c.st, trace_id);

@@ -34,7 +34,7 @@ struct MxLayout {
 struct Layout {
     int64_t T, H, I, E, k, S, rows, nb_route, n_dtw;
     size_t ctrl, hist, cnt, off, pad_off, mtile, order, base, perm, inv, pos, row_slot;
-    size_t xperm, hid, gu, ypart, dyperm, dg, hw, dtw;
+    size_t xperm, hid, gu, ypart, dyperm, dg, hw, dtw;   // ypart also holds the fused combine's fp32 [T, H]
     bool mx_fwd, mx_bwd, mx_on;   // forward / backward GEMMs in MXFP8; either (MXFP8 regions exist)
     bool fp4w;                    // FP8 x FP4 forward: w13_r / w2_r hold MXFP4 (packed E2M1)
     MxLayout mx;
@@ -70,6 +70,9 @@ cudaError_t launch_routing_kernels(cudaStream_t st, const int32_t* topk_idx, int
 cudaError_t launch_gather(const Ctx& c, const void* src0, void* dst0, const void* src1, void* dst1);
 // out[t] = sum_j part[pos[t*k+j]] (fixed j order); optionally dtopk_w[s] = sum_n dtw[pos[s], n]
 cudaError_t launch_combine(const Ctx& c, const void* part, void* out, float* dtopk_w);
+// fused combine: zero the fp32 [T, H] accumulator (before FwdDownReduce), and round it to bf16 y
+cudaError_t launch_reduce_zero(const Ctx& c);
+cudaError_t launch_reduce_finish(const Ctx& c, void* y);
 
 // router (the step before the layer): top-k of fp32 logits with the softmax over the selected,
 // and its backward; T = 0 launches nothing
@@ -86,7 +89,9 @@ enum class GemmKind : int {
     BwdGateUp,         // dXpart = [dg|du] W13[e]
     WgradDown,         // dW2[e] = dY_perm^T (w h) over the expert's rows
     WgradGateUp,       // dW13[e] = [dg|du]^T X_perm over the expert's rows
+    FwdDownReduce,     // o = h W2[e]^T, epilogue adds w o into the fp32 [T, H] accumulator (fused combine)
 };
+constexpr int kGemmKinds = 8;
 cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, bool out_f32, bool save_gu);
 // N tile of the backward down-projection product (and so the number of <dA, h> partials per row)
 int bwd_down_bn(int64_t I);
@@ -103,7 +108,7 @@ cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int 
 // tracing ids: one per kernel kind; the GEMM kinds follow kTraceGemm (BF16) and kTraceGemmMx
 enum TraceId : int {
     kTraceRouteHist = 0, kTraceRouteScan, kTraceRoutePlace, kTraceGather, kTraceCombine, kTraceQuant,
-    kTraceGemm, kTraceGemmMx = kTraceGemm + 7, kTraceKinds = kTraceGemmMx + 7
+    kTraceReduceFinish, kTraceGemm, kTraceGemmMx = kTraceGemm + kGemmKinds, kTraceKinds = kTraceGemmMx + kGemmKinds
 };
 
 // tracing hooks used by the launch sequence

@@ -55,7 +55,8 @@ bool make_layout(const moe_desc* d, Layout* L) {
     L->xperm = take((size_t)rows * d->H * 2);
     L->hid = take((size_t)rows * d->I * 2);
     L->gu = take((size_t)rows * 2 * d->I * 2);
-    L->ypart = take((size_t)rows * d->H * 2);   // also dXpart in the backward
+    // also dXpart in the backward, and the fused combine's fp32 [T, H] accumulator
+    L->ypart = take(std::max((size_t)rows * d->H * 2, (size_t)d->T * d->H * 4));
     L->dyperm = take((size_t)rows * d->H * 2);
     L->dg = take((size_t)rows * 2 * d->I * 2);
     L->hw = take((size_t)rows * d->I * 2);
@@ -97,11 +98,12 @@ bool make_layout(const moe_desc* d, Layout* L) {
 // tracing
 // ------------------------------------------------------------------------------------------
 static const char* kTraceNames[kTraceKinds] = {
-    "route_hist", "route_scan", "route_place", "gather_rows", "combine_rows", "mx_quant",
+    "route_hist", "route_scan", "route_place", "gather_rows", "combine_rows", "mx_quant", "reduce_finish",
     "gemm_fwd_gate_up_swiglu", "gemm_fwd_gate_up_save", "gemm_fwd_down_weighted", "gemm_bwd_down_swiglu_bwd",
-    "gemm_bwd_gate_up", "gemm_wgrad_down", "gemm_wgrad_gate_up",
+    "gemm_bwd_gate_up", "gemm_wgrad_down", "gemm_wgrad_gate_up", "gemm_fwd_down_reduce",
     "gemm_mx_fwd_gate_up_swiglu", "gemm_mx_fwd_gate_up_save", "gemm_mx_fwd_down_weighted",
     "gemm_mx_bwd_down_swiglu_bwd", "gemm_mx_bwd_gate_up", "gemm_mx_wgrad_down", "gemm_mx_wgrad_gate_up",
+    "gemm_mx_fwd_down_reduce",
 };
 
 struct TraceRec {
@@ -308,6 +310,8 @@ int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* t
     if (T > 0 && (rc = check_weight_reuse(scratch, L.mx_fwd, W13->data, W2->data))) return rc;
     const uint64_t tag = fwd_tag(scratch, x->data, topk_idx->data, topk_w->data, W13->data, W2->data);
     const bool save = (d->flags & MOE_FLAG_SAVE_GU) != 0;
+    const bool fused = (d->flags & MOE_FLAG_FUSED_COMBINE) != 0;
+    if (fused && L.mx_fwd) return MOE_ERR_UNSUPPORTED;   // the fused combine has a BF16 epilogue only
     if (T == 0) {
         scratch->state[0] = save ? tag : 0;
         return MOE_OK;
@@ -329,8 +333,15 @@ int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* t
         MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, nullptr, nullptr));
     }
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUp, W13->data, nullptr, false, save));  // MXFP8: emits E4M3 h
-    MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdDown, W2->data, nullptr, false, false));
-    MOE_TRY_CUDA(launch_combine(c, base + L.ypart, y->data, nullptr));
+    if (fused) {
+        // the down product's epilogue adds w o into an fp32 accumulator by token; no Ypart rows
+        MOE_TRY_CUDA(launch_reduce_zero(c));
+        MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdDownReduce, W2->data, nullptr, false, false));
+        MOE_TRY_CUDA(launch_reduce_finish(c, y->data));
+    } else {
+        MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdDown, W2->data, nullptr, false, false));
+        MOE_TRY_CUDA(launch_combine(c, base + L.ypart, y->data, nullptr));
+    }
     // routing and dispatched rows are rewritten identically for the same inputs, so an earlier
     // saved [g|u] of these inputs stays valid; anything else invalidates it
     if (save)

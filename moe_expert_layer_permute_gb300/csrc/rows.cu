@@ -121,7 +121,32 @@ __global__ void __launch_bounds__(kRowThreads, 4) combine_rows_kernel(const uint
     }
 }
 
+// y = bf16(acc) over the fused combine's fp32 [T, H] accumulator, 8 values per thread and step
+__global__ void __launch_bounds__(kRowThreads) reduce_finish_kernel(const float4* __restrict__ acc,
+                                                                     uint4* __restrict__ out, long long n8) {
+    for (long long i = (long long)blockIdx.x * kRowThreads + threadIdx.x; i < n8;
+         i += (long long)gridDim.x * kRowThreads) {
+        const float4 a = __ldg(acc + 2 * i), b = __ldg(acc + 2 * i + 1);
+        out[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                            pack_bf16x2(b.z, b.w));
+    }
+}
+
 static int row_grid(const Ctx& c) { return c.num_sms * 8; }
+
+cudaError_t launch_reduce_zero(const Ctx& c) {
+    const Layout& L = *c.L;
+    return cudaMemsetAsync(c.base + L.ypart, 0, (size_t)L.T * L.H * 4, c.st);
+}
+
+cudaError_t launch_reduce_finish(const Ctx& c, void* y) {
+    const Layout& L = *c.L;
+    trace_begin(c.st, kTraceReduceFinish);
+    reduce_finish_kernel<<<row_grid(c), kRowThreads, 0, c.st>>>(reinterpret_cast<const float4*>(c.base + L.ypart),
+                                                                 reinterpret_cast<uint4*>(y), L.T * L.H / 8);
+    trace_end(c.st, kTraceReduceFinish);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gather(const Ctx& c, const void* src0, void* dst0, const void* src1, void* dst1) {
     const Layout& L = *c.L;
