@@ -406,51 +406,12 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             const uint32_t stage_tx = kStageBytes - (a.b_fmt ? kBTileBytes / 2 : 0);
             // (with withhold_loads nothing is issued, so the MMA warp's first wait runs out while no
             // copy is in flight)
-            // Grouped-M products: the CTAs sharing an A slice (the n-tiles of one m-tile) or a B slice
-            // (the m-tiles of one expert at one n-tile) run in step, so each new K slice is a first
-            // touch that waits on DRAM for all of them.  One CTA per shared slice (n-tile 0 for A, the
-            // expert's first m-tile or pair for B) brings it into L2 kPfAhead slices before its own
-            // load, into the first slices of its next tile as well; the others then hit L2.
-            constexpr int kPfAhead = 6;
-            auto b_row_of = [&](const Tile& u) { return u.e * a.b_rows_e + ((SPLIT && MX) ? u.nt * BN : u.n0); };
-            auto prefetch = [&](const Tile& u, int q) {
-                const int k0 = q * kElems;
-                if (u.nt == 0 && !A_MN) tma_prefetch_2d(&tmA, k0, u.m0);
-                const int lm = u.m0 / kBM - s_mtile[u.e];
-                if ((PAIR ? (lm >> 1) : lm) != 0) return;
-                if (!B_MN) {
-                    if (TWO) {
-                        tma_prefetch_2d(&tmB, k0, (SPLIT && !MX) ? u.e * a.b_rows_e + rank * a.b_up + u.n0
-                                                                 : b_row_of(u) + rank * (BN / 2));
-                    } else if (SPLIT && !MX) {
-                        tma_prefetch_2d(&tmB, k0, u.e * a.b_rows_e + u.n0);
-                        tma_prefetch_2d(&tmB, k0, u.e * a.b_rows_e + a.b_up + u.n0);
-                    } else {
-                        tma_prefetch_2d(&tmB, k0, b_row_of(u));
-                    }
-                } else {
-                    constexpr int nch = BN / kMnChunk;
-#pragma unroll
-                    for (int c = 0; c < (TWO ? nch / 2 : nch); ++c)
-                        tma_prefetch_2d(&tmB, u.n0 + kMnChunk * ((TWO ? rank * nch / 2 : 0) + c), u.e * a.b_rows_e + k0);
-                }
-            };
             for (int L = unit0; L < num_tiles && ok && !a.withhold_loads; L += unit_stride) {
                 const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
-                const bool has_next = L + unit_stride < num_tiles;
-                Tile tn = t;
-                if (!WGRAD && has_next) tn = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L + unit_stride, a, s_mtile, s_pair, rank);
                 // first B row of the tile (K-major B); MXFP8 gate/up weights are stored with
                 // 128-row blocks of [64 gate | 64 up] rows, so the split tile is one block
-                const int b_row0 = b_row_of(t);
-                if (!WGRAD && L == unit0)
-                    for (int q = 0; q < kPfAhead && q < t.kb; ++q) prefetch(t, q);
+                const int b_row0 = t.e * a.b_rows_e + ((SPLIT && MX) ? t.nt * BN : t.n0);
                 for (int kb = 0; kb < t.kb; ++kb) {
-                    if constexpr (!WGRAD) {
-                        const int q = kb + kPfAhead;
-                        if (q < t.kb) prefetch(t, q);
-                        else if (has_next && q - t.kb < tn.kb) prefetch(tn, q - t.kb);
-                    }
                     if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, a.status, a.wait_limit)) { ok = false; break; }
                     uint8_t* dA = sA + stage * kATileBytes;
                     uint8_t* dB = sB + stage * kBTileBytes;
