@@ -308,6 +308,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const GemmArgs a) {
+    grid_dep_wait();
     static_assert(!TWO || !MX, "two-SM MMAs run in CTA pairs, BF16 only");
     constexpr bool PAIR = TWO;                           // clusters of two CTAs exist only for them
     constexpr int kStages = ring_stages<TWO, MX, BN, WGRAD>();
@@ -1016,22 +1017,21 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
         }
     });
     if (attr_err != cudaSuccess) return attr_err;
-    if (!PAIR) {
-        kern<<<c.num_sms, kThreads, smem, c.st>>>(ta, tb, tcm, tdm, a);
-        return cudaGetLastError();
-    }
+    if (!PAIR) return launch_pdl(kern, c.num_sms, kThreads, smem, c.st, ta, tb, tcm, tdm, a);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = c.st;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, ta, tb, tcm, tdm, a);
 }
 

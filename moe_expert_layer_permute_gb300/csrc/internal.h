@@ -10,6 +10,23 @@
 
 namespace moe {
 
+// Launches `kern` with programmatic stream serialization (see grid_dep_wait in common.cuh): the
+// launch may begin while the previous kernel on `st` finishes; the kernel itself waits for it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 constexpr int kBM = 128;          // rows of a GEMM tile; each expert's rows are padded to a multiple
 constexpr int kBK = 64;           // bf16 elements of K per pipeline stage (one 128-byte row)
 constexpr int kRouteChunk = 2048; // slots per block of the routing kernels

@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
                                                              uint8_t* __restrict__ q_row, uint8_t* __restrict__ sf_row,
                                                              uint8_t* __restrict__ q_col, uint8_t* __restrict__ sf_col,
                                                              int gate_up_I, const int* __restrict__ row_slot, int k) {
+    grid_dep_wait();
     __shared__ __align__(16) __nv_bfloat16 tile[kQRows][kQCols + 8];
     __shared__ __align__(16) uint8_t qt[kQRows][kQCols + 16];
     __shared__ __align__(16) uint8_t s_sfr[512];
@@ -237,12 +238,12 @@ cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int 
     dim3 grid(C / kQCols, (unsigned)(R_max / 128));
     auto kern = fp4 ? mx_quant_kernel<true> : mx_quant_kernel<false>;
     trace_begin(c.st, kTraceQuant);
-    kern<<<grid, kQThreads, 0, c.st>>>(
-        reinterpret_cast<const __nv_bfloat16*>(src), R_max, C, tiles_dev, reinterpret_cast<uint8_t*>(q_row),
-        reinterpret_cast<uint8_t*>(sf_row), reinterpret_cast<uint8_t*>(q_col), reinterpret_cast<uint8_t*>(sf_col),
-        gate_up_I, row_slot, (int)c.L->k);
+    const cudaError_t err = launch_pdl(
+        kern, grid, kQThreads, 0, c.st, reinterpret_cast<const __nv_bfloat16*>(src), R_max, C, tiles_dev,
+        reinterpret_cast<uint8_t*>(q_row), reinterpret_cast<uint8_t*>(sf_row), reinterpret_cast<uint8_t*>(q_col),
+        reinterpret_cast<uint8_t*>(sf_col), gate_up_I, row_slot, (int)c.L->k);
     trace_end(c.st, kTraceQuant);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace moe

@@ -41,6 +41,7 @@ template <int C>
 __global__ void __launch_bounds__(32 * kRouterWarps) router_fwd_kernel(const float* __restrict__ logits, int T, int E,
                                                                        int k, int* __restrict__ topk_idx,
                                                                        float* __restrict__ topk_w) {
+    grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const long long t = (long long)blockIdx.x * kRouterWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(32 * kRouterWarps) router_bwd_kernel(const int
                                                                        const float* __restrict__ topk_w,
                                                                        const float* __restrict__ dtopk_w, int T, int E,
                                                                        int k, float* __restrict__ dlogits) {
+    grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const long long t = (long long)blockIdx.x * kRouterWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -107,8 +109,7 @@ __global__ void __launch_bounds__(32 * kRouterWarps) router_bwd_kernel(const int
 template <int C>
 static cudaError_t fwd_c(cudaStream_t st, const float* logits, int T, int E, int k, int* idx, float* w) {
     const int blocks = (T + kRouterWarps - 1) / kRouterWarps;
-    router_fwd_kernel<C><<<blocks, 32 * kRouterWarps, 0, st>>>(logits, T, E, k, idx, w);
-    return cudaGetLastError();
+    return launch_pdl(router_fwd_kernel<C>, blocks, 32 * kRouterWarps, 0, st, logits, T, E, k, idx, w);
 }
 
 cudaError_t launch_router_fwd(cudaStream_t st, const float* logits, int T, int E, int k, int* topk_idx,
@@ -127,8 +128,8 @@ cudaError_t launch_router_bwd(cudaStream_t st, const int* topk_idx, const float*
                               int E, int k, float* dlogits) {
     if (T == 0) return cudaSuccess;
     const int blocks = (T + kRouterWarps - 1) / kRouterWarps;
-    router_bwd_kernel<<<blocks, 32 * kRouterWarps, 0, st>>>(topk_idx, topk_w, dtopk_w, T, E, k, dlogits);
-    return cudaGetLastError();
+    return launch_pdl(router_bwd_kernel, blocks, 32 * kRouterWarps, 0, st, topk_idx, topk_w, dtopk_w, T, E, k,
+                      dlogits);
 }
 
 }  // namespace moe

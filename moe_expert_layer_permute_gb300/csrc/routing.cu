@@ -28,6 +28,7 @@ constexpr int kRouteThreads = 256;
 
 __global__ void __launch_bounds__(kRouteThreads) route_hist_kernel(const int32_t* __restrict__ idx, int S, int E,
                                                                     int* __restrict__ hist, int* status) {
+    grid_dep_wait();
     extern __shared__ int sh_cnt[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) sh_cnt[e] = 0;
     __syncthreads();
@@ -72,6 +73,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict_
                                                            int* __restrict__ cnt, int* __restrict__ off,
                                                            int* __restrict__ pad_off, int* __restrict__ mtile,
                                                            int* __restrict__ order, int* __restrict__ base) {
+    grid_dep_wait();
     __shared__ int sh_cnt[kMaxExperts];
     __shared__ int sh_warp[32];
     const int e = threadIdx.x;
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_place_kernel(
     const int32_t* __restrict__ idx, int S, int E, const int* __restrict__ base, const int* __restrict__ off,
     const int* __restrict__ pad_off, const int* __restrict__ cnt, int* __restrict__ perm, int* __restrict__ inv,
     int* __restrict__ pos, int* __restrict__ row_slot) {
+    grid_dep_wait();
     constexpr int kWarps = kRouteThreads / 32;
     extern __shared__ int sh[];
     int* ctr = sh;          // [E]   next sorted position of each expert for this block
@@ -175,22 +178,26 @@ __global__ void __launch_bounds__(kRouteThreads) route_place_kernel(
 cudaError_t launch_routing_kernels(cudaStream_t st, const int32_t* topk_idx, int S, int E, const RoutingBufs& r,
                                    int* status) {
     const int nb = (S + kRouteChunk - 1) / kRouteChunk;
+    cudaError_t err = cudaSuccess;
     if (nb > 0) {
         trace_begin(st, kTraceRouteHist);
-        route_hist_kernel<<<nb, kRouteThreads, E * sizeof(int), st>>>(topk_idx, S, E, r.hist, status);
+        err = launch_pdl(route_hist_kernel, nb, kRouteThreads, E * sizeof(int), st, topk_idx, S, E, r.hist, status);
         trace_end(st, kTraceRouteHist);
     }
+    if (err != cudaSuccess) return err;
     trace_begin(st, kTraceRouteScan);
-    route_scan_kernel<<<1, 1024, 0, st>>>(r.hist, nb, E, r.cnt, r.off, r.pad_off, r.mtile, r.order, r.base);
+    err = launch_pdl(route_scan_kernel, 1, 1024, 0, st, (const int*)r.hist, nb, E, r.cnt, r.off, r.pad_off, r.mtile,
+                     r.order, r.base);
     trace_end(st, kTraceRouteScan);
+    if (err != cudaSuccess) return err;
     if (nb > 0) {
         trace_begin(st, kTraceRoutePlace);
         const size_t sm = (size_t)(E + 8 * E) * sizeof(int);
-        route_place_kernel<<<nb, kRouteThreads, sm, st>>>(topk_idx, S, E, r.base, r.off, r.pad_off, r.cnt, r.perm,
-                                                          r.inv, r.pos, r.row_slot);
+        err = launch_pdl(route_place_kernel, nb, kRouteThreads, sm, st, topk_idx, S, E, (const int*)r.base,
+                         (const int*)r.off, (const int*)r.pad_off, (const int*)r.cnt, r.perm, r.inv, r.pos, r.row_slot);
         trace_end(st, kTraceRoutePlace);
     }
-    return cudaGetLastError();
+    return err;
 }
 
 cudaError_t launch_routing(const Ctx& c, const int32_t* topk_idx) {

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const uint4* _
                                                                    const int* __restrict__ row_slot,
                                                                    const int* __restrict__ mtile_total, int k,
                                                                    int row_vecs) {
+    grid_dep_wait();
     const int nrows = (*mtile_total) * kBM;
     const int wpb = kRowThreads / 32;
     const int lane = threadIdx.x & 31;
@@ -77,6 +78,7 @@ __global__ void __launch_bounds__(kRowThreads, 4) combine_rows_kernel(const uint
                                                                     const int* __restrict__ pos, int T, int k,
                                                                     int row_vecs, const float* __restrict__ dtw,
                                                                     int n_dtw, float* __restrict__ dtopk_w) {
+    grid_dep_wait();
     constexpr int kBatch = 4;   // routed rows loaded per batch (for each of the two chunks)
     const int wpb = kRowThreads / 32;
     const int lane = threadIdx.x & 31;
@@ -124,6 +126,7 @@ __global__ void __launch_bounds__(kRowThreads, 4) combine_rows_kernel(const uint
 // y = bf16(acc) over the fused combine's fp32 [T, H] accumulator, 8 values per thread and step
 __global__ void __launch_bounds__(kRowThreads) reduce_finish_kernel(const float4* __restrict__ acc,
                                                                      uint4* __restrict__ out, long long n8) {
+    grid_dep_wait();
     for (long long i = (long long)blockIdx.x * kRowThreads + threadIdx.x; i < n8;
          i += (long long)gridDim.x * kRowThreads) {
         const float4 a = __ldg(acc + 2 * i), b = __ldg(acc + 2 * i + 1);
@@ -142,34 +145,36 @@ cudaError_t launch_reduce_zero(const Ctx& c) {
 cudaError_t launch_reduce_finish(const Ctx& c, void* y) {
     const Layout& L = *c.L;
     trace_begin(c.st, kTraceReduceFinish);
-    reduce_finish_kernel<<<row_grid(c), kRowThreads, 0, c.st>>>(reinterpret_cast<const float4*>(c.base + L.ypart),
-                                                                 reinterpret_cast<uint4*>(y), L.T * L.H / 8);
+    const cudaError_t err = launch_pdl(reduce_finish_kernel, row_grid(c), kRowThreads, 0, c.st,
+                                       reinterpret_cast<const float4*>(c.base + L.ypart), reinterpret_cast<uint4*>(y),
+                                       (long long)(L.T * L.H / 8));
     trace_end(c.st, kTraceReduceFinish);
-    return cudaGetLastError();
+    return err;
 }
 
 cudaError_t launch_gather(const Ctx& c, const void* src0, void* dst0, const void* src1, void* dst1) {
     const Layout& L = *c.L;
     const int row_vecs = (int)(L.H * 2 / 16);
     trace_begin(c.st, kTraceGather);
-    gather_rows_kernel<<<row_grid(c), kRowThreads, 0, c.st>>>(
-        reinterpret_cast<const uint4*>(src0), reinterpret_cast<uint4*>(dst0), reinterpret_cast<const uint4*>(src1),
-        reinterpret_cast<uint4*>(dst1), reinterpret_cast<const int*>(c.base + L.row_slot),
-        reinterpret_cast<const int*>(c.base + L.mtile) + L.E, (int)L.k, row_vecs);
+    const cudaError_t err = launch_pdl(
+        gather_rows_kernel, row_grid(c), kRowThreads, 0, c.st, reinterpret_cast<const uint4*>(src0),
+        reinterpret_cast<uint4*>(dst0), reinterpret_cast<const uint4*>(src1), reinterpret_cast<uint4*>(dst1),
+        reinterpret_cast<const int*>(c.base + L.row_slot), reinterpret_cast<const int*>(c.base + L.mtile) + L.E,
+        (int)L.k, row_vecs);
     trace_end(c.st, kTraceGather);
-    return cudaGetLastError();
+    return err;
 }
 
 cudaError_t launch_combine(const Ctx& c, const void* part, void* out, float* dtopk_w) {
     const Layout& L = *c.L;
     const int row_vecs = (int)(L.H * 2 / 16);
     trace_begin(c.st, kTraceCombine);
-    combine_rows_kernel<<<row_grid(c), kRowThreads, 0, c.st>>>(
-        reinterpret_cast<const uint4*>(part), reinterpret_cast<uint4*>(out),
-        reinterpret_cast<const int*>(c.base + L.pos), (int)L.T, (int)L.k, row_vecs,
+    const cudaError_t err = launch_pdl(
+        combine_rows_kernel, row_grid(c), kRowThreads, 0, c.st, reinterpret_cast<const uint4*>(part),
+        reinterpret_cast<uint4*>(out), reinterpret_cast<const int*>(c.base + L.pos), (int)L.T, (int)L.k, row_vecs,
         reinterpret_cast<const float*>(c.base + L.dtw), (int)L.n_dtw, dtopk_w);
     trace_end(c.st, kTraceCombine);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace moe
