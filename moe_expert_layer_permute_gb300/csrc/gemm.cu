@@ -104,6 +104,13 @@ __device__ __forceinline__ void box64_put_bf16x32(uint32_t sbox, int lane, const
                                 pack_bf16x2(scale * f[4], scale * f[5]), pack_bf16x2(scale * f[6], scale * f[7])));
     }
 }
+// 32 bf16 values already packed in pairs (p[0..15]) into a 32-row x 64-byte box (64-byte swizzle)
+__device__ __forceinline__ void box64_put_packed(uint32_t sbox, int lane, const uint32_t* p) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+        st_shared_v4(sbox + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4),
+                     make_uint4(p[4 * cc], p[4 * cc + 1], p[4 * cc + 2], p[4 * cc + 3]));
+}
 // hands the staged box to the async proxy and stores it at {c0 (column), c1 (row)}
 __device__ __forceinline__ void box_store(const CUtensorMap* m, uint8_t* box, int lane, int c0, int c1) {
     fence_proxy_async_cta();
@@ -610,6 +617,18 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
         uint32_t acc_phase = 0;
         for (int L = unit0; L < num_tiles; L += unit_stride) {
             const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
+            // BF16 SwiGLU backward: the thread's first chunk of saved g, u (32 columns each, packed
+            // bf16) is requested before the accumulator wait, so that its latency overlaps the wait
+            uint4 gnext[4], unext[4];
+            if constexpr (EPI == EPI_SWIGLU_BWD && !MX) {
+                const __nv_bfloat16* gurow = a.gu + ((long long)t.m0 + quarter * 32 + lane) * (2LL * a.I);
+                const int col = t.n0 + 32 * half;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    gnext[q] = __ldg(reinterpret_cast<const uint4*>(gurow + col) + q);
+                    unext[q] = __ldg(reinterpret_cast<const uint4*>(gurow + a.I + col) + q);
+                }
+            }
             if (!mbar_wait(tfull + acc, acc_phase, abort_flag, a.status, a.wait_limit)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + lane_addr + (uint32_t)(acc * BN);
@@ -780,6 +799,73 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                     for (int j = 0; j < 32; ++j) v[j] *= w;
                     store_bf16x32(out + grow * (long long)a.ld0 + t.n0 + 32 * c, v);
                 }
+            } else if constexpr (EPI == EPI_SWIGLU_BWD && !MX) {
+                // dA -> dg, du, w h per 32-column chunk; the next chunk's saved g, u are in flight
+                // while this one is computed and stored, and outputs are packed to bf16 pairs as they
+                // are produced (raw inputs 32 + next 32 + packed outputs 48 registers)
+                const int slot = a.row_slot[grow];
+                const float w = slot >= 0 ? a.topk_w[slot] : 0.f;
+                const __nv_bfloat16* gurow = a.gu + grow * (2LL * a.I);
+                uint8_t* box = sOut + (warp - 2) * 2048;
+                const uint32_t sbox = smem_u32(box);
+                const int brow = t.m0 + 32 * quarter;
+                float dot = 0.f;
+#pragma unroll 1
+                for (int c = half; c < BN / 32; c += kHalves) {
+                    const int col = t.n0 + 32 * c;
+                    uint4 graw[4], uraw[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        graw[q] = gnext[q];
+                        uraw[q] = unext[q];
+                    }
+                    if (c + kHalves < BN / 32) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            gnext[q] = __ldg(reinterpret_cast<const uint4*>(gurow + col + 32 * kHalves) + q);
+                            unext[q] = __ldg(reinterpret_cast<const uint4*>(gurow + a.I + col + 32 * kHalves) + q);
+                        }
+                    }
+                    tmem_ld32(tacc + 32 * c, v);   // dA
+                    uint32_t dgp[16], dup[16], hwp[16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t gw[4] = {graw[q].x, graw[q].y, graw[q].z, graw[q].w};
+                        const uint32_t uw[4] = {uraw[q].x, uraw[q].y, uraw[q].z, uraw[q].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 gf = unpack_bf16x2(gw[i]), uf = unpack_bf16x2(uw[i]);
+                            const float gg[2] = {gf.x, gf.y}, uu[2] = {uf.x, uf.y};
+                            float o_dg[2], o_du[2], o_hw[2];
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const float dA = v[8 * q + 2 * i + e2];
+                                const float sg = sigmoidf_fast(gg[e2]);
+                                const float sl = gg[e2] * sg;
+                                const float h = sl * uu[e2];
+                                dot += dA * h;
+                                const float dh = w * dA;
+                                o_dg[e2] = dh * uu[e2] * (sg + sl * (1.f - sg));
+                                o_du[e2] = dh * sl;
+                                o_hw[e2] = w * h;
+                            }
+                            dgp[4 * q + i] = pack_bf16x2(o_dg[0], o_dg[1]);
+                            dup[4 * q + i] = pack_bf16x2(o_du[0], o_du[1]);
+                            hwp[4 * q + i] = pack_bf16x2(o_hw[0], o_hw[1]);
+                        }
+                    }
+                    // dg, du and w h through the warp's 2 KB box, one after the other
+                    box_acquire(lane);
+                    box64_put_packed(sbox, lane, dgp);
+                    box_store(&tmC, box, lane, col, brow);
+                    box_acquire(lane);
+                    box64_put_packed(sbox, lane, dup);
+                    box_store(&tmC, box, lane, a.I + col, brow);
+                    box_acquire(lane);
+                    box64_put_packed(sbox, lane, hwp);
+                    box_store(&tmD, box, lane, col, brow);
+                }
+                a.dtw[grow * (2 * a.n_tiles) + 2 * t.nt + half] = dot;
             } else if constexpr (EPI == EPI_SWIGLU_BWD) {
                 const int slot = a.row_slot[grow];
                 const float w = slot >= 0 ? a.topk_w[slot] : 0.f;
