@@ -163,7 +163,6 @@ struct GemmArgs {
                                // (kFmtE2M1B: MXFP4 weights, unpacked to 16-byte rows by the TMA)
     float* yacc;               // fused combine: fp32 [T, H] accumulator the epilogue reduces into
     int k;                     // routed slots per token (slot / k = token)
-    int T;                     // tokens (gathered A: row T is out of range and reads zeros)
     long long wait_limit;      // cycles after which a pipeline wait gives up (MOE_DEV_TIMEOUT)
     int withhold_loads;        // test of the bounded waits: the producer issues no operand loads
 };
@@ -311,17 +310,13 @@ constexpr int ring_stages() { return (TWO || (MX && BN == 128 && WGRAD)) ? 6 : k
 // TWO: clusters of two CTAs on two m-tiles of one expert and the same n-tile; the leader CTA
 // issues cta_group::2 MMAs (M = 256) over both CTAs' shared memory and tensor memory, each CTA
 // holding half of every B tile, which it loads itself (no load is multicast).
-// GA: the A operand (K-major, not two-SM) is gathered straight from the token rows by TMA
-// tile::gather4, four rows per copy, one copy per producer lane (tmA then maps the [T, K] token
-// tensor with a one-row box): the dispatched copy of the rows is never written.
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool TWO, bool GA = false>
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool TWO>
 __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const GemmArgs a) {
     grid_dep_wait();
     static_assert(!TWO || !MX, "two-SM MMAs run in CTA pairs, BF16 only");
-    static_assert(!GA || (!TWO && !A_MN && !WGRAD), "gathered A: single-CTA K-major products");
     constexpr bool PAIR = TWO;                           // clusters of two CTAs exist only for them
     constexpr int kStages = ring_stages<TWO, MX, BN, WGRAD>();
     constexpr int kElems = MX ? 128 : 64;                // K elements per stage
@@ -409,53 +404,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if constexpr (GA) {
-            // the whole warp: lane 0 waits for free stages, sets the byte count and loads B; every
-            // lane gathers four of the A tile's 128 rows (token slot / k; padding rows read row T,
-            // out of range, as zeros)
-            int stage = 0;
-            uint32_t phase = 0;
-            long long issued = 0;
-            bool ok = true;
-            for (int L = unit0; L < num_tiles && ok && !a.withhold_loads; L += unit_stride) {
-                const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
-                const int4 sl = *reinterpret_cast<const int4*>(a.row_slot + t.m0 + 4 * lane);
-                const int r0 = sl.x >= 0 ? sl.x / a.k : a.T, r1 = sl.y >= 0 ? sl.y / a.k : a.T;
-                const int r2 = sl.z >= 0 ? sl.z / a.k : a.T, r3 = sl.w >= 0 ? sl.w / a.k : a.T;
-                const int b_row0 = t.e * a.b_rows_e + ((SPLIT && MX) ? t.nt * BN : t.n0);
-                for (int kb = 0; kb < t.kb; ++kb) {
-                    int go = 1;
-                    if (lane == 0) {
-                        go = mbar_wait(empty + stage, phase ^ 1u, abort_flag, a.status, a.wait_limit) ? 1 : 0;
-                        if (go) mbar_arrive_expect_tx(full + stage, kStageBytes);
-                    }
-                    if (!__shfl_sync(0xffffffffu, go, 0)) { ok = false; break; }
-                    const int k0 = kb * kElems;
-                    tma_gather4_2d(sA + stage * kATileBytes + lane * 4 * kRowBytes, &tmA, full + stage, k0, r0, r1, r2,
-                                   r3);
-                    if (lane == 0) {
-                        uint8_t* dB = sB + stage * kBTileBytes;
-                        if (SPLIT && !MX) {
-                            tma_load_2d(dB, &tmB, full + stage, k0, t.e * a.b_rows_e + t.n0);
-                            tma_load_2d(dB + (BN / 2) * kRowBytes, &tmB, full + stage, k0,
-                                        t.e * a.b_rows_e + a.b_up + t.n0);
-                        } else {
-                            tma_load_2d(dB, &tmB, full + stage, k0, b_row0);
-                        }
-                    }
-                    ++issued;
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                }
-            }
-            if (!ok && lane == 0) {
-                for (int s = 0; s < kStages; ++s) {
-                    if (issued > s) {
-                        const long long n = (issued - s + kStages - 1) / kStages;
-                        drain_wait(full + s, (uint32_t)((n - 1) & 1));
-                    }
-                }
-            }
-        } else if (lane == 0) {
+        if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
@@ -1112,12 +1061,12 @@ static bool tmap_2d_sw64(CUtensorMap* m, const void* ptr, int esize, uint64_t in
 template <int BN, bool MX, bool WGRAD, int EPI>
 constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN); }
 
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX, bool GA = false>
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
                        const CUtensorMap* tc = nullptr, const CUtensorMap* td = nullptr) {
     constexpr bool TWO = use_two<BN, MX, WGRAD, EPI>();
     constexpr bool PAIR = TWO;
-    auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, TWO, GA>;
+    auto kern = grouped_gemm_kernel<BN, A_MN, B_MN, SPLIT, WGRAD, EPI, MX, TWO>;
     constexpr int kThreads = gemm_threads<EPI, MX && BN == 256>();
     const size_t stage = (size_t)kATileBytes + (TWO ? BN / 2 : BN) * kRowBytes + (MX ? kSfAtom * (1 + BN / 128) : 0);
     const size_t out_bytes = tma_out<EPI, MX, BN>()
@@ -1174,8 +1123,7 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
 
 int bwd_down_bn(int64_t I) { return (I % 256 == 0) ? 256 : 128; }
 
-static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, void* out, GemmArgs& a,
-                                    const void* gather_src) {
+static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, void* out, GemmArgs& a) {
     const Layout& L = *c.L;
     char* b = c.base;
     const int64_t H = L.H, I = L.I, E = L.E, R = L.rows;
@@ -1184,16 +1132,11 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
     switch (kind) {
         case GemmKind::FwdGateUp:
         case GemmKind::FwdGateUpSaveOnly:
-            // A: the dispatched rows, or (gather_src) the token rows gathered by the producer
-            if (!(gather_src ? tmap_2d(&ta, gather_src, 2, H, L.T, 1) : tmap_2d(&ta, b + L.xperm, 2, H, R, 128)) ||
-                !tmap_2d(&tb, W, 2, H, E * 2 * I, 128) || !tmap_2d(&tc, b + L.hid, 2, I, R, 32) ||
-                !tmap_2d(&td, b + L.gu, 2, 2 * I, R, 32))
+            if (!tmap_2d(&ta, b + L.xperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 128) ||
+                !tmap_2d(&tc, b + L.hid, 2, I, R, 32) || !tmap_2d(&td, b + L.gu, 2, 2 * I, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 64); a.b_rows_e = (int)(2 * I); a.b_up = (int)I;
             a.out0 = b + L.hid; a.out1 = b + L.gu;
-            if (gather_src && kind == GemmKind::FwdGateUp)
-                return run<256, false, false, true, false, EPI_SWIGLU, false, true>(c, ta, tb, a, &tc, &td);
-            if (gather_src) return cudaErrorInvalidValue;
             return kind == GemmKind::FwdGateUp
                        ? run<256, false, false, true, false, EPI_SWIGLU, false>(c, ta, tb, a, &tc, &td)
                        : run<256, false, false, true, false, EPI_GU_ONLY, false>(c, ta, tb, a, &tc, &td);
@@ -1336,8 +1279,7 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, bool out_f32, bool save_gu,
-                        const void* gather_src) {
+cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, bool out_f32, bool save_gu) {
     const Layout& L = *c.L;
     char* b = c.base;
     GemmArgs a{};
@@ -1350,7 +1292,6 @@ cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, b
     a.E = (int)L.E;
     a.I = (int)L.I;
     a.k = (int)L.k;
-    a.T = (int)L.T;
     a.out_f32 = out_f32 ? 1 : 0;
     a.save_gu = save_gu ? 1 : 0;
     a.wait_limit = c.wait_limit > 0 ? c.wait_limit : kWaitTimeoutCycles;
@@ -1360,8 +1301,7 @@ cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, b
     const bool mx = fwd ? L.mx_fwd : L.mx_bwd;   // fp8_bwd: BF16 forward products, MXFP8 backward ones
     const int trace_id = (mx ? kTraceGemmMx : kTraceGemm) + (int)kind;
     trace_begin(c.st, trace_id);
-    if (mx && gather_src) return cudaErrorInvalidValue;
-    const cudaError_t err = mx ? launch_gemm_mx(c, kind, out, a) : launch_gemm_bf16(c, kind, W, out, a, gather_src);
+    const cudaError_t err = mx ? launch_gemm_mx(c, kind, out, a) : launch_gemm_bf16(c, kind, W, out, a);
     trace_end(c.st, trace_id);
     return err;
 }

@@ -109,10 +109,7 @@ enum class GemmKind : int {
     FwdDownReduce,     // o = h W2[e]^T, epilogue adds w o into the fp32 [T, H] accumulator (fused combine)
 };
 constexpr int kGemmKinds = 8;
-// gather_src (BF16 FwdGateUp only): the [T, H] token rows the GEMM gathers its A operand from by
-// TMA (no dispatched copy needed); null reads the dispatched rows in scratch
-cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, bool out_f32, bool save_gu,
-                        const void* gather_src = nullptr);
+cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, bool out_f32, bool save_gu);
 // N tile of the backward down-projection product (and so the number of <dA, h> partials per row)
 int bwd_down_bn(int64_t I);
 

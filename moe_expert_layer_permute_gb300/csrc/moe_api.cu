@@ -329,13 +329,10 @@ int moe_fwd(const moe_tensor* x, const moe_tensor* topk_idx, const moe_tensor* t
         if ((rc = mx_weights(c, scratch, W13->data, W2->data))) return rc;
         const bool xc = save && L.mx_bwd;
         MOE_TRY_CUDA(mx_rows(c, x->data, true, (int)H, M.x_r, M.x_r_sf, xc ? M.x_c : 0, xc ? M.x_c_sf : 0));
-    } else if (save) {
+    } else {
         MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, nullptr, nullptr));
     }
-    // a BF16 forward that saves nothing gathers its rows inside the GEMM (no dispatched copy); a
-    // saving one keeps the copy, which the W13 weight gradient reads
-    MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUp, W13->data, nullptr, false, save,
-                             (!L.mx_fwd && !save) ? x->data : nullptr));  // MXFP8: emits E4M3 h
+    MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUp, W13->data, nullptr, false, save));  // MXFP8: emits E4M3 h
     if (fused) {
         // the down product's epilogue adds w o into an fp32 accumulator by token; no Ypart rows
         MOE_TRY_CUDA(launch_reduce_zero(c));

@@ -283,21 +283,3 @@ def test_full_size_sampled(cuda_lib, name):
     # properties that hold at any size: finite outputs everywhere
     for t in (L.y, L.dx, L.dW13, L.dW2, L.dtw):
         assert torch.isfinite(t).all()
-
-
-@pytest.mark.parametrize("name", list(SMALL) + ["k1_ragged"])
-def test_gathered_rows_forward_is_bitwise_the_dispatched_one(cuda_lib, name):
-    """A BF16 forward that saves nothing gathers its token rows inside the gate/up GEMM (TMA
-    gather4, padding rows read as zeros) instead of writing the dispatched copy; it must give the
-    same y, bit for bit, as the saving forward that reads the dispatched copy."""
-    cfg = SMALL.get(name) or gen.custom_config("k1_ragged", T=777, H=256, I=128, E=5, k=1, seed=52)
-    inp = gen.make_inputs(cfg)
-    L = DeviceLayer(cuda_lib, inp)
-    L.fwd()
-    torch.cuda.synchronize()
-    assert L.status() == 0
-    y_gathered = L.y.clone()
-    L.fwd(flags=cuda_lib.MOE_FLAG_SAVE_GU)
-    torch.cuda.synchronize()
-    assert torch.equal(y_gathered, L.y)
-    assert rel_fro(f64(y_gathered), oracle.forward(*_oracle_args(inp))) < TOL
