@@ -70,19 +70,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Non-blocking probe: has the phase with the given parity completed?  (try_wait may suspend the
-// thread for a while before it answers no; test_wait answers at once.)
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 // Waits for the phase with the given parity to complete.  Gives up (returns false) when
 // *abort becomes non-zero or the wait exceeds `limit` cycles; in the latter case it raises *abort
 // itself and records MOE_DEV_TIMEOUT.

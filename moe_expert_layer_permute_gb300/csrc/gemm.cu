@@ -530,16 +530,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             bool ok = true;
             const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB), sf_base = smem_u32(sSF);
             long long consumed = 0;
-            // block-scaled products: a stage's scale atoms go to its tensor-memory columns before its
-            // MMAs read them; the next stage's are copied right after this stage's MMAs are issued
-            // if its operands have already landed, so the copy overlaps these MMAs
-            int sf_ready = -1;   // ring stage whose scales are already in tensor memory
-            auto copy_sf = [&](int st) {
-                const uint32_t cols = tmem_base + kAccStages * BN + st * kSfCols;
-                const uint32_t ss = sf_base + st * kSfBytes;
-#pragma unroll
-                for (int c = 0; c <= kSfBAtoms; ++c) tmem_cp_sf_atom(cols + 4 * c, sdesc_plain(ss + kSfAtom * c, 128));
-            };
             for (int L = unit0; L < num_tiles && ok; L += unit_stride) {
                 const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
                 if (!(TWO ? mbar_wait_cluster(tempty + acc, acc_phase ^ 1u, abort_flag, a.status, a.wait_limit)
@@ -552,7 +542,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                     const uint32_t sa = a_base + stage * kATileBytes, sb = b_base + stage * kBTileBytes;
                     if constexpr (MX) {
                         const uint32_t sf_cols = tmem_base + kAccStages * BN + stage * kSfCols;
-                        if (sf_ready != stage) copy_sf(stage);
+                        const uint32_t ss = sf_base + stage * kSfBytes;
+#pragma unroll
+                        for (int c = 0; c <= kSfBAtoms; ++c)
+                            tmem_cp_sf_atom(sf_cols + 4 * c, sdesc_plain(ss + kSfAtom * c, 128));
 #pragma unroll
                         for (int ks = 0; ks < kElems / kMmaK; ++ks) {
                             const uint64_t ad = A_MN ? sdesc_sw128(sa + ks * kMnStep, kMnLbo, 1024)
@@ -577,20 +570,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         mma_commit_pair_mc(empty + stage, kPeers);
                     else
                         mma_commit(empty + stage);
-                    if constexpr (MX) {
-                        // after the release (a commit tracks every earlier tcgen05 operation, so a copy
-                        // issued before it would hold the stage back): the next stage's scale slot was
-                        // last read by MMAs that have completed (its operands were refilled only after
-                        // their commit), so it can be written now if its operands have landed
-                        const int ns = stage + 1 == kStages ? 0 : stage + 1;
-                        const uint32_t nph = stage + 1 == kStages ? phase ^ 1u : phase;
-                        sf_ready = -1;
-                        if (mbar_test_wait(full + ns, nph)) {
-                            tc_fence_after();
-                            copy_sf(ns);
-                            sf_ready = ns;
-                        }
-                    }
                     ++consumed;
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
