@@ -31,6 +31,13 @@ namespace moe {
 
 constexpr int kQRows = 32, kQCols = 128, kQThreads = 128;
 
+// Staged-tile layout: a row holds 16 chunks of 8 bf16 (16 bytes) at a 272-byte pitch, chunk j at
+// position j ^ 2 * ((j >> 3) & 1).  The row-blocked pass has four lanes per row reading chunks
+// 4b + q (b = the lane's 32-column block): without the swap chunks q and q + 8 share banks; with it
+// eight lanes (two rows) read eight distinct bank groups.  Loads into the tile (16 consecutive
+// chunks per row) and the column pass (32-bit words of one row) stay conflict-free.
+__device__ __forceinline__ int tile_chunk(int j) { return j ^ (((j >> 3) & 1) << 1); }
+
 // Maximum |x| of packed bf16 pairs: |bf16| bit patterns order like unsigned 16-bit integers, so a
 // per-halfword unsigned max of the sign-cleared words gives both halves' maxima at once.
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t w) { return __vmaxu2(acc, w & 0x7FFF7FFFu); }
@@ -72,7 +79,7 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
     __shared__ __align__(16) uint8_t qt[kQRows][kQCols + 16];
     __shared__ __align__(16) uint8_t s_sfr[512];
     __shared__ __align__(16) uint8_t s_sfc[512];
-    __shared__ uint32_t s_cmax[2][64];  // column-pair maxima of the two row halves (column blocks)
+    __shared__ uint2 s_cmax[4][32];     // column-quad maxima of the four row quarters (column blocks)
     __shared__ long long s_src[128];   // source row of each tile row (-1: a zero padding row)
     const long long rt = (long long)blockIdx.y * 128;
     const long long R = tiles_dev ? (long long)(*tiles_dev) * kBM : R_max;
@@ -174,44 +181,59 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
     for (int sub = 0; sub < 4; ++sub) {
         const long long r0 = rt + 32 * sub;
 #pragma unroll
-        for (int it = 0; it < 4; ++it) *reinterpret_cast<uint4*>(&tile[it * 8 + lr][lc]) = nxt[it];
+        for (int it = 0; it < 4; ++it)
+            *reinterpret_cast<uint4*>(&tile[it * 8 + lr][8 * tile_chunk(lc >> 3)]) = nxt[it];
         __syncthreads();
         if (sub < 3) load_pass(sub + 1, nxt);   // in flight while this pass is quantised
         if (q_row) {
             uint4 w[4];
-            const uint4* src4 = reinterpret_cast<const uint4*>(&tile[rr][32 * b]);
+            const uint4* row4 = reinterpret_cast<const uint4*>(&tile[rr][0]);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) w[q] = src4[q];
+            for (int q = 0; q < 4; ++q) w[q] = row4[tile_chunk(4 * b + q)];
             emit_row(w, sub);
         }
         if (!FP4 && q_col) {
-            // thread -> columns 2 cp, 2 cp + 1 (cp = 32 (warp & 1) + lane) over rows 16 rh .. + 15
-            // (rh = warp >> 1): one 32-bit shared load holds both columns of a row, one packed
-            // unsigned max tracks both columns' |value| maxima, and the two row halves' maxima
-            // meet in shared memory; each row's two codes leave as one 2-byte store
-            const int cp = 32 * ((t >> 5) & 1) + (t & 31), rh = t >> 6;
-            uint32_t w[16];
-            uint32_t m2 = 0;
+            // thread -> columns 4 cq .. 4 cq + 3 (cq = lane) over rows 8 rq .. 8 rq + 7 (rq = warp): one
+            // 8-byte shared load holds the four columns of a row, two packed unsigned maxima track
+            // their |value| maxima, the four row quarters' maxima meet in shared memory (8 bytes a
+            // thread), and each row's four codes leave as one 4-byte store
+            const int cq = t & 31, rq = t >> 5;
+            uint2 w[8];
+            uint32_t ma = 0, mb = 0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                w[j] = reinterpret_cast<const uint32_t*>(&tile[16 * rh + j][0])[cp];
-                m2 = absmax_bf16x2(m2, w[j]);
+            for (int j = 0; j < 8; ++j) {
+                w[j] = reinterpret_cast<const uint2*>(&tile[8 * rq + j][0])[2 * tile_chunk(cq >> 1) + (cq & 1)];
+                ma = absmax_bf16x2(ma, w[j].x);
+                mb = absmax_bf16x2(mb, w[j].y);
             }
-            s_cmax[rh][cp] = m2;
+            s_cmax[rq][cq] = make_uint2(ma, mb);
             __syncthreads();
-            m2 = __vmaxu2(m2, s_cmax[rh ^ 1][cp]);
-            uint8_t sf0, sf1;
-            float inv0, inv1;
-            mx_scale_bits((m2 & 0xFFFFu) << 16, &sf0, &inv0);      // column 2 cp
-            mx_scale_bits(m2 & 0xFFFF0000u, &sf1, &inv1);          // column 2 cp + 1
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *reinterpret_cast<uint16_t*>(&qt[16 * rh + j][2 * cp]) =
-                    to_e4m3x2(__uint_as_float(w[j] << 16) * inv0, __uint_as_float(w[j] & 0xFFFF0000u) * inv1);
-            if (rh == 0) {   // columns 2 cp, 2 cp + 1, row block sub
-                const int ca = 2 * cp, cb = 2 * cp + 1;
-                s_sfc[16 * (ca & 31) + 4 * (ca >> 5) + sub] = sf0;
-                s_sfc[16 * (cb & 31) + 4 * (cb >> 5) + sub] = sf1;
+            for (int o = 1; o < 4; ++o) {
+                const uint2 m = s_cmax[(rq + o) & 3][cq];
+                ma = __vmaxu2(ma, m.x);
+                mb = __vmaxu2(mb, m.y);
+            }
+            uint8_t sf[4];
+            float inv[4];
+            mx_scale_bits((ma & 0xFFFFu) << 16, &sf[0], &inv[0]);   // column 4 cq
+            mx_scale_bits(ma & 0xFFFF0000u, &sf[1], &inv[1]);       // column 4 cq + 1
+            mx_scale_bits((mb & 0xFFFFu) << 16, &sf[2], &inv[2]);   // column 4 cq + 2
+            mx_scale_bits(mb & 0xFFFF0000u, &sf[3], &inv[3]);       // column 4 cq + 3
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint32_t*>(&qt[8 * rq + j][4 * cq]) =
+                    (uint32_t)to_e4m3x2(__uint_as_float(w[j].x << 16) * inv[0],
+                                        __uint_as_float(w[j].x & 0xFFFF0000u) * inv[1]) |
+                    ((uint32_t)to_e4m3x2(__uint_as_float(w[j].y << 16) * inv[2],
+                                         __uint_as_float(w[j].y & 0xFFFF0000u) * inv[3])
+                     << 16);
+            if (rq == 0) {   // columns 4 cq .. 4 cq + 3, row block sub
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int col = 4 * cq + i;
+                    s_sfc[16 * (col & 31) + 4 * (col >> 5) + sub] = sf[i];
+                }
             }
             __syncthreads();
             // the 32 x 128 codes out, thread -> (row t/4, 32 columns at 32 (t%4))
