@@ -234,6 +234,31 @@ static int check_weight_reuse(const moe_scratch* s, bool needs_copies, const voi
     return s->state[1] == weights_tag(s, w13, w2) ? MOE_OK : MOE_ERR_STATE;
 }
 
+// One side stream per device (non-blocking) with a fork and a join event, created on first use
+// and kept until exit; null if they cannot be created (the work then stays on the caller's stream).
+// Calls on the same device share them, so, as for a shared scratch buffer, calls on one device must
+// be ordered on one stream.
+struct SideStream {
+    cudaStream_t st;
+    cudaEvent_t fork, join;
+};
+static SideStream* side_stream() {
+    static std::mutex mu;
+    static SideStream streams[64];
+    static int state[64] = {0};   // 0: not tried, 1: ready, -1: unavailable
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (state[dev] == 0) {
+        SideStream& s = streams[dev];
+        const bool ok = cudaStreamCreateWithFlags(&s.st, cudaStreamNonBlocking) == cudaSuccess &&
+                        cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) == cudaSuccess &&
+                        cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) == cudaSuccess;
+        state[dev] = ok ? 1 : -1;
+    }
+    return state[dev] == 1 ? &streams[dev] : nullptr;
+}
+
 static Ctx make_ctx(cudaStream_t st, moe_scratch* s, const Layout* L, int nsm, const void* topk_w) {
     char* base = reinterpret_cast<char*>(s->data);
     Ctx c{st, base, L, reinterpret_cast<int*>(base + L->ctrl), nsm, reinterpret_cast<const float*>(topk_w)};
@@ -407,9 +432,25 @@ int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_id
     // MXFP8: the SwiGLU-backward epilogue emits the E4M3 copies of [dg|du] and w h directly
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::BwdDown, W2->data, nullptr, false, false));
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::BwdGateUp, W13->data, nullptr, false, false));
+    // dx = combine(dXpart) needs only the product above, and the two weight gradients do not read
+    // what it reads or writes: it runs on the device's side stream (forked and joined by events,
+    // so the caller's stream orders everything after this call as before), where its HBM-bound
+    // sum overlaps the tensor-bound weight-gradient products
+    SideStream* side = side_stream();
+    if (side) {
+        Ctx cs = c;
+        cs.st = side->st;
+        MOE_TRY_CUDA(cudaEventRecord(side->fork, st));
+        MOE_TRY_CUDA(cudaStreamWaitEvent(side->st, side->fork, 0));
+        MOE_TRY_CUDA(launch_combine(cs, base + L.ypart, dx->data, reinterpret_cast<float*>(dtopk_w->data)));
+        MOE_TRY_CUDA(cudaEventRecord(side->join, side->st));
+    }
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::WgradDown, nullptr, dW2->data, f32_2, false));
     MOE_TRY_CUDA(launch_gemm(c, GemmKind::WgradGateUp, nullptr, dW13->data, f32_13, false));
-    MOE_TRY_CUDA(launch_combine(c, base + L.ypart, dx->data, reinterpret_cast<float*>(dtopk_w->data)));
+    if (side)
+        MOE_TRY_CUDA(cudaStreamWaitEvent(st, side->join, 0));
+    else
+        MOE_TRY_CUDA(launch_combine(c, base + L.ypart, dx->data, reinterpret_cast<float*>(dtopk_w->data)));
     scratch->state[0] = tag;  // routing, dispatched x and [g|u] now describe these inputs
     return MOE_OK;
 }
