@@ -36,6 +36,11 @@
  *   - Alignment: every device pointer must be 16-byte aligned (TMA); the scratch pointer 256-byte.
  *   - T == 0 is a valid no-op (dW13 / dW2 are zeroed by moe_bwd).
  *   - Calls that share one scratch buffer must be ordered on one stream.
+ *   - moe_bwd runs its final combine (dx) on a side stream of the device, forked from and joined
+ *     back to `stream` by events inside the call, so that it overlaps the weight-gradient products;
+ *     work enqueued on `stream` after the call is ordered after all of it.  The side stream and its
+ *     events are created on the first moe_bwd on a device and shared by all calls on that device:
+ *     host threads that call moe_bwd concurrently on one device must serialise those calls.
  */
 #ifndef MOE_LAYER_H
 #define MOE_LAYER_H
