@@ -118,6 +118,9 @@ int bwd_down_bn(int64_t I);
 // row-blocked copy of a [E*2I, H] gate/up weight in [64 gate | 64 up] row blocks.
 // With row_slot (padded rows only) source row r is row_slot[r] / k, zero where row_slot[r] < 0.
 // fp4: the row-blocked copy holds MXFP4 (packed E2M1, C / 2 bytes a row) and q_col must be null.
+// the row-blocked E4M3 copy of the dispatched rows of src [T, H], token-major (quant.cu)
+cudaError_t launch_mx_rows_token(const Ctx& c, const void* src, const int* pos, const int* row_slot,
+                                 const int* tiles_dev, void* q_row, void* sf_row);
 cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int C, const int* tiles_dev, void* q_row,
                             void* sf_row, void* q_col, void* sf_col, int gate_up_I, const int* row_slot = nullptr,
                             bool fp4 = false);
@@ -125,7 +128,7 @@ cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int 
 // tracing ids: one per kernel kind; the GEMM kinds follow kTraceGemm (BF16) and kTraceGemmMx
 enum TraceId : int {
     kTraceRouteHist = 0, kTraceRouteScan, kTraceRoutePlace, kTraceGather, kTraceCombine, kTraceQuant,
-    kTraceReduceFinish, kTraceGemm, kTraceGemmMx = kTraceGemm + kGemmKinds, kTraceKinds = kTraceGemmMx + kGemmKinds
+    kTraceReduceFinish, kTraceQuantRows, kTraceGemm, kTraceGemmMx = kTraceGemm + kGemmKinds, kTraceKinds = kTraceGemmMx + kGemmKinds
 };
 
 // tracing hooks used by the launch sequence

@@ -253,6 +253,105 @@ __global__ void __launch_bounds__(kQThreads) mx_quant_kernel(const __nv_bfloat16
             reinterpret_cast<const uint4*>(s_sfc)[t - 32];
 }
 
+// The row-blocked E4M3 copy of the dispatched rows, token-major.  A row block (32 consecutive
+// columns of one row) does not depend on where the row is dispatched, so one warp quantises each
+// token row once and stores its codes and scale bytes to every one of the token's k dispatched
+// rows (pos); units past the tokens write the padding rows' zero codes and zero scales, 32 rows
+// a unit.  This reads x from HBM once, in order, where the dispatched-row walk of mx_quant_kernel
+// reads each token row k times from L2 while its stores stream past.
+// Lane l holds the 16-byte vectors l + 32 q (q < 8) of each 2048-column chunk, so block
+// l / 4 + 8 q of the chunk lives in lanes 4 (l / 4) .. + 3 and its maximum takes two shuffles.
+// The scale bytes of four consecutive blocks form one 4-byte word of the atom layout above;
+// lane g < 16 ends up holding the chunk's word g and stores it for each destination row.
+constexpr int kTokThreads = 256;
+
+__global__ void __launch_bounds__(kTokThreads) mx_rows_token_kernel(const uint4* __restrict__ src, int T, int C, int k,
+                                                                    const int* __restrict__ pos,
+                                                                    const int* __restrict__ row_slot,
+                                                                    const int* __restrict__ tiles_dev,
+                                                                    uint8_t* __restrict__ q_row,
+                                                                    uint8_t* __restrict__ sf_row) {
+    grid_dep_wait();
+    const int nrows = (*tiles_dev) * kBM;
+    const int lane = threadIdx.x & 31;
+    const int wpb = kTokThreads / 32;
+    const int stride = gridDim.x * wpb;
+    const int rv = C / 8;              // 16-byte bf16 vectors in a row
+    const long long k_atoms = C / 128;
+    const int units = T + (nrows + 31) / 32;
+    for (int u = blockIdx.x * wpb + (threadIdx.x >> 5); u < units; u += stride) {
+        if (u < T) {
+            const int p0 = lane < k ? pos[(size_t)u * k + lane] : -1;
+            for (int v0 = 0; v0 < rv; v0 += 256) {
+                const int nq = min(256, rv - v0) / 32;   // C % 256 == 0: whole 32-vector steps
+                const uint4* s = src + (size_t)u * rv + v0;
+                uint4 w[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) w[q] = q < nq ? __ldg(s + lane + 32 * q) : make_uint4(0, 0, 0, 0);
+                uint2 code[8];
+                uint32_t word = 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    code[q] = make_uint2(0, 0);
+                    if (q >= nq) continue;   // warp-uniform
+                    uint32_t m2 = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(0u, w[q].x), w[q].y), w[q].z), w[q].w);
+                    m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, 1));
+                    m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, 2));
+                    uint8_t sf;
+                    float inv;
+                    mx_scale_bits(absmax_to_f32_bits(m2), &sf, &inv);
+                    code[q] = e4m3x8(w[q], inv);
+                    // the word of blocks 8 q + 4 h .. + 3 (h = lane / 16) in every lane of half h
+                    uint32_t pk = (uint32_t)sf << (8 * ((lane >> 2) & 3));
+                    pk |= __shfl_xor_sync(0xffffffffu, pk, 4);
+                    pk |= __shfl_xor_sync(0xffffffffu, pk, 8);
+                    const uint32_t from = __shfl_sync(0xffffffffu, pk, (lane & 1) << 4);
+                    if (((lane & 15) >> 1) == q) word = from;   // lane g < 16: word g = 2 q + (g & 1)
+                }
+                for (int j0 = 0; j0 < k; j0 += 32) {
+                    const int pj = j0 == 0 ? p0 : (j0 + lane < k ? pos[(size_t)u * k + j0 + lane] : -1);
+                    const int nj = min(32, k - j0);
+                    for (int j = 0; j < nj; ++j) {
+                        const int r = __shfl_sync(0xffffffffu, pj, j);
+                        if (r < 0) continue;   // a slot with an out-of-range expert id is not dispatched
+                        uint8_t* d = q_row + (size_t)r * C + (size_t)v0 * 8;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            if (q < nq) *reinterpret_cast<uint2*>(d + 8 * (lane + 32 * q)) = code[q];
+                        if (lane < 2 * nq)
+                            *reinterpret_cast<uint32_t*>(sf_row + sf_index(r, v0 / 4 + 4 * lane, k_atoms)) = word;
+                    }
+                }
+            }
+        } else {
+            const int row0 = (u - T) * 32;
+            const bool pad = row0 + lane < nrows && row_slot[row0 + lane] < 0;
+            unsigned m = __ballot_sync(0xffffffffu, pad);
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1;
+                const long long r = row0 + b;
+                uint4* d = reinterpret_cast<uint4*>(q_row + r * C);
+                for (int v = lane; v < C / 16; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+                for (int g = lane; g < C / 128; g += 32)
+                    *reinterpret_cast<uint32_t*>(sf_row + sf_index(r, 4 * g, k_atoms)) = 0u;
+            }
+        }
+    }
+}
+
+cudaError_t launch_mx_rows_token(const Ctx& c, const void* src, const int* pos, const int* row_slot,
+                                 const int* tiles_dev, void* q_row, void* sf_row) {
+    const Layout& L = *c.L;
+    trace_begin(c.st, kTraceQuantRows);
+    const cudaError_t err = launch_pdl(mx_rows_token_kernel, c.num_sms * 8, kTokThreads, 0, c.st,
+                                       reinterpret_cast<const uint4*>(src), (int)L.T, (int)L.H, (int)L.k, pos,
+                                       row_slot, tiles_dev, reinterpret_cast<uint8_t*>(q_row),
+                                       reinterpret_cast<uint8_t*>(sf_row));
+    trace_end(c.st, kTraceQuantRows);
+    return err;
+}
+
 cudaError_t launch_mx_quant(const Ctx& c, const void* src, long long R_max, int C, const int* tiles_dev, void* q_row,
                             void* sf_row, void* q_col, void* sf_col, int gate_up_I, const int* row_slot, bool fp4) {
     if (R_max <= 0) return cudaSuccess;
