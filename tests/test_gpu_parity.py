@@ -25,6 +25,8 @@ SMALL = {
     # several m- and n-tiles per expert with ragged tails, K over several pipeline rounds
     "medium": gen.custom_config("medium", T=2048, H=512, I=256, E=16, k=4, seed=21),
     "medium_I384": gen.custom_config("medium_I384", T=1500, H=768, I=384, E=12, k=3, seed=22),
+    # wide I: four n-tiles of the forward gate/up and two of the backward down per m-tile
+    "medium_I512": gen.custom_config("medium_I512", T=1024, H=256, I=512, E=8, k=2, seed=24),
     "skew_small": gen.custom_config("skew_small", T=1024, H=256, I=128, E=32, k=8, routing="zipf", seed=23),
 }
 
