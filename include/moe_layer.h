@@ -231,11 +231,13 @@ int moe_route_static(const int32_t* topk_idx, int64_t T, int64_t k, int64_t E, i
  *   MOE_VIEW_PAD_OFFSETS int32[E+1]   start row of each expert in the padded row layout
  *   MOE_VIEW_XPERM    bf16 [rows, H]  dispatched x rows (padded layout: expert e's rows start at
  *                                     PAD_OFFSETS[e], padding rows are zero)
- *   MOE_VIEW_HID      bf16 [rows, I]  silu(g) * u of every routed row (forward)
+ *   MOE_VIEW_HID      bf16 [rows, I]  w * silu(g) * u of every routed row, w the row's routing
+ *                                     weight (BF16 forward: the down product then applies no
+ *                                     weight, and the backward reuses these rows)
  *   MOE_VIEW_GU       bf16 [rows, 2I] [g | u] pre-activations
  *   MOE_VIEW_YPART    bf16 [rows, H]  w * expert output per routed row (forward, before combine)
  *   MOE_VIEW_DG       bf16 [rows, 2I] [dg | du] (backward)
- *   MOE_VIEW_HW       bf16 [rows, I]  w * h (backward)
+ *   MOE_VIEW_HW       bf16 [rows, I]  w * h: the same region as MOE_VIEW_HID
  *   MOE_VIEW_DYPERM   bf16 [rows, H]  dispatched dy rows (backward)
  * `rows` is T*k + 128*E, the largest padded row count.  Returns MOE_ERR_SHAPE for an unknown id. */
 enum {

@@ -163,6 +163,7 @@ struct GemmArgs {
                                // (kFmtE2M1B: MXFP4 weights, unpacked to 16-byte rows by the TMA)
     float* yacc;               // fused combine: fp32 [T, H] accumulator the epilogue reduces into
     int k;                     // routed slots per token (slot / k = token)
+    int w_in_a;                // BF16 forward down: the routing weight is already in A (w h)
     long long wait_limit;      // cycles after which a pipeline wait gives up (MOE_DEV_TIMEOUT)
     int withhold_loads;        // test of the bounded waits: the producer issues no operand loads
 };
@@ -661,7 +662,14 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 const int brow = t.m0 + 32 * quarter;   // first row of the warp's boxes
                 if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
                     // columns [0, BN/2) = gate, [BN/2, BN) = up, for I-columns [n0, n0 + BN/2); per
-                    // 64 I-columns: the h box, then (saving) the g and u boxes, re-read from TMEM
+                    // 64 I-columns: the w h box (the row's routing weight applied here, so that the
+                    // down product needs none and the backward reuses w h), then (saving) the g and
+                    // u boxes, re-read from TMEM
+                    float w = 0.f;
+                    if (EPI == EPI_SWIGLU) {
+                        const int slot = a.row_slot[grow];
+                        w = slot >= 0 ? a.topk_w[slot] : 0.f;
+                    }
 #pragma unroll 1
                     for (int b = 0; b < BN / 128; ++b) {
                         if (EPI == EPI_SWIGLU) {
@@ -673,7 +681,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                                 tmem_ld32(tacc + BN / 2 + 64 * b + 32 * h, u);
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) v[j] = v[j] * sigmoidf_fast(v[j]) * u[j];
-                                box_put_bf16x32(sbox, lane, h, v, 1.f);
+                                box_put_bf16x32(sbox, lane, h, v, w);
                             }
                             box_store(&tmC, box, lane, t.n0 + 64 * b, brow);
                         }
@@ -728,7 +736,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                     // then 8 lanes per row add 16 bytes each into the row's token of the accumulator,
                     // so one vector reduction instruction covers four whole 128-byte row segments
                     const int slot = a.row_slot[grow];
-                    const float w = slot >= 0 ? a.topk_w[slot] : 0.f;
+                    const float w = a.w_in_a ? 1.f : (slot >= 0 ? a.topk_w[slot] : 0.f);
                     const int tok = slot >= 0 ? slot / a.k : -1;
 #pragma unroll 1
                     for (int b = 0; b < BN / 32; ++b) {
@@ -749,7 +757,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                     }
                 } else {   // EPI_WEIGHTED, EPI_PLAIN: one bf16 row block
                     float w = 1.f;
-                    if constexpr (EPI == EPI_WEIGHTED) {
+                    if (EPI == EPI_WEIGHTED && !a.w_in_a) {
                         const int slot = a.row_slot[grow];
                         w = slot >= 0 ? a.topk_w[slot] : 0.f;
                     }
@@ -790,7 +798,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 }
             } else if constexpr (EPI == EPI_WEIGHTED) {
                 const int slot = a.row_slot[grow];
-                const float w = slot >= 0 ? a.topk_w[slot] : 0.f;
+                const float w = a.w_in_a ? 1.f : (slot >= 0 ? a.topk_w[slot] : 0.f);
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out0);
 #pragma unroll 1
                 for (int c = half; c < BN / 32; c += kHalves) {
@@ -800,9 +808,9 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                     store_bf16x32(out + grow * (long long)a.ld0 + t.n0 + 32 * c, v);
                 }
             } else if constexpr (EPI == EPI_SWIGLU_BWD && !MX) {
-                // dA -> dg, du, w h per 32-column chunk; the next chunk's saved g, u are in flight
-                // while this one is computed and stored, and outputs are packed to bf16 pairs as they
-                // are produced (raw inputs 32 + next 32 + packed outputs 48 registers)
+                // dA -> dg, du per 32-column chunk (w h was saved by the forward); the next chunk's
+                // saved g, u are in flight while this one is computed and stored, and outputs are
+                // packed to bf16 pairs as they are produced
                 const int slot = a.row_slot[grow];
                 const float w = slot >= 0 ? a.topk_w[slot] : 0.f;
                 const __nv_bfloat16* gurow = a.gu + grow * (2LL * a.I);
@@ -827,7 +835,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         }
                     }
                     tmem_ld32(tacc + 32 * c, v);   // dA
-                    uint32_t dgp[16], dup[16], hwp[16];
+                    uint32_t dgp[16], dup[16];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const uint32_t gw[4] = {graw[q].x, graw[q].y, graw[q].z, graw[q].w};
@@ -836,7 +844,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         for (int i = 0; i < 4; ++i) {
                             const float2 gf = unpack_bf16x2(gw[i]), uf = unpack_bf16x2(uw[i]);
                             const float gg[2] = {gf.x, gf.y}, uu[2] = {uf.x, uf.y};
-                            float o_dg[2], o_du[2], o_hw[2];
+                            float o_dg[2], o_du[2];
 #pragma unroll
                             for (int e2 = 0; e2 < 2; ++e2) {
                                 const float dA = v[8 * q + 2 * i + e2];
@@ -847,23 +855,18 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                                 const float dh = w * dA;
                                 o_dg[e2] = dh * uu[e2] * (sg + sl * (1.f - sg));
                                 o_du[e2] = dh * sl;
-                                o_hw[e2] = w * h;
                             }
                             dgp[4 * q + i] = pack_bf16x2(o_dg[0], o_dg[1]);
                             dup[4 * q + i] = pack_bf16x2(o_du[0], o_du[1]);
-                            hwp[4 * q + i] = pack_bf16x2(o_hw[0], o_hw[1]);
                         }
                     }
-                    // dg, du and w h through the warp's 2 KB box, one after the other
+                    // dg and du through the warp's 2 KB box, one after the other
                     box_acquire(lane);
                     box64_put_packed(sbox, lane, dgp);
                     box_store(&tmC, box, lane, col, brow);
                     box_acquire(lane);
                     box64_put_packed(sbox, lane, dup);
                     box_store(&tmC, box, lane, a.I + col, brow);
-                    box_acquire(lane);
-                    box64_put_packed(sbox, lane, hwp);
-                    box_store(&tmD, box, lane, col, brow);
                 }
                 a.dtw[grow * (2 * a.n_tiles) + 2 * t.nt + half] = dot;
             } else if constexpr (EPI == EPI_SWIGLU_BWD) {
@@ -1146,23 +1149,26 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 64); a.b_rows_e = (int)H;
             a.out0 = b + L.ypart; a.ld0 = (int)H;
+            a.w_in_a = 1;   // A = w h from the gate/up epilogue
             return run<256, false, false, false, false, EPI_WEIGHTED, false>(c, ta, tb, a, &tc);
         case GemmKind::FwdDownReduce:
             if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 256))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 64); a.b_rows_e = (int)H;
             a.yacc = reinterpret_cast<float*>(b + L.ypart); a.ld0 = (int)H;
+            a.w_in_a = 1;
             // the reducing epilogue stages in its box but stores nothing by TMA: no output map
             return run<256, false, false, false, false, EPI_WEIGHTED_RED, false>(c, ta, tb, a, &ta);
         case GemmKind::BwdDown: {
             const int bn = bwd_down_bn(I);
+            // w h is not an output here: the forward's gate/up epilogue saved it (hid)
             if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 64) ||
-                !tmap_2d_sw64(&tc, b + L.dg, 2, 2 * I, R, 32) || !tmap_2d_sw64(&td, b + L.hw, 2, I, R, 32))
+                !tmap_2d_sw64(&tc, b + L.dg, 2, 2 * I, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(I / bn); a.k_blocks = (int)(H / 64); a.b_rows_e = (int)H;
-            a.out0 = b + L.dg; a.out1 = b + L.hw; a.dtw = reinterpret_cast<float*>(b + L.dtw);
-            return bn == 256 ? run<256, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a, &tc, &td)
-                             : run<128, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a, &tc, &td);
+            a.out0 = b + L.dg; a.dtw = reinterpret_cast<float*>(b + L.dtw);
+            return bn == 256 ? run<256, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a, &tc, &tc)
+                             : run<128, false, true, false, false, EPI_SWIGLU_BWD, false>(c, ta, tb, a, &tc, &tc);
         }
         case GemmKind::BwdGateUp:
             if (!tmap_2d(&ta, b + L.dg, 2, 2 * I, R, 128) || !tmap_2d(&tb, W, 2, H, E * 2 * I, 64) ||
@@ -1173,7 +1179,7 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
             return run<256, false, true, false, false, EPI_PLAIN, false>(c, ta, tb, a, &tc);
         case GemmKind::WgradDown: {
             const int bn = bwd_down_bn(I);
-            if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 64) || !tmap_2d(&tb, b + L.hw, 2, I, R, 64) ||
+            if (!tmap_2d(&ta, b + L.dyperm, 2, H, R, 64) || !tmap_2d(&tb, b + L.hid, 2, I, R, 64) ||
                 !tmap_2d(&tc, out, oes, I, E * H, 32))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / bn);
@@ -1239,7 +1245,7 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 128); a.b_rows_e = (int)H;
             a.sfA = u8(M.dy_r_sf); a.sfA_kt = (int)(H / 128);
             a.sfB = u8(M.w2_c_sf); a.sfB_kt = (int)(E * H / 128);
-            a.out0 = b + L.dg; a.out1 = b + L.hw; a.dtw = reinterpret_cast<float*>(b + L.dtw);
+            a.out0 = b + L.dg; a.dtw = reinterpret_cast<float*>(b + L.dtw);
             a.q0 = reinterpret_cast<uint8_t*>(b + M.dg_r); a.q0_sf = reinterpret_cast<uint8_t*>(b + M.dg_r_sf);
             a.q1 = reinterpret_cast<uint8_t*>(b + M.dg_c); a.q1_sf = reinterpret_cast<uint8_t*>(b + M.dg_c_sf);
             a.q2 = reinterpret_cast<uint8_t*>(b + M.hw_c); a.q2_sf = reinterpret_cast<uint8_t*>(b + M.hw_c_sf);

@@ -59,7 +59,7 @@ bool make_layout(const moe_desc* d, Layout* L) {
     L->ypart = take(std::max((size_t)rows * d->H * 2, (size_t)d->T * d->H * 4));
     L->dyperm = take((size_t)rows * d->H * 2);
     L->dg = take((size_t)rows * 2 * d->I * 2);
-    L->hw = take((size_t)rows * d->I * 2);
+    L->hw = L->hid;   // BF16: the gate/up epilogue stores w h there, and the backward reads it
     L->dtw = take((size_t)rows * L->n_dtw * 4);
     L->mx = MxLayout{};
     for (size_t& v : L->mx_bytes) v = 0;
@@ -427,7 +427,10 @@ int moe_bwd(const moe_tensor* dy, const moe_tensor* x, const moe_tensor* topk_id
             MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, nullptr, nullptr));
         else
             MOE_TRY_CUDA(launch_gather(c, x->data, base + L.xperm, dy->data, base + L.dyperm));
-        MOE_TRY_CUDA(launch_gemm(c, GemmKind::FwdGateUpSaveOnly, W13->data, nullptr, false, true));
+        // a BF16 backward also needs the forward's w h (its W2 weight-gradient operand); with an
+        // MXFP8 backward the SwiGLU-backward epilogue makes that operand's E4M3 copy itself
+        MOE_TRY_CUDA(launch_gemm(c, L.mx_on ? GemmKind::FwdGateUpSaveOnly : GemmKind::FwdGateUp, W13->data,
+                                 nullptr, false, true));
     } else if (!L.mx_bwd) {
         MOE_TRY_CUDA(launch_gather(c, dy->data, base + L.dyperm, nullptr, nullptr));
     }

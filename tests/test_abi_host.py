@@ -50,13 +50,15 @@ def test_scratch_bytes_rules(bd):
 def test_scratch_views_are_disjoint_and_aligned(bd):
     d = bd.make_desc(1000, 512, 256, 16, 4)
     total = bd.moe_scratch_bytes(d)
-    spans = []
+    spans = {}
     for v in range(12):
         off, nb = ctypes.c_uint64(), ctypes.c_uint64()
         assert bd.LIB.moe_scratch_view(ctypes.byref(d), v, ctypes.byref(off), ctypes.byref(nb)) == 0
         assert off.value % 256 == 0 and off.value + nb.value <= total
-        spans.append((off.value, off.value + nb.value))
-    spans.sort()
+        spans[v] = (off.value, off.value + nb.value)
+    # w h: the backward reads the rows the forward's gate/up epilogue stored, one region
+    assert spans.pop(bd.MOE_VIEW_HW) == spans[bd.MOE_VIEW_HID]
+    spans = sorted(spans.values())
     for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
         assert a1 <= b0
     off, nb = ctypes.c_uint64(), ctypes.c_uint64()

@@ -78,8 +78,9 @@ def test_forward_and_intermediates(cuda_lib, name):
     assert torch.all(xperm[:int(pad[-1])][torch.from_numpy(padmask).cuda()] == 0)
     gu = f64(L.view(cuda_lib.MOE_VIEW_GU, torch.bfloat16, (R, 2 * cfg.I))[torch.from_numpy(prow).cuda()])
     assert rel_fro(gu[:, :cfg.I], fw["g"]) < TOL and rel_fro(gu[:, cfg.I:], fw["u"]) < TOL
+    # the gate/up epilogue stores w h (the routing weight applied before the down product)
     hid = f64(L.view(cuda_lib.MOE_VIEW_HID, torch.bfloat16, (R, cfg.I))[torch.from_numpy(prow).cuda()])
-    assert rel_fro(hid, fw["h"]) < TOL
+    assert rel_fro(hid, fw["w_sorted"][:, None] * fw["h"]) < TOL
     ypart = f64(L.view(cuda_lib.MOE_VIEW_YPART, torch.bfloat16, (R, cfg.H))[torch.from_numpy(prow).cuda()])
     assert rel_fro(ypart, fw["w_sorted"][:, None] * fw["o"]) < TOL
 
