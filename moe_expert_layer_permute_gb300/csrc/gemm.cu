@@ -870,10 +870,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 }
                 a.dtw[grow * (2 * a.n_tiles) + 2 * t.nt + half] = dot;
             } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+                // MXFP8: dg, du along 2I and along the rows, and w h along the rows, as E4M3 copies
+                static_assert(MX, "the BF16 SwiGLU backward has its own epilogue above");
                 const int slot = a.row_slot[grow];
                 const float w = slot >= 0 ? a.topk_w[slot] : 0.f;
-                __nv_bfloat16* dG = reinterpret_cast<__nv_bfloat16*>(a.out0);
-                __nv_bfloat16* hw = reinterpret_cast<__nv_bfloat16*>(a.out1);
                 const __nv_bfloat16* gurow = a.gu + grow * (2LL * a.I);
                 float dot = 0.f;
 #pragma unroll 1
@@ -914,34 +914,14 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         u[j] = du;
                         v[j] = w * h;
                     }
-                    if constexpr (MX) {
-                        const long long gi = grow * (2LL * a.I);
-                        const int kq = 2 * a.I / 128;
-                        const long long kblk = grow >> 5;       // the warp's 32 rows form one block
-                        quant_row32(g, a.q0 + gi + col, a.q0_sf + sf_index(grow, col / 32, kq));
-                        quant_row32(u, a.q0 + gi + a.I + col, a.q0_sf + sf_index(grow, (a.I + col) / 32, kq));
-                        quant_col32_warp(g, a.q1 + gi + col, a.q1_sf, col, kblk, a.r_atoms);
-                        quant_col32_warp(u, a.q1 + gi + a.I + col, a.q1_sf, a.I + col, kblk, a.r_atoms);
-                        quant_col32_warp(v, a.q2 + grow * (long long)a.I + col, a.q2_sf, col, kblk, a.r_atoms);
-                    } else if constexpr (kTmaOut) {
-                        // dg, du and w h through the warp's 2 KB box, one after the other
-                        uint8_t* box = sOut + (warp - 2) * 2048;
-                        const uint32_t sbox = smem_u32(box);
-                        const int brow = t.m0 + 32 * quarter;
-                        box_acquire(lane);
-                        box64_put_bf16x32(sbox, lane, g);
-                        box_store(&tmC, box, lane, col, brow);
-                        box_acquire(lane);
-                        box64_put_bf16x32(sbox, lane, u);
-                        box_store(&tmC, box, lane, a.I + col, brow);
-                        box_acquire(lane);
-                        box64_put_bf16x32(sbox, lane, v);
-                        box_store(&tmD, box, lane, col, brow);
-                    } else {
-                        store_bf16x32(dG + grow * (2LL * a.I) + col, g);
-                        store_bf16x32(dG + grow * (2LL * a.I) + a.I + col, u);
-                        store_bf16x32(hw + grow * (long long)a.I + col, v);
-                    }
+                    const long long gi = grow * (2LL * a.I);
+                    const int kq = 2 * a.I / 128;
+                    const long long kblk = grow >> 5;       // the warp's 32 rows form one block
+                    quant_row32(g, a.q0 + gi + col, a.q0_sf + sf_index(grow, col / 32, kq));
+                    quant_row32(u, a.q0 + gi + a.I + col, a.q0_sf + sf_index(grow, (a.I + col) / 32, kq));
+                    quant_col32_warp(g, a.q1 + gi + col, a.q1_sf, col, kblk, a.r_atoms);
+                    quant_col32_warp(u, a.q1 + gi + a.I + col, a.q1_sf, a.I + col, kblk, a.r_atoms);
+                    quant_col32_warp(v, a.q2 + grow * (long long)a.I + col, a.q2_sf, col, kblk, a.r_atoms);
                 }
                 a.dtw[grow * (2 * a.n_tiles) + 2 * t.nt + half] = dot;
             } else if constexpr (EPI == EPI_PLAIN) {

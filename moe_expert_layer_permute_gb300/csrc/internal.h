@@ -99,14 +99,15 @@ cudaError_t launch_router_bwd(cudaStream_t st, const int* topk_idx, const float*
 
 // grouped GEMMs (persistent, TMA + tcgen05)
 enum class GemmKind : int {
-    FwdGateUp = 0,     // [g|u] = X_perm W13[e]^T, epilogue h = silu(g) u  (optionally saves [g|u])
-    FwdGateUpSaveOnly, // same GEMM, epilogue stores [g|u] only (backward recompute)
-    FwdDown,           // o = h W2[e]^T, epilogue Ypart = w o
-    BwdDown,           // dA = dY_perm W2[e], epilogue SwiGLU backward -> [dg|du], w h, <dA, h>
+    FwdGateUp = 0,     // [g|u] = X_perm W13[e]^T, epilogue w h = w silu(g) u (MXFP8: h, unweighted)
+                       // (optionally saves [g|u])
+    FwdGateUpSaveOnly, // same GEMM, epilogue stores [g|u] only (MXFP8 backward recompute)
+    FwdDown,           // Ypart = (w h) W2[e]^T (MXFP8: o = h W2[e]^T, epilogue Ypart = w o)
+    BwdDown,           // dA = dY_perm W2[e], epilogue SwiGLU backward -> [dg|du], <dA, h> (MXFP8: and w h)
     BwdGateUp,         // dXpart = [dg|du] W13[e]
     WgradDown,         // dW2[e] = dY_perm^T (w h) over the expert's rows
     WgradGateUp,       // dW13[e] = [dg|du]^T X_perm over the expert's rows
-    FwdDownReduce,     // o = h W2[e]^T, epilogue adds w o into the fp32 [T, H] accumulator (fused combine)
+    FwdDownReduce,     // (w h) W2[e]^T, added by the epilogue into the fp32 [T, H] accumulator (fused combine)
 };
 constexpr int kGemmKinds = 8;
 cudaError_t launch_gemm(const Ctx& c, GemmKind kind, const void* W, void* out, bool out_f32, bool save_gu);

@@ -2,12 +2,13 @@
 // backward launch sequences, device status, per-kernel tracing.
 //
 // Forward (one call, all on the caller's stream, no host synchronisation):
-//   routing -> gather x -> [g|u] = X W13^T, h = silu(g) u -> Ypart = w (h W2^T) -> y = combine
+//   routing -> gather x -> [g|u] = X W13^T, w h = w silu(g) u -> Ypart = (w h) W2^T -> y = combine
+//   (MXFP8: h is quantised unweighted and the down epilogue applies w)
 // Backward of <dy, y>:
-//   [routing -> gather x -> [g|u] recompute]  (skipped under MOE_FLAG_REUSE_FWD)
-//   gather dy -> dA = dY W2 with the SwiGLU backward in the epilogue ([dg|du], w h, <dA, h>)
-//   -> dXpart = [dg|du] W13 -> dW2 = dY^T (w h) -> dW13 = [dg|du]^T X -> dx = combine(dXpart),
-//   dtopk_w = sum of the <dA, h> partials.
+//   [routing -> gather x -> [g|u] (and w h) recompute]  (skipped under MOE_FLAG_REUSE_FWD)
+//   gather dy -> dA = dY W2 with the SwiGLU backward in the epilogue ([dg|du], <dA, h>; MXFP8
+//   also the E4M3 copy of w h) -> dXpart = [dg|du] W13 -> dW2 = dY^T (w h) -> dW13 = [dg|du]^T X
+//   -> dx = combine(dXpart), dtopk_w = sum of the <dA, h> partials.
 // The single call per direction and the GPU-only scratch in place of intermediate tensors follow
 // MarkTechPost, "Prime Intellect Releases Prime Mega MoE", section "How does the fused kernel
 // work?"; the shape rules follow ic.work analysis, section "算子下沉时代的硬件死锁暗礁".
