@@ -19,12 +19,15 @@
 // the sorted positions they leave free, [offsets[E], T*k), hold perm = -1.
 // The padded-layout outputs (pad_off, mtile, order, pos, row_slot) and the status word are
 // optional: the allocation-free entry point (route_static.cu) runs the same kernels without them.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 256;   // route_hist
+constexpr int kPlaceThreads = 512;   // route_place: a 2048-slot chunk in four rounds
 
 __global__ void __launch_bounds__(kRouteThreads) route_hist_kernel(const int32_t* __restrict__ idx, int S, int E,
                                                                     int* __restrict__ hist, int* status) {
@@ -113,21 +116,21 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int* __restrict_
     }
 }
 
-__global__ void __launch_bounds__(kRouteThreads) route_place_kernel(
+__global__ void __launch_bounds__(kPlaceThreads) route_place_kernel(
     const int32_t* __restrict__ idx, int S, int E, const int* __restrict__ base, const int* __restrict__ off,
     const int* __restrict__ pad_off, const int* __restrict__ cnt, int* __restrict__ perm, int* __restrict__ inv,
     int* __restrict__ pos, int* __restrict__ row_slot) {
     grid_dep_wait();
-    constexpr int kWarps = kRouteThreads / 32;
+    constexpr int kWarps = kPlaceThreads / 32;
     extern __shared__ int sh[];
     int* ctr = sh;          // [E]   next sorted position of each expert for this block
     int* wc = sh + E;       // [kWarps][E] per-warp counts of the current round
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int e = tid; e < E; e += kRouteThreads) ctr[e] = base[(size_t)blockIdx.x * E + e];
-    for (int i = tid; i < kWarps * E; i += kRouteThreads) wc[i] = 0;
+    for (int e = tid; e < E; e += kPlaceThreads) ctr[e] = base[(size_t)blockIdx.x * E + e];
+    for (int i = tid; i < kWarps * E; i += kPlaceThreads) wc[i] = 0;
     __syncthreads();
     const int s0 = blockIdx.x * kRouteChunk, s1 = min(S, s0 + kRouteChunk);
-    for (int r0 = s0; r0 < s1; r0 += kRouteThreads) {
+    for (int r0 = s0; r0 < s1; r0 += kPlaceThreads) {
         const int s = r0 + tid;
         const bool valid = s < s1;
         const int e = valid ? idx[s] : -1;
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_place_kernel(
             if (pos) pos[s] = -1;
         }
         __syncthreads();
-        for (int f = tid; f < E; f += kRouteThreads) {
+        for (int f = tid; f < E; f += kPlaceThreads) {
             int add = 0;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
@@ -165,12 +168,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_place_kernel(
         __syncthreads();
     }
     // sorted positions left free by dropped slots (none for valid ids)
-    for (int p = off[E] + blockIdx.x * kRouteThreads + tid; p < S; p += gridDim.x * kRouteThreads) perm[p] = -1;
+    for (int p = off[E] + blockIdx.x * kPlaceThreads + tid; p < S; p += gridDim.x * kPlaceThreads) perm[p] = -1;
     // padding rows of the groups this block owns
     if (row_slot) {
         for (int f = blockIdx.x; f < E; f += gridDim.x) {
             const int lo = pad_off[f] + cnt[f], hi = pad_off[f + 1];
-            for (int r = lo + tid; r < hi; r += kRouteThreads) row_slot[r] = -1;
+            for (int r = lo + tid; r < hi; r += kPlaceThreads) row_slot[r] = -1;
         }
     }
 }
@@ -192,8 +195,15 @@ cudaError_t launch_routing_kernels(cudaStream_t st, const int32_t* topk_idx, int
     if (err != cudaSuccess) return err;
     if (nb > 0) {
         trace_begin(st, kTraceRoutePlace);
-        const size_t sm = (size_t)(E + 8 * E) * sizeof(int);
-        err = launch_pdl(route_place_kernel, nb, kRouteThreads, sm, st, topk_idx, S, E, (const int*)r.base,
+        const size_t sm = (size_t)(E + (kPlaceThreads / 32) * E) * sizeof(int);
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [] {
+            attr_err = cudaFuncSetAttribute(route_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)((kMaxExperts + (kPlaceThreads / 32) * kMaxExperts) * sizeof(int)));
+        });
+        if (attr_err != cudaSuccess) return attr_err;
+        err = launch_pdl(route_place_kernel, nb, kPlaceThreads, sm, st, topk_idx, S, E, (const int*)r.base,
                          (const int*)r.off, (const int*)r.pad_off, (const int*)r.cnt, r.perm, r.inv, r.pos, r.row_slot);
         trace_end(st, kTraceRoutePlace);
     }
