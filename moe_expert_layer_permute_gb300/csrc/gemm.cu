@@ -57,7 +57,8 @@ constexpr bool tma_out() {
             (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WGRAD ||
              EPI == EPI_WEIGHTED_RED)) ||
            (!MX && EPI == EPI_SWIGLU_BWD) ||
-           (MX && BN == 256 && (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY));
+           (MX && BN == 256 &&
+            (EPI == EPI_WEIGHTED || EPI == EPI_PLAIN || EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY || EPI == EPI_WGRAD));
 }
 // bytes of one warp's staging box: 32 rows x 128 bytes, or 32 x 64 (64-byte swizzle) for the
 // eight-warp epilogues (the SwiGLU backward, the drained MXFP8 128 x 256 tiles), whose 4 KB
@@ -103,6 +104,14 @@ __device__ __forceinline__ void box64_put_bf16x32(uint32_t sbox, int lane, const
                      make_uint4(pack_bf16x2(scale * f[0], scale * f[1]), pack_bf16x2(scale * f[2], scale * f[3]),
                                 pack_bf16x2(scale * f[4], scale * f[5]), pack_bf16x2(scale * f[6], scale * f[7])));
     }
+}
+// 16 fp32 values into the lane's row of a 32-row x 64-byte box (64-byte swizzle)
+__device__ __forceinline__ void box64_put_f32x16(uint32_t sbox, int lane, const float* v) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+        st_shared_v4(sbox + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4),
+                     make_uint4(__float_as_uint(v[4 * cc]), __float_as_uint(v[4 * cc + 1]), __float_as_uint(v[4 * cc + 2]),
+                                __float_as_uint(v[4 * cc + 3])));
 }
 // 32 bf16 values already packed in pairs (p[0..15]) into a 32-row x 64-byte box (64-byte swizzle)
 __device__ __forceinline__ void box64_put_packed(uint32_t sbox, int lane, const uint32_t* p) {
@@ -286,16 +295,35 @@ __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& 
             }
         }
     } else if constexpr (EPI == EPI_WGRAD) {
-        const long long off = (long long)t.e * a.out_e_stride + grow * a.ld0 + t.n0 + 128 * h;
+        if (t.kb == 0) {   // an expert without rows: a zero gradient
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float o[32];
+            for (int j = 0; j < 128; ++j) d[j] = 0.f;
+        }
+        if constexpr (TMA) {
+            // rows of this expert's block of the weight gradient [E * M, N], whole 64-byte row
+            // segments through the warp's box: 16 fp32 or 32 bf16 columns a store
+            const int orow = t.e * a.m_tiles * kBM + brow;
+            const uint32_t sbox = smem_u32(box);
+            if (a.out_f32) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = t.kb > 0 ? d[32 * c + j] : 0.f;
-            if (a.out_f32)
-                store_f32x32(reinterpret_cast<float*>(a.out0) + off + 32 * c, o);
-            else
-                store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.out0) + off + 32 * c, o);
+                for (int c = 0; c < 8; ++c) {
+                    box_acquire(lane);
+                    box64_put_f32x16(sbox, lane, d + 16 * c);
+                    box_store(tmC, box, lane, t.n0 + 128 * h + 16 * c, orow);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) box64_emit(tmC, box, lane, d + 32 * c, 1.f, t.n0 + 128 * h + 32 * c, orow);
+            }
+        } else {
+            const long long off = (long long)t.e * a.out_e_stride + grow * a.ld0 + t.n0 + 128 * h;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (a.out_f32)
+                    store_f32x32(reinterpret_cast<float*>(a.out0) + off + 32 * c, d + 32 * c);
+                else
+                    store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.out0) + off + 32 * c, d + 32 * c);
+            }
         }
     }
 }
@@ -1032,8 +1060,8 @@ static bool tmap_2d_sw64(CUtensorMap* m, const void* ptr, int esize, uint64_t in
     const cuuint64_t strides[1] = {inner * esize};
     const cuuint32_t box[2] = {(cuuint32_t)(64 / esize), box_rows};
     const cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(m, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1244,23 +1272,29 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             // weight gradients keep 128 x 128 tiles with two accumulators: their contraction over an
             // expert's rows is short, so a drained single accumulator would stall the MMAs, and the
             // fp32 output stores need the epilogue to overlap the next tile
-            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 128) ||
-                !tmap_2d(&tc, out, oes, I, E * H, 32))
+            if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 128))
                 return cudaErrorInvalidValue;
-            a.m_tiles = (int)(H / 128); a.n_tiles = (int)(I / 128);
+            a.m_tiles = (int)(H / 128);
             a.sfA = u8(M.dy_c_sf); a.sfA_kt = (int)(R / 128);
             a.sfB = u8(M.hw_c_sf); a.sfB_kt = (int)(R / 128);
             a.out0 = out; a.ld0 = (int)I; a.out_e_stride = H * I;
+            if (I % 256 == 0) {
+                if (!tmap_2d_sw64(&tc, out, oes, I, E * H, 32)) return cudaErrorInvalidValue;
+                a.n_tiles = (int)(I / 256);
+                return run<256, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
+            }
+            if (!tmap_2d(&tc, out, oes, I, E * H, 32)) return cudaErrorInvalidValue;
+            a.n_tiles = (int)(I / 128);
             return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
         case GemmKind::WgradGateUp:
             if (!tmap_2d(&ta, b + M.dg_c, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.x_c, 1, H, R, 128) ||
-                !tmap_2d(&tc, out, oes, H, E * 2 * I, 32))
+                !tmap_2d_sw64(&tc, out, oes, H, E * 2 * I, 32))
                 return cudaErrorInvalidValue;
-            a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 128);
+            a.m_tiles = (int)(2 * I / 128); a.n_tiles = (int)(H / 256);   // H % 256 == 0
             a.sfA = u8(M.dg_c_sf); a.sfA_kt = (int)(R / 128);
             a.sfB = u8(M.x_c_sf); a.sfB_kt = (int)(R / 128);
             a.out0 = out; a.ld0 = (int)H; a.out_e_stride = 2 * I * H;
-            return run<128, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
+            return run<256, true, true, false, true, EPI_WGRAD, true>(c, ta, tb, a, &tc);
     }
     return cudaErrorInvalidValue;
 }
