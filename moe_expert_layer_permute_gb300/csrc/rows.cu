@@ -5,9 +5,10 @@
 // every expert on one GPU they reduce to
 //   gather  : dst[pos[t*k + j]] = src[t] for each token t and choice j, zero on the padding rows,
 //   combine : out[t] = sum_j part[pos[t*k + j]], summed in fp32 in the fixed order j = 0..k-1,
-// where the routing weight has already been applied to `part` by the down-projection epilogue
-// (aggregation by routing weight: kongchang.com, "Prime Intellect推出Prime Mega MoE", section
-// "为什么 MoE 训练特别需要融合内核").  One warp moves one row with 16-byte accesses.
+// where `part` already carries the routing weight (aggregation by routing weight: kongchang.com,
+// "Prime Intellect推出Prime Mega MoE", section "为什么 MoE 训练特别需要融合内核"): applied to h by the
+// BF16 gate/up epilogue, to the down product's output by the MXFP8 one.  The gather moves two
+// token rows per warp, the combine one token per warp, both with 16-byte accesses.
 #include "common.cuh"
 #include "internal.h"
 
