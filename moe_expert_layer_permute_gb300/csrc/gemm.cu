@@ -1206,8 +1206,10 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
     return cudaErrorInvalidValue;
 }
 
-// MXFP8: 128 x 256 tiles (one accumulator) for the forward and data-gradient products except the
-// SwiGLU backward; 128 x 128 tiles (two accumulators) for it and the weight gradients.  Operands
+// MXFP8: 128 x 256 tiles (one accumulator, drained to registers) for every product but the SwiGLU
+// backward, which keeps 128 x 128 tiles with two accumulators (as does a W2 weight gradient with
+// I % 256 != 0).  A 128 x 128 block-scaled MMA with its two scale copies issues at about half the
+// rate of a 128 x 256 one with its three.  Operands
 // are the E4M3 copies made by the quantiser and the epilogues (quant.cu, the fused epilogues
 // above); in the FP8 x FP4 forward the weights are the quantiser's packed E2M1 copies.
 static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmArgs& a) {
@@ -1269,9 +1271,7 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.out0 = b + L.ypart; a.ld0 = (int)H;
             return run<256, false, true, false, false, EPI_PLAIN, true>(c, ta, tb, a, &tc);
         case GemmKind::WgradDown:
-            // weight gradients keep 128 x 128 tiles with two accumulators: their contraction over an
-            // expert's rows is short, so a drained single accumulator would stall the MMAs, and the
-            // fp32 output stores need the epilogue to overlap the next tile
+            // drained 128 x 256 tiles whose fp32 rows leave through 64-byte-swizzled TMA boxes
             if (!tmap_2d(&ta, b + M.dy_c, 1, H, R, 128) || !tmap_2d(&tb, b + M.hw_c, 1, I, R, 128))
                 return cudaErrorInvalidValue;
             a.m_tiles = (int)(H / 128);
