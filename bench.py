@@ -141,9 +141,10 @@ class ClockSampler:
 # DRAM bytes (read + write) per launch of a kernel, from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum) of the current build on the profile_30b_e32 workload (4096 tokens, 32
 # experts: the 30B layer's per-expert work), scaled x4 to the 128-expert layer, since every size
-# grows with E at equal per-expert work.  The forward gate/up figure is its saving launch (343.5 MB
-# read, 129.0 MB written).  A kernel changed since its capture is left out (null).
-PROFILED_TRAFFIC = {("qwen3_30b_a3b", "gemm_fwd_gate_up_swiglu"): 4 * (343.536e6 + 128.982e6)}
+# grows with E at equal per-expert work.  The forward gate/up figure is its saving launch (344.0 MB
+# read, 128.7 MB written; the build whose epilogue stores w h).  A kernel changed since its capture
+# is left out (null).
+PROFILED_TRAFFIC = {("qwen3_30b_a3b", "gemm_fwd_gate_up_swiglu"): 4 * (343.972e6 + 128.740e6)}
 
 GEMM_FLOPS = {  # algorithmic FLOPs per launch of each grouped GEMM (BF16 or MXFP8), in units of S*H*I
     "gemm_fwd_gate_up_swiglu": 4, "gemm_fwd_gate_up_save": 4, "gemm_fwd_down_weighted": 2,
