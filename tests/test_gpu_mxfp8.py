@@ -30,6 +30,8 @@ SMALL = {
     "medium": mx(gen.custom_config("medium", T=2048, H=512, I=256, E=16, k=4, seed=21)),
     "medium_I384": mx(gen.custom_config("medium_I384", T=1500, H=768, I=384, E=12, k=3, seed=22)),
     "skew_small": mx(gen.custom_config("skew_small", T=1024, H=256, I=128, E=32, k=8, routing="zipf", seed=23)),
+    # k > 32: the token-major row quantiser stores to a token's destinations 32 at a time
+    "wide_k": mx(gen.custom_config("wide_k", T=96, H=256, I=128, E=48, k=36, seed=25)),
 }
 
 

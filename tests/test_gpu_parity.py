@@ -28,6 +28,8 @@ SMALL = {
     # wide I: four n-tiles of the forward gate/up and two of the backward down per m-tile
     "medium_I512": gen.custom_config("medium_I512", T=1024, H=256, I=512, E=8, k=2, seed=24),
     "skew_small": gen.custom_config("skew_small", T=1024, H=256, I=128, E=32, k=8, routing="zipf", seed=23),
+    # k > 32: the token-major gather loads a token's destinations 32 at a time
+    "wide_k": gen.custom_config("wide_k", T=96, H=256, I=128, E=48, k=36, seed=25),
 }
 
 
