@@ -256,3 +256,22 @@ def test_zero_tokens_block_scaled(cuda_lib, precision):
     L.bwd()
     torch.cuda.synchronize()
     assert torch.all(L.dW13 == 0) and torch.all(L.dW2 == 0)
+
+
+@pytest.mark.parametrize("case", ["medium", "empty_experts"])
+def test_backward_bf16_weight_gradients(cuda_lib, case):
+    """A caller may take dW13, dW2 in bf16 (reading 13: the caller's choice of dtype): the drained
+    128 x 256 weight-gradient tiles then store bf16 rows, and experts without rows get zeros."""
+    inp = gen.make_inputs(SMALL["medium"]) if case == "medium" else _edge_inputs("empty_experts", "mxfp8")
+    L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.bfloat16)
+    L.fwd(flags=cuda_lib.MOE_FLAG_SAVE_GU)
+    L.bwd(flags=cuda_lib.MOE_FLAG_REUSE_FWD | cuda_lib.MOE_FLAG_REUSE_WEIGHTS)
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    ref = oracle.backward(inp.f64("dy"), *_args(inp), mxfp8=True)
+    for got, n in ((L.dW13, "dW13"), (L.dW2, "dW2")):
+        assert got.dtype == torch.bfloat16
+        assert rel_fro(f64(got), ref[n]) < TOL, (n, rel_fro(f64(got), ref[n]))
+    if case == "empty_experts":
+        idle = sorted(set(range(inp.cfg.E)) - set(np.unique(inp.topk_idx).tolist()))
+        assert idle and torch.all(L.dW13[idle] == 0) and torch.all(L.dW2[idle] == 0)
