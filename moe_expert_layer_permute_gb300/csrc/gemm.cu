@@ -1066,11 +1066,12 @@ static bool tmap_2d_sw64(CUtensorMap* m, const void* ptr, int esize, uint64_t in
 }
 
 // Two-SM MMAs (256 x 256 per CTA pair, each SM holding half of every B tile) for the BF16 weight
-// gradients and the backward gate/up product, where they measured 6-10% faster on GB300; the
-// forward products and the SwiGLU backward keep one CTA per 128 x 256 tile (a grouped-M pair
-// needs two m-tiles of one expert, and the duplicated odd tiles cancel the gain there).
+// gradients, the backward gate/up product and the SwiGLU backward, where they measured faster on
+// GB300 (the pair's shared-memory ring covers half again as much operand latency); the forward
+// products keep one CTA per 128 x 256 tile (a grouped-M pair needs two m-tiles of one expert, and
+// the duplicated odd tiles cancel the gain there).
 template <int BN, bool MX, bool WGRAD, int EPI>
-constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN); }
+constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN || EPI == EPI_SWIGLU_BWD); }
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
