@@ -1066,12 +1066,14 @@ static bool tmap_2d_sw64(CUtensorMap* m, const void* ptr, int esize, uint64_t in
 }
 
 // Two-SM MMAs (256 x 256 per CTA pair, each SM holding half of every B tile) for the BF16 weight
-// gradients, the backward gate/up product and the SwiGLU backward, where they measured faster on
-// GB300 (the pair's shared-memory ring covers half again as much operand latency); the forward
-// products keep one CTA per 128 x 256 tile (a grouped-M pair needs two m-tiles of one expert, and
-// the duplicated odd tiles cancel the gain there).
+// gradients, the backward gate/up product, the SwiGLU backward and the forward down product, where
+// they measured faster on GB300 (the pair's shared-memory ring covers half again as much operand
+// latency); the forward gate/up keeps one CTA per 128 x 256 tile (a grouped-M pair needs two
+// m-tiles of one expert, and the duplicated odd tiles cancel the gain there).
 template <int BN, bool MX, bool WGRAD, int EPI>
-constexpr bool use_two() { return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN || EPI == EPI_SWIGLU_BWD); }
+constexpr bool use_two() {
+    return !MX && BN == 256 && (WGRAD || EPI == EPI_PLAIN || EPI == EPI_SWIGLU_BWD || EPI == EPI_WEIGHTED);
+}
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool WGRAD, int EPI, bool MX>
 static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
@@ -1153,7 +1155,9 @@ static cudaError_t launch_gemm_bf16(const Ctx& c, GemmKind kind, const void* W, 
                        ? run<256, false, false, true, false, EPI_SWIGLU, false>(c, ta, tb, a, &tc, &td)
                        : run<256, false, false, true, false, EPI_GU_ONLY, false>(c, ta, tb, a, &tc, &td);
         case GemmKind::FwdDown:
-            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) || !tmap_2d(&tb, W, 2, I, E * H, 256) ||
+            // K-major B boxes hold the rows one CTA loads: all 256, or its 128-row half on CTA pairs
+            if (!tmap_2d(&ta, b + L.hid, 2, I, R, 128) ||
+                !tmap_2d(&tb, W, 2, I, E * H, use_two<256, false, false, EPI_WEIGHTED>() ? 128 : 256) ||
                 !tmap_2d(&tc, b + L.ypart, 2, H, R, 32))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(H / 256); a.k_blocks = (int)(I / 64); a.b_rows_e = (int)H;
