@@ -373,6 +373,13 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     // saved [g|u]), so that L2 receives whole lines rather than 16-byte halves of sectors
     constexpr bool kTmaOut = tma_out<EPI, MX, BN>();
     constexpr int kOutBytes = kTmaOut ? kEpiWarps * out_box_bytes<EPI, kSingle>() : 0;
+    // MXFP8 SwiGLU backward: the tile's saved g and u reach shared memory by TMA (tmD, boxes of
+    // 128 rows x 64 columns) in two halves of 64 columns each, issued one tile ahead by the first
+    // epilogue warp, so that the epilogue does not wait on its own global loads
+    constexpr bool kGuSmem = MX && EPI == EPI_SWIGLU_BWD;
+    constexpr int kGuHalfBytes = 2 * kBM * kRowBytes;   // the g box and the u box of one half
+    constexpr int kGuBytes = kGuSmem ? 2 * kGuHalfBytes : 0;
+    static_assert(!kGuSmem || (BN == 128 && !PAIR && kEpiWarps == 8), "two passes of 64 columns, one CTA");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -380,13 +387,16 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     uint8_t* sB = smem + kStages * kATileBytes;
     uint8_t* sSF = sB + kStages * kBTileBytes;           // MXFP8: per stage A atom then B atoms
     uint8_t* sOut = sSF + kStages * kSfBytes;           // TMA-stored outputs: a 4 KB box per epilogue warp
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kOutBytes);
+    uint8_t* sGu = sOut + kOutBytes;                    // MXFP8 SwiGLU backward: saved g, u of a tile
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sGu + kGuBytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
     uint64_t* tfull = bars + 2 * kStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* gu_full = drain + 1;    // [2] a half of the saved g, u has landed
+    uint64_t* gu_free = drain + 3;    // [2] every epilogue warp has read that half
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
     int* s_mtile = reinterpret_cast<int*>(tslot + 4);
     int* s_pair = s_mtile + (a.E + 1);
@@ -412,6 +422,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             mbar_init(tempty + b, (TWO ? 2 : 1) * kEpiWarps);   // one arrival per epilogue warp (TWO: both CTAs')
         }
         mbar_init(drain, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(gu_full + b, 1);
+            mbar_init(gu_free + b, kEpiWarps);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -644,8 +658,28 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         int acc = 0;
         uint32_t acc_phase = 0;
+        // saved g, u of the MXFP8 SwiGLU backward: half p of tile L (rows m0.., columns n0 + 64 p..)
+        // into its shared-memory half, issued by the first epilogue warp's lane 0
+        const bool gu_issuer = kGuSmem && warp == 2 && lane == 0;
+        uint32_t gu_phase = 0;
+        long long gu_issued[2] = {0, 0};
+        auto gu_load = [&](int Ln, int p) {
+            const int m0 = (Ln / a.n_tiles) * kBM, n0 = (Ln % a.n_tiles) * BN + 64 * p;
+            uint8_t* dst = sGu + p * kGuHalfBytes;
+            mbar_arrive_expect_tx(gu_full + p, kGuHalfBytes);
+            tma_load_2d(dst, &tmD, gu_full + p, n0, m0);
+            tma_load_2d(dst + kBM * kRowBytes, &tmD, gu_full + p, a.I + n0, m0);
+            ++gu_issued[p];
+        };
+        if (gu_issuer && unit0 < num_tiles) {
+            gu_load(unit0, 0);
+            gu_load(unit0, 1);
+        }
         for (int L = unit0; L < num_tiles; L += unit_stride) {
             const Tile t = decode_tile<BN, WGRAD, SPLIT, kElems, PAIR>(L, a, s_mtile, s_pair, rank);
+            // MXFP8 SwiGLU backward: the row's routing weight is requested before the accumulator wait
+            int w_slot = -1;
+            if constexpr (kGuSmem) w_slot = a.row_slot[(long long)t.m0 + r];
             // BF16 SwiGLU backward: the thread's first chunk of saved g, u (32 columns each, packed
             // bf16) is requested before the accumulator wait, so that its latency overlaps the wait
             uint4 gnext[4], unext[4];
@@ -900,20 +934,39 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             } else if constexpr (EPI == EPI_SWIGLU_BWD) {
                 // MXFP8: dg, du along 2I and along the rows, and w h along the rows, as E4M3 copies
                 static_assert(MX, "the BF16 SwiGLU backward has its own epilogue above");
-                const int slot = a.row_slot[grow];
-                const float w = slot >= 0 ? a.topk_w[slot] : 0.f;
-                const __nv_bfloat16* gurow = a.gu + grow * (2LL * a.I);
+                const float w = w_slot >= 0 ? a.topk_w[w_slot] : 0.f;
                 float dot = 0.f;
+                bool gu_ok = true;
 #pragma unroll 1
-                for (int c = half; c < BN / 32; c += kHalves) {
+                for (int p = 0; p < 2; ++p) {
+                    // pass p: chunk c = half + 2 p, 32 columns inside shared-memory half p
+                    const int c = half + kHalves * p;
                     float g[32], u[32];
                     const int col = t.n0 + 32 * c;
-                    // the saved g, u are requested first so that their latency overlaps the TMEM load
+                    // (the warp leaves together when any lane's bounded wait gave up)
+                    if (!__all_sync(0xffffffffu, mbar_wait(gu_full + p, gu_phase, abort_flag, a.status, a.wait_limit))) {
+                        gu_ok = false;
+                        break;
+                    }
+                    const uint32_t sg = smem_u32(sGu + p * kGuHalfBytes) + r * kRowBytes;
                     uint4 graw[4], uraw[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        graw[q] = __ldg(reinterpret_cast<const uint4*>(gurow + col) + q);
-                        uraw[q] = __ldg(reinterpret_cast<const uint4*>(gurow + a.I + col) + q);
+                        const uint32_t off = (uint32_t)(((4 * half + q) ^ (r & 7)) << 4);   // 128-byte swizzle
+                        graw[q] = ld_shared_v4(sg + off);
+                        uraw[q] = ld_shared_v4(sg + kBM * kRowBytes + off);
+                    }
+                    // every lane has its g, u in registers: the warp releases its part of the half
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(gu_free + p);
+                    bool issued = true;
+                    if (gu_issuer && L + unit_stride < num_tiles) {
+                        issued = mbar_wait(gu_free + p, gu_phase, abort_flag, a.status, a.wait_limit);
+                        if (issued) gu_load(L + unit_stride, p);
+                    }
+                    if (!__all_sync(0xffffffffu, issued)) {
+                        gu_ok = false;
+                        break;
                     }
                     tmem_ld32(tacc + 32 * c, v);   // dA
 #pragma unroll
@@ -951,6 +1004,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                     quant_col32_warp(u, a.q1 + gi + a.I + col, a.q1_sf, a.I + col, kblk, a.r_atoms);
                     quant_col32_warp(v, a.q2 + grow * (long long)a.I + col, a.q2_sf, col, kblk, a.r_atoms);
                 }
+                gu_phase ^= 1u;
+                if (!gu_ok) break;
                 a.dtw[grow * (2 * a.n_tiles) + 2 * t.nt + half] = dot;
             } else if constexpr (EPI == EPI_PLAIN) {
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out0);
@@ -985,6 +1040,11 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
             if (acc == 0) acc_phase ^= 1u;
         }
         if (kTmaOut && lane == 0) bulk_wait_all();   // the stores are complete before the CTA exits
+        if (gu_issuer) {
+            // every g, u copy issued has landed (bounded) before the CTA exits
+            for (int p = 0; p < 2; ++p)
+                if (gu_issued[p] > 0) drain_wait(gu_full + p, (uint32_t)((gu_issued[p] - 1) & 1));
+        }
     }
     __syncwarp();
     tc_fence_before();
@@ -1086,7 +1146,8 @@ static cudaError_t run(const Ctx& c, const CUtensorMap& ta, const CUtensorMap& t
     const size_t out_bytes = tma_out<EPI, MX, BN>()
                                  ? (size_t)epi_warps<EPI, MX && BN == 256>() * out_box_bytes<EPI, MX && BN == 256>()
                                  : 0;
-    const size_t fixed = 1024 + ring_stages<TWO, MX, BN, WGRAD>() * stage + out_bytes + 256;
+    const size_t gu_bytes = (MX && EPI == EPI_SWIGLU_BWD) ? (size_t)4 * kBM * kRowBytes : 0;
+    const size_t fixed = 1024 + ring_stages<TWO, MX, BN, WGRAD>() * stage + out_bytes + gu_bytes + 256;
     if (tma_out<EPI, MX, BN>() && !tc) return cudaErrorInvalidValue;
     const CUtensorMap& tcm = tc ? *tc : ta;   // kernels without a TMA-stored output never read it
     const CUtensorMap& tdm = td ? *td : tcm;
@@ -1255,7 +1316,9 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.out0 = b + L.ypart; a.ld0 = (int)H;
             return run<256, false, false, false, false, EPI_WEIGHTED, true>(c, ta, tb, a, &tc);
         case GemmKind::BwdDown:
-            if (!tmap_2d(&ta, b + M.dy_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w2_c, 1, I, E * H, 128))
+            // td: the saved [g|u] rows, read by TMA in 128-row x 64-column boxes
+            if (!tmap_2d(&ta, b + M.dy_r, 1, H, R, 128) || !tmap_2d(&tb, b + M.w2_c, 1, I, E * H, 128) ||
+                !tmap_2d(&td, b + L.gu, 2, 2 * I, R, 128))
                 return cudaErrorInvalidValue;
             a.n_tiles = (int)(I / 128); a.k_blocks = (int)(H / 128); a.b_rows_e = (int)H;
             a.sfA = u8(M.dy_r_sf); a.sfA_kt = (int)(H / 128);
@@ -1265,7 +1328,7 @@ static cudaError_t launch_gemm_mx(const Ctx& c, GemmKind kind, void* out, GemmAr
             a.q1 = reinterpret_cast<uint8_t*>(b + M.dg_c); a.q1_sf = reinterpret_cast<uint8_t*>(b + M.dg_c_sf);
             a.q2 = reinterpret_cast<uint8_t*>(b + M.hw_c); a.q2_sf = reinterpret_cast<uint8_t*>(b + M.hw_c_sf);
             a.r_atoms = (int)(R / 128);
-            return run<128, false, true, false, false, EPI_SWIGLU_BWD, true>(c, ta, tb, a);
+            return run<128, false, true, false, false, EPI_SWIGLU_BWD, true>(c, ta, tb, a, nullptr, &td);
         case GemmKind::BwdGateUp:
             if (!tmap_2d(&ta, b + M.dg_r, 1, 2 * I, R, 128) || !tmap_2d(&tb, b + M.w13_c, 1, H, E * 2 * I, 128) ||
                 !tmap_2d_sw64(&tc, b + L.ypart, 2, H, R, 32))
