@@ -438,16 +438,17 @@ __device__ __forceinline__ uint16_t to_e4m3x2(float a, float b) {
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-// 32 values scaled by inv[] (per value) to 32 E4M3 bytes at a 16-byte aligned destination.
+// 32 values scaled by inv[] (per value) to 32 E4M3 bytes at a 32-byte aligned destination.
 __device__ __forceinline__ void store_e4m3x32(uint8_t* dst, const float* v, const float* inv) {
     uint32_t w[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         w[j] = (uint32_t)to_e4m3x2(v[4 * j] * inv[4 * j], v[4 * j + 1] * inv[4 * j + 1]) |
                ((uint32_t)to_e4m3x2(v[4 * j + 2] * inv[4 * j + 2], v[4 * j + 3] * inv[4 * j + 3]) << 16);
-    uint4* d = reinterpret_cast<uint4*>(dst);
-    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    // one 32-byte store (dst is 32-byte aligned: a row's 32-column block of E4M3 codes)
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
 }
 
 // Row block: the thread's 32 consecutive values of one row share one scale.
