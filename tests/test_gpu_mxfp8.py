@@ -35,6 +35,44 @@ SMALL = {
 }
 
 
+@pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
+def test_activation_quantiser_on_hand_built_blocks(cuda_lib, precision):
+    """x and dy made of the weight-quantiser edge blocks (each 32-column row block holds the E4M3
+    midpoints, their bf16 neighbours, saturating values, subnormals and zeros, at scales across
+    the E8M0 range) with zero weights: the dispatched row-blocked and token-blocked copies decode
+    exactly to the oracle's quantise-dequantise, and the padding rows hold zero codes."""
+    import dataclasses
+
+    from test_gpu_quant_edges import _blocks
+    T, H, I, E, k = 192, 512, 128, 6, 2
+    cfg = dataclasses.replace(gen.custom_config("act_edges", T=T, H=H, I=I, E=E, k=k, seed=43), precision=precision)
+    inp = gen.make_inputs(cfg)
+    rng = np.random.default_rng(11)
+    inp.x = _blocks(T * H // 32, "e4m3", rng).reshape(T, H)
+    inp.dy = _blocks(T * H // 32, "e4m3", rng).reshape(T, H)
+    inp.W13 = np.zeros_like(inp.W13)
+    inp.W2 = np.zeros_like(inp.W2)
+    L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
+    L.bwd()
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    R = L.rows()
+    r, prow = _padded_rows(L, inp)
+    used = int(L.view(L.bd.MOE_VIEW_PAD_OFFSETS, torch.int32, (E + 1,)).cpu().numpy()[E])
+    pad = np.setdiff1d(np.arange(used), prow)
+    assert pad.size > 0
+    X = inp.f64("x")[r["perm"] // k]
+    dY = inp.f64("dy")[r["perm"] // k]
+    views = [("x_c", X, "col"), ("dy_r", dY, "row"), ("dy_c", dY, "col")]
+    if precision == "mxfp8":
+        views.append(("x_r", X, "row"))
+    for name, ref, kind in views:
+        q, sf = _mxview(L, name, (R, H))
+        expect = oracle.mx_qdq(ref, axis=1) if kind == "row" else oracle.mx_qdq_segments(ref, r["off"])
+        np.testing.assert_array_equal(decode_mx(q, sf, kind)[prow], expect, err_msg=name)
+        assert not q[pad].any(), name
+
+
 def _args(inp):
     return inp.f64("x"), inp.topk_idx, inp.f64("topk_w"), inp.f64("W13"), inp.f64("W2")
 
@@ -58,8 +96,9 @@ def _mxview(L, name, shape):
     return q, sf
 
 
-def test_quantiser_matches_oracle_bit_exact(cuda_lib):
-    inp = gen.make_inputs(SMALL["medium"])
+@pytest.mark.parametrize("name", ["medium", "medium_I384", "skew_small"])
+def test_quantiser_matches_oracle_bit_exact(cuda_lib, name):
+    inp = gen.make_inputs(SMALL[name])
     cfg = inp.cfg
     L = DeviceLayer(cuda_lib, inp, wgrad_dtype=torch.float32)
     L.bwd()
