@@ -8,19 +8,24 @@
 // products (ic.work analysis, section "从 3.11 倍到 1.32 倍的性能漏斗").  Operands are BF16, or
 // MXFP8 (E4M3 with one E8M0 scale per 32 elements along K) on the block-scaled MMA.
 //
-// One kernel template serves all seven products in both precisions.  Each CTA is persistent (one
+// One kernel template serves all eight products in both precisions.  Each CTA is persistent (one
 // per SM) and walks a static list of 128 x BN output tiles; its warps are specialised:
 //   warp 0      TMA producer: loads 128-byte-deep K slices of A and B (64 bf16 or 128 E4M3
-//               elements) into a 4-stage smem ring (128-byte swizzle), plus for MXFP8 the
-//               512-byte scale-factor atoms of the slice, and counts the bytes on an mbarrier;
+//               elements) into a smem ring of 4 or 6 stages (128-byte swizzle), plus for MXFP8
+//               the 512-byte scale-factor atoms of the slice, and counts the bytes on an mbarrier;
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN; K=16 bf16 or K=32 E4M3,
-//               for MXFP8 after tcgen05.cp of the scale atoms into TMEM) into one of two TMEM
-//               accumulators and releases each smem stage with tcgen05.commit;
-//   warps 2..   epilogue (4 warps, or 8 for the SwiGLU backward): tcgen05.ld the finished
-//               accumulator (one TMEM lane = one row per thread; warp w reads lane quarter w % 4,
-//               and with 8 warps the two warps of a quarter take alternate 32-column chunks),
-//               apply the fused epilogue and store to global memory, then release the
-//               accumulator, so the epilogue of tile i overlaps the MMAs of tile i+1.
+//               for MXFP8 after tcgen05.cp of the scale atoms into TMEM) into a TMEM accumulator
+//               and releases each smem stage with tcgen05.commit;
+//   warps 2..   epilogue (4 or 8 warps): tcgen05.ld the finished accumulator (one TMEM lane = one
+//               row per thread; warp w reads lane quarter w % 4, and with 8 warps the two warps of
+//               a quarter take alternate 32-column chunks), apply the fused epilogue, stage row
+//               blocks in shared memory for TMA stores, and release the accumulator.
+// Accumulators: BF16 and the 128-wide MXFP8 tiles keep two, so the epilogue of tile i overlaps
+// the MMAs of tile i+1; MXFP8 128 x 256 tiles keep one (two would leave no TMEM for the scales),
+// which eight epilogue warps drain to registers before they compute.  The BF16 products with
+// N = 256, except the forward gate/up and the reducing forward down, run on CTA pairs
+// (cta_group::2, M = 256 per pair, each CTA loading its A rows and half of B).  The SwiGLU backward reads the saved g, u of its tile from
+// shared memory (MXFP8: TMA-loaded one tile ahead) or from registers prefetched a chunk ahead (BF16).
 // Routed rows are laid out per expert padded to multiples of 128, so a row tile belongs to one
 // expert and a weight-gradient K slice never crosses into the next expert's rows.
 // Tile lists: "grouped-M" products (forward and data gradients) enumerate
