@@ -181,7 +181,7 @@ def _routed(cfg, idx):
 
 
 @pytest.mark.parametrize("case", ["one_token", "all_on_one_expert", "empty_experts", "single_expert_top1",
-                                  "fewer_rows_than_a_tile"])
+                                  "fewer_rows_than_a_tile", "max_experts"])
 def test_edge_cases(cuda_lib, case):
     if case == "one_token":
         inp = gen.make_inputs(gen.custom_config(T=1, H=256, I=128, E=8, k=2, seed=31))
@@ -194,6 +194,9 @@ def test_edge_cases(cuda_lib, case):
         inp = _routed(cfg, idx)
     elif case == "single_expert_top1":
         inp = gen.make_inputs(gen.custom_config(T=200, H=256, I=128, E=1, k=1, seed=34))
+    elif case == "max_experts":
+        # the largest expert count the layer takes (1024): about four rows per expert, some idle
+        inp = gen.make_inputs(gen.custom_config(T=512, H=256, I=128, E=1024, k=8, seed=38))
     else:
         inp = gen.make_inputs(gen.custom_config(T=20, H=512, I=256, E=4, k=2, seed=35))
     L = DeviceLayer(cuda_lib, inp)
@@ -210,8 +213,8 @@ def test_edge_cases(cuda_lib, case):
             assert torch.all(got == 0), n
         else:
             assert rel_fro(f64(got), ref[n]) < TOL, n
-    if case == "empty_experts":
-        idle = sorted(set(range(16)) - set(np.unique(inp.topk_idx).tolist()))
+    if case in ("empty_experts", "max_experts"):
+        idle = sorted(set(range(inp.cfg.E)) - set(np.unique(inp.topk_idx).tolist()))
         assert torch.all(L.dW13[idle] == 0) and torch.all(L.dW2[idle] == 0)
 
 
