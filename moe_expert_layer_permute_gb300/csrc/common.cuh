@@ -363,34 +363,6 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
     return __bfloat1622float2(v);
 }
-// Stores 32 floats as bf16 (64 contiguous bytes, 16-byte aligned destination).
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 w;
-        w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-        w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-        w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-        w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-        d[q] = w;
-    }
-}
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 w = s[q];
-        float2 a = unpack_bf16x2(w.x), b = unpack_bf16x2(w.y), c = unpack_bf16x2(w.z), d = unpack_bf16x2(w.w);
-        v[8 * q + 0] = a.x; v[8 * q + 1] = a.y; v[8 * q + 2] = b.x; v[8 * q + 3] = b.y;
-        v[8 * q + 4] = c.x; v[8 * q + 5] = c.y; v[8 * q + 6] = d.x; v[8 * q + 7] = d.y;
-    }
-}
-__device__ __forceinline__ void store_f32x32(float* dst, const float* v) {
-    float4* d = reinterpret_cast<float4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
 // 1/x by the hardware's approximate reciprocal (rcp.approx, about 1 ulp; subnormals flushed).
 __device__ __forceinline__ float rcp_approx(float x) {
     float r;

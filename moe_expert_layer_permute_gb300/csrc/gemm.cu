@@ -252,27 +252,22 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // Epilogue of a 128 x 256 MXFP8 tile from registers: d holds columns [128 h, 128 h + 128) of
 // the thread's row.  For the gate/up product these are one [64 gate | 64 up] block of the
-// interleaved weight, i.e. g and u of I-columns [n0 + 64 h, n0 + 64 h + 64).  With TMA, the bf16
-// outputs go through the warp's 2 KB staging box (32 rows from brow, 32 columns at a time).
-template <int BN, int EPI, bool TMA>
+// interleaved weight, i.e. g and u of I-columns [n0 + 64 h, n0 + 64 h + 64).  The bf16 and fp32
+// row outputs go through the warp's 2 KB staging box (32 rows from brow, 64 bytes a row at a time)
+// and leave by TMA store; the E4M3 h of the gate/up product is stored from registers.
+template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& t, long long grow, int h, float* d,
                                                  const CUtensorMap* tmC, const CUtensorMap* tmD, uint8_t* box,
                                                  int lane, int brow) {
     if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
-        __nv_bfloat16* gu = reinterpret_cast<__nv_bfloat16*>(a.out1);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             float* g = d + 32 * c;
             float* u = d + 64 + 32 * c;
             const int col = t.n0 + 64 * h + 32 * c;
             if (EPI == EPI_GU_ONLY || a.save_gu) {
-                if constexpr (TMA) {
-                    box64_emit(tmD, box, lane, g, 1.f, col, brow);
-                    box64_emit(tmD, box, lane, u, 1.f, a.I + col, brow);
-                } else {
-                    store_bf16x32(gu + grow * (2LL * a.I) + col, g);
-                    store_bf16x32(gu + grow * (2LL * a.I) + a.I + col, u);
-                }
+                box64_emit(tmD, box, lane, g, 1.f, col, brow);
+                box64_emit(tmD, box, lane, u, 1.f, a.I + col, brow);
             }
             if constexpr (EPI == EPI_SWIGLU) {
                 float hv[32];
@@ -287,48 +282,27 @@ __device__ __forceinline__ void epilogue_drained(const GemmArgs& a, const Tile& 
             const int slot = a.row_slot[grow];
             w = slot >= 0 ? a.topk_w[slot] : 0.f;
         }
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out0) + grow * (long long)a.ld0 + t.n0 + 128 * h;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            if constexpr (TMA) {
-                box64_emit(tmC, box, lane, d + 32 * c, w, t.n0 + 128 * h + 32 * c, brow);
-            } else {
-                float o[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = w * d[32 * c + j];
-                store_bf16x32(out + 32 * c, o);
-            }
-        }
+        for (int c = 0; c < 4; ++c) box64_emit(tmC, box, lane, d + 32 * c, w, t.n0 + 128 * h + 32 * c, brow);
     } else if constexpr (EPI == EPI_WGRAD) {
         if (t.kb == 0) {   // an expert without rows: a zero gradient
 #pragma unroll
             for (int j = 0; j < 128; ++j) d[j] = 0.f;
         }
-        if constexpr (TMA) {
-            // rows of this expert's block of the weight gradient [E * M, N], whole 64-byte row
-            // segments through the warp's box: 16 fp32 or 32 bf16 columns a store
-            const int orow = t.e * a.m_tiles * kBM + brow;
-            const uint32_t sbox = smem_u32(box);
-            if (a.out_f32) {
+        // rows of this expert's block of the weight gradient [E * M, N], whole 64-byte row
+        // segments through the warp's box: 16 fp32 or 32 bf16 columns a store
+        const int orow = t.e * a.m_tiles * kBM + brow;
+        const uint32_t sbox = smem_u32(box);
+        if (a.out_f32) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    box_acquire(lane);
-                    box64_put_f32x16(sbox, lane, d + 16 * c);
-                    box_store(tmC, box, lane, t.n0 + 128 * h + 16 * c, orow);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) box64_emit(tmC, box, lane, d + 32 * c, 1.f, t.n0 + 128 * h + 32 * c, orow);
+            for (int c = 0; c < 8; ++c) {
+                box_acquire(lane);
+                box64_put_f32x16(sbox, lane, d + 16 * c);
+                box_store(tmC, box, lane, t.n0 + 128 * h + 16 * c, orow);
             }
         } else {
-            const long long off = (long long)t.e * a.out_e_stride + grow * a.ld0 + t.n0 + 128 * h;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (a.out_f32)
-                    store_f32x32(reinterpret_cast<float*>(a.out0) + off + 32 * c, d + 32 * c);
-                else
-                    store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.out0) + off + 32 * c, d + 32 * c);
-            }
+            for (int c = 0; c < 4; ++c) box64_emit(tmC, box, lane, d + 32 * c, 1.f, t.n0 + 128 * h + 32 * c, orow);
         }
     }
 }
@@ -378,6 +352,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
     // saved [g|u]), so that L2 receives whole lines rather than 16-byte halves of sectors
     constexpr bool kTmaOut = tma_out<EPI, MX, BN>();
     constexpr int kOutBytes = kTmaOut ? kEpiWarps * out_box_bytes<EPI, kSingle>() : 0;
+    static_assert(kTmaOut || EPI == EPI_SWIGLU_BWD, "epilogues other than the MXFP8 SwiGLU backward's stage their "
+                                                    "rows for TMA stores");
     // MXFP8 SwiGLU backward: the tile's saved g and u reach shared memory by TMA (tmD, boxes of
     // 128 rows x 64 columns) in two halves of 64 columns each, issued one tile ahead by the first
     // epilogue warp, so that the epilogue does not wait on its own global loads
@@ -715,7 +691,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty + acc);
                 if (t.valid)
-                    epilogue_drained<BN, EPI, kTmaOut>(a, t, grow, half, d, &tmC, &tmD,
+                    epilogue_drained<BN, EPI>(a, t, grow, half, d, &tmC, &tmD,
                                                        sOut + (warp - 2) * out_box_bytes<EPI, kSingle>(), lane,
                                                        t.m0 + 32 * quarter);
                 acc_phase ^= 1u;
@@ -838,41 +814,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                         }
                         box_store(&tmC, box, lane, t.n0 + 64 * b, brow);
                     }
-                }
-            } else if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GU_ONLY) {
-                // columns [0, BN/2) = gate, [BN/2, BN) = up, for I-columns [n0, n0 + BN/2)
-                __nv_bfloat16* hid = reinterpret_cast<__nv_bfloat16*>(a.out0);
-                __nv_bfloat16* gu = reinterpret_cast<__nv_bfloat16*>(a.out1);
-#pragma unroll 1
-                for (int c = half; c < BN / 64; c += kHalves) {
-                    float u[32];
-                    tmem_ld32(tacc + 32 * c, v);
-                    tmem_ld32(tacc + BN / 2 + 32 * c, u);
-                    if (EPI == EPI_GU_ONLY || a.save_gu) {
-                        store_bf16x32(gu + grow * (2LL * a.I) + t.n0 + 32 * c, v);
-                        store_bf16x32(gu + grow * (2LL * a.I) + a.I + t.n0 + 32 * c, u);
-                    }
-                    if constexpr (EPI == EPI_SWIGLU) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = v[j] * sigmoidf_fast(v[j]) * u[j];
-                        const int col = t.n0 + 32 * c;
-                        if constexpr (MX)
-                            quant_row32(v, a.q0 + grow * (long long)a.I + col,
-                                        a.q0_sf + sf_index(grow, col / 32, a.I / 128));
-                        else
-                            store_bf16x32(hid + grow * (long long)a.I + col, v);
-                    }
-                }
-            } else if constexpr (EPI == EPI_WEIGHTED) {
-                const int slot = a.row_slot[grow];
-                const float w = a.w_in_a ? 1.f : (slot >= 0 ? a.topk_w[slot] : 0.f);
-                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out0);
-#pragma unroll 1
-                for (int c = half; c < BN / 32; c += kHalves) {
-                    tmem_ld32(tacc + 32 * c, v);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] *= w;
-                    store_bf16x32(out + grow * (long long)a.ld0 + t.n0 + 32 * c, v);
                 }
             } else if constexpr (EPI == EPI_SWIGLU_BWD && !MX) {
                 // dA -> dg, du per 32-column chunk (w h was saved by the forward); the next chunk's
@@ -1012,28 +953,6 @@ __global__ void __launch_bounds__(gemm_threads<EPI, MX && BN == 256>(), 1)
                 gu_phase ^= 1u;
                 if (!gu_ok) break;
                 a.dtw[grow * (2 * a.n_tiles) + 2 * t.nt + half] = dot;
-            } else if constexpr (EPI == EPI_PLAIN) {
-                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out0);
-#pragma unroll 1
-                for (int c = half; c < BN / 32; c += kHalves) {
-                    tmem_ld32(tacc + 32 * c, v);
-                    store_bf16x32(out + grow * (long long)a.ld0 + t.n0 + 32 * c, v);
-                }
-            } else {  // EPI_WGRAD
-                const long long off = (long long)t.e * a.out_e_stride + grow * a.ld0 + t.n0;
-#pragma unroll 1
-                for (int c = half; c < BN / 32; c += kHalves) {
-                    if (t.kb > 0) {
-                        tmem_ld32(tacc + 32 * c, v);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                    }
-                    if (a.out_f32)
-                        store_f32x32(reinterpret_cast<float*>(a.out0) + off + 32 * c, v);
-                    else
-                        store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.out0) + off + 32 * c, v);
-                }
             }
             tc_fence_before();
             __syncwarp();
